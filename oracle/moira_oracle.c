@@ -1,0 +1,328 @@
+/*
+ * moira_oracle.c -- TEST INFRASTRUCTURE, not part of the product.
+ *
+ * A plain, slow, fp64 CPU restatement of what the MOIRA sparse-decode hot
+ * path computes.  Only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark may load this library; the product path (the CUDA
+ * library) never calls it and shares no code, header or table with it.
+ *
+ * Sources (the method is described only in prose, so every step below is the
+ * plainest reading of that prose; readings are listed beside each function):
+ *   [MOIRA]  "MOIRA: Mass-Oriented Indexing with Ragged Attention for
+ *            Long-Context Decoding" (arXiv 2610.04313), abstract: per request,
+ *            layer, KV head and step, a coverage rule keeps the smallest set
+ *            of KV-cache pages whose *estimated* attention mass reaches a
+ *            fraction gamma; attention then reads only those pages.
+ *   [FFD]    "Faster Flash Decoding" (FFD, arXiv 2609.00097; the page is a
+ *            Chinese translation), section 2 (related work): metadata
+ *            estimators summarise a block by its mean vector (Quest/SparQ);
+ *            section 1 and figure 1: top-p selection needs a global softmax to
+ *            form the cumulative probability.
+ *
+ * The estimator is not fixed by the pages; this oracle and the CUDA library
+ * both use the same stated choice: a page's summary is the mean of its keys,
+ * stored as bf16; its score for query head h is sm_scale * q_h . kbar; the
+ * page mass is the average over the GQA group of the per-head softmax over
+ * the full pages.
+ *
+ * Every floating-point step is fp64; bf16 inputs are widened exactly.
+ * Nothing here is blocked, fused or reordered beyond the definitions.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- bf16 <-> double ---------------------------------------------------- */
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round a double to the nearest bf16 (ties to even), in one rounding step.
+ * bf16 carries 8 significant bits; normal numbers have exponent >= -126 and
+ * below that the spacing stays at 2^-133 (subnormals). */
+static uint16_t double_to_bf16_rne(double x)
+{
+    if (isnan(x)) return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isinf(a)) return sign | 0x7F80;
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e);                 /* a = f * 2^e, f in [0.5, 1) */
+    int unbiased = e - 1;               /* a = 1.xxx * 2^unbiased */
+    int quantum = (unbiased >= -126 ? unbiased : -126) - 7;
+    double r = nearbyint(ldexp(a, -quantum));   /* ties to even */
+    double v = ldexp(r, quantum);               /* exact */
+    if (v > 0x1.FEp127) return sign | 0x7F80;   /* beyond the largest finite bf16 */
+    float fv = (float)v;                        /* exact: v has <= 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &fv, sizeof u);
+    return sign | (uint16_t)(u >> 16);
+}
+
+/* Exposed so the tests can pin the rounding helper on its own. */
+uint16_t oracle_round_bf16(double x) { return double_to_bf16_rne(x); }
+
+/* ---- page summaries ----------------------------------------------------- */
+
+/* Summary of each (page, KV head) block: the mean of its S key vectors
+ * ([FFD] section 2: "mean vectors" as block metadata), summed in fp64 in token
+ * order and rounded once to bf16.
+ *   k_blocks : [n_blocks][S][d] bf16 bit patterns
+ *   summ_out : [n_blocks][d]    bf16 bit patterns */
+void oracle_summaries(const uint16_t *k_blocks, int64_t n_blocks, int32_t S,
+                      int32_t d, uint16_t *summ_out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        for (int32_t i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int32_t t = 0; t < S; ++t)
+                acc += bf16_to_double(k_blocks[((size_t)b * S + t) * d + i]);
+            summ_out[(size_t)b * d + i] = double_to_bf16_rne(acc / (double)S);
+        }
+    }
+}
+
+/* ---- estimated page mass ------------------------------------------------ */
+
+/* Scores and masses for one (request, KV head) unit.
+ *   q_group : [G][d] bf16, the G query heads that share this KV head
+ *   summ    : [F][d] bf16, summaries of the F full pages in logical order
+ *   scores  : [G][F] out (nullable): s_{h,p} = sm_scale * q_h . kbar_p
+ *   mass    : [F] out: m_p = (1/G) sum_h softmax_p(s_{h,.})
+ * The softmax runs over the full pages only (the partial tail page has no
+ * summary until it fills). */
+void oracle_page_mass(const uint16_t *q_group, const uint16_t *summ, int32_t G,
+                      int32_t F, int32_t d, double sm_scale, double *scores,
+                      double *mass)
+{
+    double *s = (double *)malloc(sizeof(double) * (size_t)(F > 0 ? F : 1));
+    for (int32_t p = 0; p < F; ++p) mass[p] = 0.0;
+    for (int32_t h = 0; h < G; ++h) {
+        double smax = -INFINITY;
+        for (int32_t p = 0; p < F; ++p) {
+            double dot = 0.0;
+            for (int32_t i = 0; i < d; ++i)
+                dot += bf16_to_double(q_group[(size_t)h * d + i]) *
+                       bf16_to_double(summ[(size_t)p * d + i]);
+            s[p] = sm_scale * dot;
+            if (scores) scores[(size_t)h * F + p] = s[p];
+            if (s[p] > smax) smax = s[p];
+        }
+        double z = 0.0;
+        for (int32_t p = 0; p < F; ++p) z += exp(s[p] - smax);
+        for (int32_t p = 0; p < F; ++p) mass[p] += exp(s[p] - smax) / z / (double)G;
+    }
+    free(s);
+}
+
+/* ---- coverage rule ------------------------------------------------------ */
+
+typedef struct { double m; int32_t p; } mass_idx;
+
+/* Order of the coverage rule: larger mass first; equal masses by lower
+ * logical page index. */
+static int by_mass_desc_then_index(const void *a, const void *b)
+{
+    const mass_idx *x = (const mass_idx *)a, *y = (const mass_idx *)b;
+    if (x->m > y->m) return -1;
+    if (x->m < y->m) return 1;
+    return (x->p > y->p) - (x->p < y->p);
+}
+
+/* [MOIRA] abstract: keep the smallest set of pages whose estimated mass
+ * reaches gamma.  Sorting by mass and taking the shortest prefix whose running
+ * sum is >= gamma gives a smallest such set (any k pages have no more mass
+ * than the k largest).  gamma >= 1 keeps every page.  If rounding keeps the
+ * running sum below gamma, every page is kept.
+ *   mass      : [F]
+ *   keep      : [F] out, 1 for kept pages
+ *   order     : [F] out (nullable), logical indices in rule order
+ *   cum       : [F] out (nullable), running sums in rule order
+ * Returns the number of kept pages. */
+int32_t oracle_cover(const double *mass, int32_t F, double gamma,
+                     uint8_t *keep, int32_t *order, double *cum)
+{
+    mass_idx *v = (mass_idx *)malloc(sizeof(mass_idx) * (size_t)(F > 0 ? F : 1));
+    for (int32_t p = 0; p < F; ++p) { v[p].m = mass[p]; v[p].p = p; }
+    qsort(v, (size_t)F, sizeof(mass_idx), by_mass_desc_then_index);
+    int32_t k = F;
+    double run = 0.0;
+    for (int32_t i = 0; i < F; ++i) {
+        run += v[i].m;
+        if (order) order[i] = v[i].p;
+        if (cum) cum[i] = run;
+        if (k == F && gamma < 1.0 && run >= gamma) k = i + 1;
+    }
+    for (int32_t p = 0; p < F; ++p) keep[p] = 0;
+    for (int32_t i = 0; i < k; ++i) keep[v[i].p] = 1;
+    free(v);
+    return k;
+}
+
+/* One unit's selection: estimator + coverage + the partial tail page.
+ *   summ_pool : [*][Hkv][d] bf16 summaries by physical page; page_row maps
+ *               logical page p to its physical page
+ *   seq_len   : tokens of the request; F = seq_len / S full pages, and a tail
+ *               page (logical index F) when seq_len % S != 0.  The tail is
+ *               always kept (it has no summary yet) and, being the highest
+ *               logical index, is the last entry.
+ *   list_out  : [F + 1] out, kept logical page indices, ascending
+ *   mass/order/cum : optional [F] outputs as in the functions above
+ * Returns the list length. */
+int32_t oracle_select_unit(const uint16_t *q_group, const uint16_t *summ_pool,
+                           int32_t Hkv, int32_t j, const int32_t *page_row,
+                           int32_t seq_len, int32_t S, int32_t G, int32_t d,
+                           double gamma, double sm_scale, int32_t *list_out,
+                           double *mass_out, int32_t *order_out, double *cum_out)
+{
+    int32_t F = seq_len / S, T = (seq_len % S) != 0;
+    int32_t n = 0;
+    if (gamma >= 1.0 || F == 0) {
+        for (int32_t p = 0; p < F + T; ++p) list_out[n++] = p;
+        return n;
+    }
+    uint16_t *summ = (uint16_t *)calloc((size_t)F * d, sizeof(uint16_t));
+    for (int32_t p = 0; p < F; ++p)
+        memcpy(summ + (size_t)p * d,
+               summ_pool + ((size_t)page_row[p] * Hkv + j) * d, sizeof(uint16_t) * d);
+    double *mass = (double *)malloc(sizeof(double) * (size_t)F);
+    uint8_t *keep = (uint8_t *)malloc((size_t)F);
+    oracle_page_mass(q_group, summ, G, F, d, sm_scale, NULL, mass);
+    oracle_cover(mass, F, gamma, keep, order_out, cum_out);
+    for (int32_t p = 0; p < F; ++p)
+        if (keep[p]) list_out[n++] = p;
+    if (T) list_out[n++] = F;
+    if (mass_out) memcpy(mass_out, mass, sizeof(double) * (size_t)F);
+    free(summ);
+    free(mass);
+    free(keep);
+    return n;
+}
+
+/* ---- exact attention over the kept tokens ------------------------------ */
+
+/* Softmax attention of the G query heads over the tokens of the listed pages.
+ *   k_pool, v_pool : [*][Hkv][S][d] bf16 by physical page; page_row maps
+ *                    logical page p to its physical page
+ *   list           : [len] logical page indices
+ *   seq_len        : page p holds tokens [p*S, min((p+1)*S, seq_len))
+ *   out            : [G][d]; zero when no token is listed */
+void oracle_attend_unit(const uint16_t *q_group, const uint16_t *k_pool,
+                        const uint16_t *v_pool, int32_t Hkv, int32_t j,
+                        const int32_t *page_row, const int32_t *list,
+                        int32_t len, int32_t seq_len, int32_t S, int32_t G,
+                        int32_t d, double sm_scale, double *out)
+{
+    int64_t ntok = 0;
+    for (int32_t e = 0; e < len; ++e) {
+        int64_t lo = (int64_t)list[e] * S, hi = lo + S;
+        if (hi > seq_len) hi = seq_len;
+        if (hi > lo) ntok += hi - lo;
+    }
+    size_t blk = (size_t)S * d;
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(ntok > 0 ? ntok : 1));
+    for (int32_t h = 0; h < G; ++h) {
+        double *o = out + (size_t)h * d;
+        for (int32_t i = 0; i < d; ++i) o[i] = 0.0;
+        if (ntok == 0) continue;
+        double lmax = -INFINITY;
+        int64_t x = 0;
+        for (int32_t e = 0; e < len; ++e) {
+            int64_t p = list[e];
+            const uint16_t *kb = k_pool + ((size_t)page_row[p] * Hkv + j) * blk;
+            for (int32_t t = 0; t < S && p * S + t < seq_len; ++t) {
+                double dot = 0.0;
+                for (int32_t i = 0; i < d; ++i)
+                    dot += bf16_to_double(q_group[(size_t)h * d + i]) *
+                           bf16_to_double(kb[(size_t)t * d + i]);
+                logit[x] = sm_scale * dot;
+                if (logit[x] > lmax) lmax = logit[x];
+                ++x;
+            }
+        }
+        double z = 0.0;
+        x = 0;
+        for (int32_t e = 0; e < len; ++e) {
+            int64_t p = list[e];
+            const uint16_t *vb = v_pool + ((size_t)page_row[p] * Hkv + j) * blk;
+            for (int32_t t = 0; t < S && p * S + t < seq_len; ++t) {
+                double w = exp(logit[x] - lmax);
+                z += w;
+                for (int32_t i = 0; i < d; ++i)
+                    o[i] += w * bf16_to_double(vb[(size_t)t * d + i]);
+                ++x;
+            }
+        }
+        for (int32_t i = 0; i < d; ++i) o[i] /= z;
+    }
+    free(logit);
+}
+
+/* ---- one decode-attention step over a pooled KV cache ------------------ */
+
+/* Selection + attention for n_layers layers of a paged KV cache, every
+ * (layer, request, KV head) unit independently (OpenMP over units).
+ * Layouts (bf16 unless stated):
+ *   q          : [n_layers][B][Hq][d]
+ *   summ       : [n_layers][P][Hkv][d]      summaries of the physical pages
+ *   k_pool     : [n_layers][P][Hkv][S][d], v_pool likewise
+ *   page_table : int32 [B][max_pages], logical -> physical page
+ *   seq_lens   : int32 [B]
+ *   lengths    : int32 out [n_layers][B][Hkv]
+ *   out        : double out [n_layers][B][Hq][d]
+ * Query head h reads KV head h / G (G = Hq / Hkv).
+ * Returns the number of threads used. */
+int32_t oracle_decode_step(const uint16_t *q, const uint16_t *summ,
+                           const uint16_t *k_pool, const uint16_t *v_pool,
+                           const int32_t *page_table, const int32_t *seq_lens,
+                           int32_t n_layers, int32_t B, int32_t Hq, int32_t Hkv,
+                           int32_t d, int32_t S, int64_t P, int32_t max_pages,
+                           double gamma, double sm_scale, int32_t *lengths,
+                           double *out, int32_t n_threads)
+{
+    int32_t G = Hq / Hkv;
+    int64_t units = (int64_t)n_layers * B * Hkv;
+    int32_t used = 1;
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#pragma omp parallel
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+    }
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t u = 0; u < units; ++u) {
+        int32_t l = (int32_t)(u / ((int64_t)B * Hkv));
+        int32_t r = (int32_t)((u / Hkv) % B);
+        int32_t j = (int32_t)(u % Hkv);
+        int32_t L = seq_lens[r];
+        const int32_t *row = page_table + (size_t)r * max_pages;
+        const uint16_t *qg = q + (((size_t)l * B + r) * Hq + (size_t)j * G) * d;
+        size_t lay_pages = (size_t)P * Hkv;
+        int32_t *list = (int32_t *)malloc(sizeof(int32_t) * (size_t)(L / S + 2));
+        int32_t len = oracle_select_unit(qg, summ + (size_t)l * lay_pages * d, Hkv, j,
+                                         row, L, S, G, d, gamma, sm_scale, list,
+                                         NULL, NULL, NULL);
+        lengths[u] = len;
+        oracle_attend_unit(qg, k_pool + (size_t)l * lay_pages * S * d,
+                           v_pool + (size_t)l * lay_pages * S * d, Hkv, j, row,
+                           list, len, L, S, G, d, sm_scale,
+                           out + (((size_t)l * B + r) * Hq + (size_t)j * G) * d);
+        free(list);
+    }
+    return used;
+}
