@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Decode-attention benchmark of the MOIRA sparse-decode library on GB300.
+
+One step = every layer's selection + attention (the library's
+moira_decode_step: score -> select -> attend per layer, 32 layers), captured
+once in a CUDA graph and replayed.  Workload: a single Llama-3-8B-shaped
+request at 131072 tokens (32 layers, 32 query / 8 KV heads, head dim 128,
+16-token pages), seeded synthetic keys with planted high-mass pages.
+
+Printed (rank 0, one JSON line): microseconds per step at gamma = 0.99 and
+the achieved HBM GB/s on the bytes the step must read, next to the same
+library at gamma = 0.98 and at gamma = 1 (dense, the same split-KV kernel
+over every page), the attention kernel's roofline fraction, an end-to-end
+figure through the host-buffer entry point, sampled SM clocks, and the
+fp64 CPU oracle timed on a bounded sample of the same workload.
+
+`--impl reference` times only the oracle (the CPU reference) on the host.
+Under torchrun each rank runs an independent replica (the path has no
+exchange step); the max over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/decode-attn step & achieved HBM GB/s at 128k ctx, γ=0.99 vs γ=1 dense"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x over all ranks (x itself when running alone)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- bytes
+
+def step_bytes(w, lengths: np.ndarray, gamma: float):
+    """Algorithmic bytes of one step: summaries of every full page (gamma < 1),
+    K and V of the listed tokens, q in and fp32 out.  lengths: [L][B][Hkv]."""
+    sp = w.spec
+    d, S = sp.head_dim, sp.page_size
+    L = w.seq_lens.astype(np.int64)
+    F, T = L // S, (L % S != 0).astype(np.int64)
+    tail_tok = L % S
+    per_layer_summ = int(F.sum()) * sp.kv_heads * d * 2 if gamma < 1.0 else 0
+    lens = lengths.astype(np.int64)                                   # [L][B][Hkv]
+    tokens = (lens - T[None, :, None]) * S + (T * tail_tok)[None, :, None]
+    kv = tokens * d * 2 * 2                                           # K + V bf16
+    q_b = sp.batch * sp.q_heads * d * 2
+    o_b = sp.batch * sp.q_heads * d * 4
+    layer = kv.sum(axis=(1, 2)) + per_layer_summ + q_b + o_b          # [L]
+    pages_read = float(lens.sum()) / float((F + T).sum() * sp.kv_heads * sp.layers)
+    return layer, int(layer.sum()), pages_read, {
+        "summaries": per_layer_summ * sp.layers, "kv": int(kv.sum()),
+        "q": q_b * sp.layers, "out": o_b * sp.layers}
+
+
+# --------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(w, layers, gamma):
+    """Host copies of the given layers and the oracle's own summaries."""
+    from oracle import oracle
+    idx = torch.tensor(layers, device=w.k_pool.device)
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    k = u16(w.k_pool.index_select(0, idx))
+    v = u16(w.v_pool.index_select(0, idx))
+    q = u16(w.q.index_select(0, idx))
+    summ = oracle.summaries(k.reshape(-1, 16, 128)).reshape(k.shape[0], k.shape[1], k.shape[2], 128)
+    return q, summ, k, v
+
+
+def time_oracle(w, layers, gamma, threads=0):
+    from oracle import oracle
+    q, summ, k, v = oracle_sample(w, layers, gamma)
+    t0 = time.perf_counter()
+    _, _, used = oracle.decode_step(q, summ, k, v, w.page_table, w.seq_lens, gamma, w.sm_scale,
+                                    n_threads=threads)
+    return time.perf_counter() - t0, used
+
+
+# --------------------------------------------------------------------------- our arm
+
+def capture_step(st, gamma):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        st.step(gamma)                                   # eager warm-up outside capture
+        with torch.cuda.graph(g, stream=s):
+            st.step(gamma)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, steps, warmup, world):
+    for _ in range(warmup):
+        g.replay()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / steps                   # ms per step
+
+
+def time_kernels(st, gamma, layers):
+    """Per-layer CUDA-event timing of select (score + select kernels) and of
+    the attention kernel alone, launched eagerly on the current stream."""
+    stream = torch.cuda.current_stream()
+    sel, att = [], []
+    for l in layers:
+        a0, a1, a2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a0.record(stream)
+        st.select_layer(l, gamma)
+        a1.record(stream)
+        st.attend_layer(l, st.lists, st.lengths[l])
+        a2.record(stream)
+        torch.cuda.synchronize()
+        sel.append(a0.elapsed_time(a1))
+        att.append(a1.elapsed_time(a2))
+    return np.array(sel), np.array(att)
+
+
+def run_ours(args):
+    import sparse_long_context_page_gb300 as moira
+    from sparse_long_context_page_gb300 import workloads as W
+    from sparse_long_context_page_gb300.state import DecodeState
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    moira.load_library()
+    peak, peak_src = hbm_peak()
+    t0 = time.time()
+    over = {"layers": args.layers} if args.layers else {}
+    w = W.make_workload(args.workload, seed=args.seed, device=f"cuda:{local}", **over)
+    st = DecodeState(w)
+    st.summarize()
+    torch.cuda.synchronize()
+    log(f"[bench] workload {args.workload} generated in {time.time() - t0:.1f}s, "
+        f"P={w.num_phys_pages} pages, KV {2 * w.k_pool.numel() * 2 / 2**30:.1f} GiB")
+    sp = w.spec
+    gammas = [float(np.float32(g)) for g in (args.gamma, 0.98, 1.0)]
+    head = gammas[0]
+    results = {}
+    for gm in gammas:
+        g = capture_step(st, gm)
+        clocks = ClockSampler(local) if gm == head else None
+        ms = time_graph(g, args.steps if gm == head else max(3, args.steps // 2), args.warmup, world)
+        clk = clocks.stop() if clocks else None
+        ms = max_over_ranks(ms, world)
+        lengths = st.lengths.cpu().numpy()
+        per_layer, total, frac, parts = step_bytes(w, lengths, gm)
+        results[gm] = dict(ms=ms, bytes=total, frac=frac, parts=parts, per_layer=per_layer,
+                           lengths=lengths, clocks=clk)
+        log(f"[bench] gamma={gm:.4f}: {ms * 1e3:.1f} us/step, {total / ms / 1e6:.0f} GB/s, "
+            f"pages read {frac:.3f}")
+        del g
+    assert moira.read_device_status(st.ws) == 0, "device status word set during the benchmark"
+
+    # dominant kernel: attention, timed per launch at the headline gamma
+    layers = list(range(sp.layers))
+    for _ in range(2):
+        time_kernels(st, head, layers[:4])
+    sel_ms, att_ms = time_kernels(st, head, layers)
+    lengths = st.lengths.cpu().numpy()
+    per_layer, _, _, _ = step_bytes(w, lengths, head)
+    summ_layer = results[head]["parts"]["summaries"] / sp.layers
+    att_bytes = per_layer - summ_layer                    # K/V of kept tokens + q + out
+    att_gbs = float(att_bytes.mean() / (att_ms.mean() * 1e6))
+
+    # end to end: host q in, host out back, through moira_decode_step_host
+    q_host = w.q.cpu().pin_memory()
+    out_host = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
+    q_dev, out_dev = torch.empty_like(w.q), torch.empty_like(st.out)
+
+    def host_step():
+        moira.decode_step_host(st.shape, q_host, q_dev, w.k_pool, w.v_pool, st.summ, st.page_table,
+                               st.seq_lens, head, st.sm_scale, st.lists, st.lengths, out_dev,
+                               out_host, st.ws)
+
+    for _ in range(args.warmup):
+        host_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        host_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    # CPU baseline: the oracle on a bounded sample of the same step (rank 0 only)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n = max(1, min(sp.layers, args.cpu_layers))
+        sample = list(range(n))
+        secs, used = time_oracle(w, sample, head)
+        cpu = {"value": secs / n * sp.layers * 1e6, "unit": "us/step", "cores": used,
+               "kind": "oracle",
+               "sample": f"layers {sample[0]}..{sample[-1]} of {sp.layers} (all 8 KV heads, full "
+                         f"{int(w.seq_lens[0])}-token context) at gamma={head:.2f}; value = "
+                         f"measured seconds x {sp.layers}/{n}; summaries precomputed (off-step)"}
+
+    hd = results[head]
+    dense = results[1.0]
+    launches_per_step = sp.layers * 3
+    line = {
+        "metric": METRIC,
+        "value": round(hd["ms"] * 1e3, 2),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(hd["ms"], 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded q/K/V, keys of 1-5% of pages per (layer, KV head) planted as "
+                "c*qhat+N(0,1) with c~U[0,4] (stands in for RULER at 128k)",
+        "config": {"workload": f"{args.workload}: {sp.batch} request(s) x {int(w.seq_lens.max())} "
+                               f"tokens, {sp.layers} layers, {sp.q_heads} q / {sp.kv_heads} kv heads, "
+                               f"d=128, 16-token pages",
+                   "gamma": round(head, 4), "seed": args.seed,
+                   "l2": "inputs larger than L2 (each step reads >5 GB of K/V)",
+                   "graph": "whole 32-layer step in one CUDA graph, replayed"},
+        "hbm_gbs": round(hd["bytes"] / hd["ms"] / 1e6, 1),
+        "hbm_frac_of_measured": round(hd["bytes"] / hd["ms"] / 1e6 / peak, 4),
+        "hbm_frac_of_8tbs_nominal": round(hd["bytes"] / hd["ms"] / 1e6 / 8000.0, 4),
+        "bytes_per_step": hd["bytes"],
+        "bytes_parts": hd["parts"],
+        "pages_read_fraction": {f"{g:.2f}": round(results[g]["frac"], 4) for g in gammas},
+        "dense": {"gamma": 1.0, "us_per_step": round(dense["ms"] * 1e3, 2),
+                  "hbm_gbs": round(dense["bytes"] / dense["ms"] / 1e6, 1),
+                  "speedup_of_headline": round(dense["ms"] / hd["ms"], 3)},
+        "gamma_0.98": {"us_per_step": round(results[gammas[1]]["ms"] * 1e3, 2),
+                       "hbm_gbs": round(results[gammas[1]]["bytes"] / results[gammas[1]]["ms"] / 1e6, 1),
+                       "speedup_vs_dense": round(dense["ms"] / results[gammas[1]]["ms"], 3)},
+        "per_layer_us": {"select": round(float(sel_ms.mean() * 1e3), 2),
+                         "attend": round(float(att_ms.mean() * 1e3), 2)},
+        "roofline": {"kernel": "k_attend", "bound": "hbm", "achieved": round(att_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(att_gbs / peak, 4),
+                     "peak_source": peak_src, "traffic": None,
+                     "bytes_per_launch": int(att_bytes.mean())},
+        "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "us/step",
+                "h2d_bytes_per_step": int(q_host.numel() * 2),
+                "d2h_bytes_per_step": int(out_host.numel() * 4)},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": hd["clocks"],
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The fp64 oracle on the host cores, one bounded sample per step."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    from sparse_long_context_page_gb300 import workloads as W
+    from oracle import oracle
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = W.make_workload(args.workload, seed=args.seed, device=dev)
+    sp = w.spec
+    head = float(np.float32(args.gamma))
+    times = []
+    used = 1
+    for i in range(args.warmup + args.steps):
+        l = i % sp.layers
+        secs, used = time_oracle(w, [l], head)
+        if i >= args.warmup:
+            times.append(secs * sp.layers)
+    v = float(np.mean(times)) * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/step",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same generator and seed)",
+        "config": {"workload": args.workload, "gamma": round(head, 4), "seed": args.seed},
+        "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": used, "kind": "oracle",
+                         "sample": f"one layer (all KV heads, full context) per step, "
+                                   f"x{sp.layers} for a 32-layer step"},
+        "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b_128k")
+    ap.add_argument("--gamma", type=float, default=0.99)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-layers", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="fewer layers than the workload's (small profiling cases only)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)          # timing rule: at least 3 warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * moira.h -- C ABI of the GB300 (sm_103a) sparse-decode library.
+ *
+ * The library implements the data-parallel hot path of MOIRA-style sparse
+ * decoding described in "MOIRA: Mass-Oriented Indexing with Ragged Attention
+ * for Long-Context Decoding" (arXiv 2610.04313), abstract:
+ *   - for every request, layer, KV head and decode step, a coverage rule keeps
+ *     the smallest set of KV-cache pages whose estimated attention mass
+ *     reaches a fraction gamma                          -> moira_select
+ *   - a self-planning attention kernel reads only those pages; every thread
+ *     block derives its own share of the work from the list lengths, so no
+ *     host-side plan runs and the whole step can live in one CUDA graph
+ *                                                       -> moira_attend
+ *   - the per-page estimate needs per-page metadata; following the
+ *     mean-vector summaries named in "Faster Flash Decoding" (arXiv
+ *     2609.00097), section 2, a page's summary is the bf16 mean of its keys
+ *                                                       -> moira_update_summaries
+ *
+ * Estimator (the pages leave it open; this is the library's stated choice):
+ *   kbar_p   = bf16 round-to-nearest-even of the mean of page p's keys
+ *   s_{h,p}  = sm_scale * q_h . kbar_p            (query head h of the group)
+ *   m_p      = (1/G) * sum_h softmax_p(s_{h,.})   (over the full pages)
+ * Coverage: sort pages by (m_p descending, logical index ascending) and keep
+ * the shortest prefix whose running sum is >= gamma; gamma >= 1 keeps every
+ * page without estimating.  A partial last page (seq_len % page_size != 0)
+ * has no summary yet; it is always kept and is the last list entry.
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the
+ *     caller allocates and owns every buffer.  The library never allocates,
+ *     frees or synchronises inside moira_select / moira_attend /
+ *     moira_decode_step and never reads device data back on the host there,
+ *     so those calls can be captured in a CUDA graph (gamma and sm_scale are
+ *     then fixed at capture time).
+ *   - bf16 tensors are passed as raw pointers to IEEE bfloat16 values.
+ *   - Layouts are dense, row-major, without padding.  Query head h reads KV
+ *     head h / G with G = num_q_heads / num_kv_heads.
+ *   - Host-side argument checks run first; on any error nothing is launched
+ *     and a status other than MOIRA_OK is returned.
+ *   - Problems only visible on the device (a physical page id outside the
+ *     pool, a length out of range, a device wait that ran out) never trap:
+ *     the kernel skips or clamps the offending item and ORs a MOIRA_DEV_* bit
+ *     into the status word kept in the workspace; read it with
+ *     moira_read_device_status().
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).
+ */
+#ifndef MOIRA_H
+#define MOIRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moira_stream_t;   /* identical to cudaStream_t */
+
+typedef enum moira_status {
+    MOIRA_OK = 0,
+    MOIRA_EINVAL = 1,        /* an argument failed a host-side check; nothing launched */
+    MOIRA_EWORKSPACE = 2,    /* workspace NULL, misaligned or smaller than required */
+    MOIRA_ECUDA = 3,         /* a CUDA runtime call or a kernel launch failed */
+    MOIRA_EUNSUPPORTED = 4   /* a shape this build does not implement (see moira_shape) */
+} moira_status;
+
+/* Bits of the device status word (sticky until cleared). */
+#define MOIRA_DEV_BADPAGE 0x1u   /* a page id outside [0, num_phys_pages) was skipped */
+#define MOIRA_DEV_BADLEN  0x2u   /* a seq_len or list length out of range was clamped */
+#define MOIRA_DEV_TIMEOUT 0x4u   /* a bounded device wait ran out; results are invalid */
+
+/* Limits of this build. */
+#define MOIRA_HEAD_DIM 128               /* d */
+#define MOIRA_PAGE_SIZE 16               /* S, tokens per page */
+#define MOIRA_GROUP 4                    /* G = Hq / Hkv */
+#define MOIRA_MAX_PAGES_PER_SEQ 32768    /* max_pages: 512k tokens per request */
+#define MOIRA_MAX_UNITS 4096             /* batch * num_kv_heads */
+
+/* Model / cache geometry.  This build requires head_dim == 128,
+ * page_size == 16 and num_q_heads == 4 * num_kv_heads
+ * (MOIRA_EUNSUPPORTED otherwise). */
+typedef struct moira_shape {
+    int32_t num_q_heads;      /* Hq */
+    int32_t num_kv_heads;     /* Hkv */
+    int32_t head_dim;         /* d */
+    int32_t page_size;        /* S */
+    int64_t num_phys_pages;   /* P: pages in ONE layer's pool */
+} moira_shape;
+
+/* Bytes of device workspace that moira_select / moira_attend /
+ * moira_decode_step need for `batch` requests of at most `max_pages` pages,
+ * on the CURRENT device (the attention grid is sized from its SM count).
+ * Returns 0 if the arguments are invalid.  One workspace may serve every
+ * layer of a step issued in order on one stream; concurrent calls need
+ * separate workspaces. */
+size_t moira_workspace_bytes(const moira_shape *shape, int32_t batch, int32_t max_pages);
+
+/* Zero the workspace (device status word and the self-resetting merge
+ * counters must start at zero).  Call once after allocating it.  Enqueues a
+ * memset on `stream`; returns MOIRA_ECUDA if that fails. */
+moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream_t stream);
+
+/* Page summaries (north-star entry point "moira_update_summaries when a page
+ * fills"; estimator form: mean vectors, "Faster Flash Decoding" section 2).
+ * For each listed physical page p and KV head j:
+ *   summ[p][j][:] = bf16_rne( mean over the S tokens of k_pool[p][j][:][:] ),
+ * accumulated in fp64 so that the mean is rounded once.
+ *   k_pool     : bf16 [P][Hkv][S][d]   one layer's key pool (read)
+ *   summ       : bf16 [P][Hkv][d]      that layer's summaries (written for
+ *                                      the listed pages only)
+ *   phys_pages : int32 [n]             physical page ids; ids outside [0, P)
+ *                                      are skipped (MOIRA_DEV_BADPAGE)
+ * Not part of the decode step: call it when pages fill or after prefill. */
+moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool, void *summ,
+                                    const int32_t *phys_pages, int32_t n, moira_stream_t stream);
+
+/* The coverage rule ("MOIRA" abstract: "a coverage rule keeps the smallest
+ * set of pages whose estimated attention mass reaches a fraction gamma"),
+ * for every (request, KV head) of one layer.
+ *   q          : bf16 [batch][Hq][d]          this layer's queries
+ *   summ       : bf16 [P][Hkv][d]             this layer's page summaries
+ *   page_table : int32 [batch][max_pages]     logical -> physical page
+ *   seq_lens   : int32 [batch]                tokens per request, including
+ *                                             the current one (0 allowed)
+ *   gamma      : (0, 1]; 1 keeps every page (dense) without estimating
+ *   sm_scale   : score scale, normally 1/sqrt(d)
+ *   lists      : int32 [batch][Hkv][max_pages] out: physical ids of the kept
+ *                pages in ascending logical order, the partial tail page (if
+ *                any) last; entries past `lengths` are left untouched
+ *   lengths    : int32 [batch][Hkv] out
+ * Equal masses are taken lower logical index first.  If rounding keeps the
+ * total estimated mass below gamma, every page is kept. */
+moira_status moira_select(const moira_shape *shape, const void *q, const void *summ,
+                          const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                          int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
+                          int32_t *lengths, void *workspace, size_t ws_bytes,
+                          moira_stream_t stream);
+
+/* Self-planning ragged attention ("MOIRA" abstract: "lets each thread block
+ * derive its own share of the work from the list lengths, so the whole
+ * decode step stays inside the CUDA graph").  A fixed grid (a multiple of
+ * the SM count) splits the concatenated lists into equal page ranges; each
+ * block finds its range from a device-side scan of `lengths`, computes
+ * online-softmax partials per list segment, and the last block to finish a
+ * list merges its partials by log-sum-exp (sequence-split decoding,
+ * "Faster Flash Decoding" section 2).
+ *   q          : bf16 [batch][Hq][d]
+ *   k_pool     : bf16 [P][Hkv][S][d]   this layer's keys   (16-byte aligned)
+ *   v_pool     : bf16 [P][Hkv][S][d]   this layer's values (16-byte aligned)
+ *   lists, lengths : as produced by moira_select (any lists that follow the
+ *                same contract are accepted: the last entry of a list holds
+ *                seq_len % S valid tokens when that is non-zero)
+ *   seq_lens   : int32 [batch]
+ *   out        : fp32 [batch][Hq][d] out: softmax(sm_scale q K^T) V over the
+ *                listed tokens; zero for an empty list
+ * Computes in bf16 x bf16 -> fp32 on the tensor cores with fp32 softmax. */
+moira_status moira_attend(const moira_shape *shape, const void *q, const void *k_pool,
+                          const void *v_pool, const int32_t *lists, const int32_t *lengths,
+                          const int32_t *seq_lens, int32_t batch, int32_t max_pages,
+                          float sm_scale, float *out, void *workspace, size_t ws_bytes,
+                          moira_stream_t stream);
+
+/* One whole decode-attention step: for layer l = 0 .. num_layers-1,
+ * moira_select then moira_attend on that layer's slices, in order on one
+ * stream (the per-layer calls above, looped on the host).
+ *   q_all      : bf16 [L][batch][Hq][d]
+ *   k_pool_all, v_pool_all : bf16 [L][P][Hkv][S][d]
+ *   summ_all   : bf16 [L][P][Hkv][d]
+ *   lists      : int32 [batch][Hkv][max_pages]  scratch, reused per layer
+ *   lengths_all: int32 [L][batch][Hkv] out (every layer's list lengths)
+ *   out_all    : fp32 [L][batch][Hq][d] out */
+moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, const void *q_all,
+                               const void *k_pool_all, const void *v_pool_all,
+                               const void *summ_all, const int32_t *page_table,
+                               const int32_t *seq_lens, int32_t batch, int32_t max_pages,
+                               float gamma, float sm_scale, int32_t *lists, int32_t *lengths_all,
+                               float *out_all, void *workspace, size_t ws_bytes,
+                               moira_stream_t stream);
+
+/* The same step with the per-step inputs and outputs in HOST memory:
+ * q_host (bf16 [L][batch][Hq][d]) is copied to the device staging buffer
+ * q_dev, the step runs, and out_dev is copied back to out_host (fp32
+ * [L][batch][Hq][d]).  Copies are cudaMemcpyAsync on `stream` (pinned host
+ * memory makes them asynchronous); the call does not synchronise. */
+moira_status moira_decode_step_host(const moira_shape *shape, int32_t num_layers,
+                                    const void *q_host, void *q_dev, const void *k_pool_all,
+                                    const void *v_pool_all, const void *summ_all,
+                                    const int32_t *page_table, const int32_t *seq_lens,
+                                    int32_t batch, int32_t max_pages, float gamma, float sm_scale,
+                                    int32_t *lists, int32_t *lengths_all, float *out_dev,
+                                    float *out_host, void *workspace, size_t ws_bytes,
+                                    moira_stream_t stream);
+
+/* Synchronise `stream`, copy the device status word (MOIRA_DEV_* bits) to
+ * *status_out (HOST pointer) and clear it when `clear` is non-zero.  A host
+ * call: never issue it while `stream` is being captured. */
+moira_status moira_read_device_status(void *workspace, size_t ws_bytes, uint32_t *status_out,
+                                      int32_t clear, moira_stream_t stream);
+
+/* Thread blocks of the attention grid on the current device (a multiple of
+ * its SM count); a property used by tests and benchmarks. */
+int32_t moira_attend_grid_blocks(void);
+
+/* Static description of a status code. */
+const char *moira_status_string(moira_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOIRA_H */

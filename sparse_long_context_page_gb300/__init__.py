@@ -1,0 +1,21 @@
+"""GB300-native (sm_103a) hot path of MOIRA-style sparse decoding.
+
+MOIRA ("Mass-Oriented Indexing with Ragged Attention for Long-Context
+Decoding", arXiv 2610.04313): per request, layer and KV head, a coverage rule
+keeps the smallest set of KV-cache pages whose estimated attention mass
+reaches gamma, and a self-planning ragged attention kernel reads only those
+pages.  The compute lives in ``libmoira.so`` (hand-written CUDA, C ABI in
+``include/moira.h``); this package only marshals torch tensors into it.
+The library is loaded on first use; there is no CPU fallback.
+"""
+from ._binding import (DEV_BADLEN, DEV_BADPAGE, DEV_TIMEOUT, EXPORTS, GROUP, HEAD_DIM,
+                       MAX_PAGES_PER_SEQ, MAX_UNITS, PAGE_SIZE, MoiraError, Shape, attend,
+                       attend_grid_blocks, decode_step, decode_step_host, library_path,
+                       load_library, make_workspace, read_device_status, select, shape_of,
+                       update_summaries, workspace_bytes, workspace_init)
+
+__all__ = ["DEV_BADLEN", "DEV_BADPAGE", "DEV_TIMEOUT", "EXPORTS", "GROUP", "HEAD_DIM",
+           "MAX_PAGES_PER_SEQ", "MAX_UNITS", "PAGE_SIZE", "MoiraError", "Shape", "attend",
+           "attend_grid_blocks", "decode_step", "decode_step_host", "library_path",
+           "load_library", "make_workspace", "read_device_status", "select", "shape_of",
+           "update_summaries", "workspace_bytes", "workspace_init"]

@@ -1,0 +1,242 @@
+"""ctypes binding over ``libmoira.so`` (argument marshalling only).
+
+Every function takes torch CUDA tensors, checks dtype / device / layout,
+and passes raw pointers plus the current CUDA stream to the C ABI declared in
+``include/moira.h``.  All computation happens in the library's kernels; there
+is no CPU or PyTorch fallback: if the library is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+
+STATUS = {0: "MOIRA_OK", 1: "MOIRA_EINVAL", 2: "MOIRA_EWORKSPACE", 3: "MOIRA_ECUDA",
+          4: "MOIRA_EUNSUPPORTED"}
+DEV_BADPAGE, DEV_BADLEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
+HEAD_DIM, PAGE_SIZE, GROUP = 128, 16, 4
+MAX_PAGES_PER_SEQ, MAX_UNITS = 32768, 4096
+
+# every symbol include/moira.h declares
+EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summaries",
+           "moira_select", "moira_attend", "moira_decode_step", "moira_decode_step_host",
+           "moira_read_device_status", "moira_attend_grid_blocks", "moira_status_string")
+
+
+class MoiraError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} "
+                         f"({_lib.moira_status_string(status).decode() if _lib else ''})")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_phys_pages", ctypes.c_int64)]
+
+    @classmethod
+    def of(cls, num_q_heads, num_kv_heads, num_phys_pages, head_dim=HEAD_DIM, page_size=PAGE_SIZE):
+        return cls(num_q_heads, num_kv_heads, head_dim, page_size, num_phys_pages)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True):
+    """Load libmoira.so (building it in-tree first when it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"{path} is missing; build it with sparse_long_context_page_gb300.build")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    sp = ctypes.POINTER(Shape)
+    lib.moira_workspace_bytes.argtypes = [sp, _i32, _i32]
+    lib.moira_workspace_bytes.restype = ctypes.c_size_t
+    lib.moira_workspace_init.argtypes = [_vp, ctypes.c_size_t, _vp]
+    lib.moira_workspace_init.restype = ctypes.c_int
+    lib.moira_update_summaries.argtypes = [sp, _vp, _vp, _vp, _i32, _vp]
+    lib.moira_update_summaries.restype = ctypes.c_int
+    lib.moira_select.argtypes = [sp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, ctypes.c_float,
+                                 _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.moira_select.restype = ctypes.c_int
+    lib.moira_attend.argtypes = [sp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _vp,
+                                 _vp, ctypes.c_size_t, _vp]
+    lib.moira_attend.restype = ctypes.c_int
+    lib.moira_decode_step.argtypes = [sp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                      ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp,
+                                      ctypes.c_size_t, _vp]
+    lib.moira_decode_step.restype = ctypes.c_int
+    lib.moira_decode_step_host.argtypes = [sp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                           ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
+                                           ctypes.c_size_t, _vp]
+    lib.moira_decode_step_host.restype = ctypes.c_int
+    lib.moira_read_device_status.argtypes = [_vp, ctypes.c_size_t, _u32p, _i32, _vp]
+    lib.moira_read_device_status.restype = ctypes.c_int
+    lib.moira_attend_grid_blocks.argtypes = []
+    lib.moira_attend_grid_blocks.restype = _i32
+    lib.moira_status_string.argtypes = [ctypes.c_int]
+    lib.moira_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise MoiraError(st, what)
+
+
+def _stream(stream=None) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def shape_of(num_q_heads: int, num_kv_heads: int, num_phys_pages: int) -> Shape:
+    return Shape.of(num_q_heads, num_kv_heads, num_phys_pages)
+
+
+def workspace_bytes(shape: Shape, batch: int, max_pages: int) -> int:
+    n = load_library().moira_workspace_bytes(ctypes.byref(shape), batch, max_pages)
+    if n == 0:
+        raise MoiraError(1, "moira_workspace_bytes")
+    return int(n)
+
+
+def make_workspace(shape: Shape, batch: int, max_pages: int, device=None) -> torch.Tensor:
+    """Allocate (through torch) and zero a workspace for these sizes."""
+    n = workspace_bytes(shape, batch, max_pages)
+    ws = torch.empty(n + 256, dtype=torch.uint8, device=device or "cuda")
+    off = (-ws.data_ptr()) % 256
+    ws = ws[off:off + n]
+    workspace_init(ws)
+    return ws
+
+
+def workspace_init(ws: torch.Tensor, stream=None):
+    _check(load_library().moira_workspace_init(_dev(ws, "workspace", torch.uint8), ws.numel(),
+                                               _stream(stream)), "moira_workspace_init")
+
+
+def update_summaries(shape: Shape, k_pool: torch.Tensor, summ: torch.Tensor,
+                     phys_pages: torch.Tensor, stream=None):
+    """summ[p] = bf16 mean of k_pool[p]'s keys for every listed physical page p."""
+    lib = load_library()
+    _check(lib.moira_update_summaries(ctypes.byref(shape), _dev(k_pool, "k_pool", torch.bfloat16),
+                                      _dev(summ, "summ", torch.bfloat16),
+                                      _dev(phys_pages, "phys_pages", torch.int32, 1),
+                                      phys_pages.numel(), _stream(stream)),
+           "moira_update_summaries")
+
+
+def select(shape: Shape, q, summ, page_table, seq_lens, gamma: float, sm_scale: float, lists,
+           lengths, ws, stream=None):
+    """Per-(request, KV head) coverage lists for one layer (see include/moira.h)."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    _check(lib.moira_select(ctypes.byref(shape), _dev(q, "q", torch.bfloat16),
+                            _dev(summ, "summ", torch.bfloat16),
+                            _dev(page_table, "page_table", torch.int32, 2),
+                            _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                            float(gamma), float(sm_scale), _dev(lists, "lists", torch.int32),
+                            _dev(lengths, "lengths", torch.int32), _dev(ws, "workspace", torch.uint8),
+                            ws.numel(), _stream(stream)), "moira_select")
+
+
+def attend(shape: Shape, q, k_pool, v_pool, lists, lengths, seq_lens, max_pages: int,
+           sm_scale: float, out, ws, stream=None):
+    """Attention of one layer over the listed pages; writes fp32 ``out``."""
+    lib = load_library()
+    batch = seq_lens.numel()
+    _check(lib.moira_attend(ctypes.byref(shape), _dev(q, "q", torch.bfloat16),
+                            _dev(k_pool, "k_pool", torch.bfloat16), _dev(v_pool, "v_pool", torch.bfloat16),
+                            _dev(lists, "lists", torch.int32), _dev(lengths, "lengths", torch.int32),
+                            _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                            float(sm_scale), _dev(out, "out", torch.float32),
+                            _dev(ws, "workspace", torch.uint8), ws.numel(), _stream(stream)),
+           "moira_attend")
+
+
+def decode_step(shape: Shape, q_all, k_pool_all, v_pool_all, summ_all, page_table, seq_lens,
+                gamma: float, sm_scale: float, lists, lengths_all, out_all, ws, stream=None):
+    """select + attend for every layer, in order on one stream."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    _check(lib.moira_decode_step(ctypes.byref(shape), q_all.shape[0],
+                                 _dev(q_all, "q_all", torch.bfloat16),
+                                 _dev(k_pool_all, "k_pool_all", torch.bfloat16),
+                                 _dev(v_pool_all, "v_pool_all", torch.bfloat16),
+                                 _dev(summ_all, "summ_all", torch.bfloat16),
+                                 _dev(page_table, "page_table", torch.int32, 2),
+                                 _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                                 float(gamma), float(sm_scale), _dev(lists, "lists", torch.int32),
+                                 _dev(lengths_all, "lengths_all", torch.int32),
+                                 _dev(out_all, "out_all", torch.float32),
+                                 _dev(ws, "workspace", torch.uint8), ws.numel(), _stream(stream)),
+           "moira_decode_step")
+
+
+def decode_step_host(shape: Shape, q_host, q_dev, k_pool_all, v_pool_all, summ_all, page_table,
+                     seq_lens, gamma: float, sm_scale: float, lists, lengths_all, out_dev,
+                     out_host, ws, stream=None):
+    """The step with q read from and out written to HOST (pinned) tensors."""
+    lib = load_library()
+    for t, nm in ((q_host, "q_host"), (out_host, "out_host")):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous host tensor")
+    if q_host.dtype != torch.bfloat16 or out_host.dtype != torch.float32:
+        raise TypeError("q_host must be bf16 and out_host fp32")
+    batch, max_pages = page_table.shape
+    _check(lib.moira_decode_step_host(ctypes.byref(shape), q_host.shape[0], q_host.data_ptr(),
+                                      _dev(q_dev, "q_dev", torch.bfloat16),
+                                      _dev(k_pool_all, "k_pool_all", torch.bfloat16),
+                                      _dev(v_pool_all, "v_pool_all", torch.bfloat16),
+                                      _dev(summ_all, "summ_all", torch.bfloat16),
+                                      _dev(page_table, "page_table", torch.int32, 2),
+                                      _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                                      float(gamma), float(sm_scale),
+                                      _dev(lists, "lists", torch.int32),
+                                      _dev(lengths_all, "lengths_all", torch.int32),
+                                      _dev(out_dev, "out_dev", torch.float32), out_host.data_ptr(),
+                                      _dev(ws, "workspace", torch.uint8), ws.numel(),
+                                      _stream(stream)), "moira_decode_step_host")
+
+
+def read_device_status(ws, clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the MOIRA_DEV_* bits (host call)."""
+    lib = load_library()
+    out = ctypes.c_uint32(0)
+    _check(lib.moira_read_device_status(_dev(ws, "workspace", torch.uint8), ws.numel(),
+                                        ctypes.byref(out), 1 if clear else 0, _stream(stream)),
+           "moira_read_device_status")
+    return int(out.value)
+
+
+def attend_grid_blocks() -> int:
+    return int(load_library().moira_attend_grid_blocks())

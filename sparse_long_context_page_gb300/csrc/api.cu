@@ -1,0 +1,318 @@
+// C ABI of the sparse-decode library: host-side argument checks, workspace
+// carving, TMA descriptor encoding and kernel launches.  Nothing here
+// allocates, synchronises or reads device memory inside select/attend/step.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/moira.h"
+#include "moira_device.cuh"
+#include "moira_launch.h"
+
+using namespace moira;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int current_sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+
+int attend_blocks() { return current_sm_count() * attend_blocks_per_sm(); }
+
+moira_status check_shape(const moira_shape *s)
+{
+    if (!s) return MOIRA_EINVAL;
+    if (s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->head_dim <= 0 || s->page_size <= 0 ||
+        s->num_phys_pages <= 0)
+        return MOIRA_EINVAL;
+    if (s->num_q_heads % s->num_kv_heads != 0) return MOIRA_EINVAL;
+    if (s->head_dim != kHeadDim || s->page_size != kPageSize) return MOIRA_EUNSUPPORTED;
+    if (s->num_q_heads / s->num_kv_heads != kGroup) return MOIRA_EUNSUPPORTED;
+    if (32 % s->num_kv_heads != 0) return MOIRA_EUNSUPPORTED;       // Hkv in {1, 2, 4, 8}
+    // TMA row coordinates are 32-bit: P * Hkv * S rows per layer pool.
+    if (s->num_phys_pages * s->num_kv_heads * kPageSize >= (1LL << 31)) return MOIRA_EUNSUPPORTED;
+    return MOIRA_OK;
+}
+
+moira_status check_batch(const moira_shape *s, int32_t batch, int32_t max_pages)
+{
+    if (batch <= 0 || max_pages <= 0) return MOIRA_EINVAL;
+    if (max_pages > kMaxPagesPerSeq) return MOIRA_EUNSUPPORTED;
+    if (static_cast<long long>(batch) * s->num_kv_heads > kMaxUnits) return MOIRA_EUNSUPPORTED;
+    return MOIRA_OK;
+}
+
+WsLayout layout_for(const moira_shape *s, int32_t batch, int32_t max_pages)
+{
+    return ws_layout(batch, s->num_q_heads, max_pages, batch * s->num_kv_heads, attend_blocks());
+}
+
+moira_status check_ws(const moira_shape *s, int32_t batch, int32_t max_pages, void *ws, size_t bytes)
+{
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOIRA_EWORKSPACE;
+    if (bytes < layout_for(s, batch, max_pages).total) return MOIRA_EWORKSPACE;
+    return MOIRA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// One layer's pool viewed as a 2-D bf16 tensor [P * Hkv * S rows][d], loaded
+// in boxes of 16 rows x 64 elements (128 bytes) with the 128-byte swizzle.
+bool make_pool_map(CUtensorMap *map, const void *pool, const moira_shape *s)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim),
+                          static_cast<cuuint64_t>(s->num_phys_pages) * s->num_kv_heads * kPageSize};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPageSize)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+moira_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOIRA_OK : MOIRA_ECUDA; }
+
+moira_status select_impl(const moira_shape *shape, const void *q, const void *summ,
+                         const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                         int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
+                         int32_t *lengths, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const WsLayout L = layout_for(shape, batch, max_pages);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
+    float *scores = reinterpret_cast<float *>(w + L.scores);
+    float *chunks = reinterpret_cast<float *>(w + L.chunks);
+    const bool dense = gamma >= 1.0f;
+    // gamma on the 2^-31 fixed-point grid of the mass histograms, rounded up
+    const unsigned long long gfx =
+        dense ? 0ull : static_cast<unsigned long long>(std::ceil(static_cast<double>(gamma) * 0x1p31));
+    if (!dense) {
+        const float scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+        cudaError_t e = launch_score(q, summ, page_table, seq_lens, batch, shape->num_q_heads,
+                                     shape->num_kv_heads, max_pages, shape->num_phys_pages,
+                                     scale_log2, scores, chunks, status, stream);
+        if (e != cudaSuccess) return MOIRA_ECUDA;
+    }
+    return cuda_status(launch_select(scores, chunks, page_table, seq_lens, batch,
+                                     shape->num_q_heads, shape->num_kv_heads, max_pages,
+                                     shape->num_phys_pages, gfx, dense, lists, lengths, status,
+                                     stream));
+}
+
+moira_status attend_impl(const moira_shape *shape, const void *q, const void *k_pool,
+                         const void *v_pool, const int32_t *lists, const int32_t *lengths,
+                         const int32_t *seq_lens, int32_t batch, int32_t max_pages, float sm_scale,
+                         float *out, void *ws, size_t ws_bytes, cudaStream_t stream)
+{
+    const WsLayout L = layout_for(shape, batch, max_pages);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    CUtensorMap mk, mv;
+    if (!make_pool_map(&mk, k_pool, shape) || !make_pool_map(&mv, v_pool, shape)) return MOIRA_ECUDA;
+    AttendArgs a;
+    a.q = q;
+    a.lists = lists;
+    a.lengths = lengths;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.partials = reinterpret_cast<float *>(w + L.partials);
+    a.counters = reinterpret_cast<uint32_t *>(w + L.counters);
+    a.status = reinterpret_cast<uint32_t *>(w + L.status);
+    a.hq = shape->num_q_heads;
+    a.hkv = shape->num_kv_heads;
+    a.units = batch * shape->num_kv_heads;
+    a.max_pages = max_pages;
+    a.num_pages = shape->num_phys_pages;
+    a.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    return cuda_status(launch_attend(mk, mv, a, attend_blocks(), stream));
+}
+
+bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
+
+}  // namespace
+
+extern "C" {
+
+size_t moira_workspace_bytes(const moira_shape *shape, int32_t batch, int32_t max_pages)
+{
+    if (check_shape(shape) != MOIRA_OK || check_batch(shape, batch, max_pages) != MOIRA_OK) return 0;
+    if (attend_blocks() <= 0) return 0;
+    return layout_for(shape, batch, max_pages).total;
+}
+
+moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream_t stream)
+{
+    if (!workspace || ws_bytes == 0) return MOIRA_EWORKSPACE;
+    return cuda_status(cudaMemsetAsync(workspace, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool, void *summ,
+                                    const int32_t *phys_pages, int32_t n, moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if (n < 0 || (n > 0 && (!k_pool || !summ || !phys_pages))) return MOIRA_EINVAL;
+    if (n == 0) return MOIRA_OK;
+    if (!aligned16(k_pool) || !aligned16(summ)) return MOIRA_EINVAL;
+    // This call takes no workspace, so there is no status word: page ids out
+    // of range are skipped without a record (select and attend flag them).
+    return cuda_status(launch_summarize(k_pool, summ, phys_pages, n, shape->num_kv_heads,
+                                        shape->num_phys_pages, nullptr,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moira_status moira_select(const moira_shape *shape, const void *q, const void *summ,
+                          const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                          int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
+                          int32_t *lengths, void *workspace, size_t ws_bytes, moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (!(gamma > 0.f && gamma <= 1.f) || !finite_pos(sm_scale)) return MOIRA_EINVAL;
+    if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
+    if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
+    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
+    return select_impl(shape, q, summ, page_table, seq_lens, batch, max_pages, gamma, sm_scale,
+                       lists, lengths, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moira_status moira_attend(const moira_shape *shape, const void *q, const void *k_pool,
+                          const void *v_pool, const int32_t *lists, const int32_t *lengths,
+                          const int32_t *seq_lens, int32_t batch, int32_t max_pages,
+                          float sm_scale, float *out, void *workspace, size_t ws_bytes,
+                          moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (!finite_pos(sm_scale)) return MOIRA_EINVAL;
+    if (!q || !k_pool || !v_pool || !lists || !lengths || !seq_lens || !out) return MOIRA_EINVAL;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return MOIRA_EINVAL;
+    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
+    return attend_impl(shape, q, k_pool, v_pool, lists, lengths, seq_lens, batch, max_pages,
+                       sm_scale, out, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, const void *q_all,
+                               const void *k_pool_all, const void *v_pool_all,
+                               const void *summ_all, const int32_t *page_table,
+                               const int32_t *seq_lens, int32_t batch, int32_t max_pages,
+                               float gamma, float sm_scale, int32_t *lists, int32_t *lengths_all,
+                               float *out_all, void *workspace, size_t ws_bytes,
+                               moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (num_layers <= 0) return MOIRA_EINVAL;
+    if (!(gamma > 0.f && gamma <= 1.f) || !finite_pos(sm_scale)) return MOIRA_EINVAL;
+    if (!q_all || !k_pool_all || !v_pool_all || !summ_all || !page_table || !seq_lens || !lists ||
+        !lengths_all || !out_all)
+        return MOIRA_EINVAL;
+    if (!aligned16(q_all) || !aligned16(k_pool_all) || !aligned16(v_pool_all) ||
+        !aligned16(summ_all) || !aligned16(out_all))
+        return MOIRA_EINVAL;
+    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t d = kHeadDim;
+    const size_t q_layer = static_cast<size_t>(batch) * shape->num_q_heads * d;      // elements
+    const size_t kv_layer = static_cast<size_t>(shape->num_phys_pages) * shape->num_kv_heads * kPageSize * d;
+    const size_t sm_layer = static_cast<size_t>(shape->num_phys_pages) * shape->num_kv_heads * d;
+    const size_t len_layer = static_cast<size_t>(batch) * shape->num_kv_heads;
+    const uint16_t *q = static_cast<const uint16_t *>(q_all);
+    const uint16_t *kp = static_cast<const uint16_t *>(k_pool_all);
+    const uint16_t *vp = static_cast<const uint16_t *>(v_pool_all);
+    const uint16_t *sp = static_cast<const uint16_t *>(summ_all);
+    for (int l = 0; l < num_layers; ++l) {
+        st = select_impl(shape, q + l * q_layer, sp + l * sm_layer, page_table, seq_lens, batch,
+                         max_pages, gamma, sm_scale, lists, lengths_all + l * len_layer, workspace,
+                         ws_bytes, s);
+        if (st != MOIRA_OK) return st;
+        st = attend_impl(shape, q + l * q_layer, kp + l * kv_layer, vp + l * kv_layer, lists,
+                         lengths_all + l * len_layer, seq_lens, batch, max_pages, sm_scale,
+                         out_all + l * q_layer, workspace, ws_bytes, s);
+        if (st != MOIRA_OK) return st;
+    }
+    return MOIRA_OK;
+}
+
+moira_status moira_decode_step_host(const moira_shape *shape, int32_t num_layers,
+                                    const void *q_host, void *q_dev, const void *k_pool_all,
+                                    const void *v_pool_all, const void *summ_all,
+                                    const int32_t *page_table, const int32_t *seq_lens,
+                                    int32_t batch, int32_t max_pages, float gamma, float sm_scale,
+                                    int32_t *lists, int32_t *lengths_all, float *out_dev,
+                                    float *out_host, void *workspace, size_t ws_bytes,
+                                    moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (num_layers <= 0 || !q_host || !out_host || !q_dev || !out_dev) return MOIRA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const size_t n = static_cast<size_t>(num_layers) * batch * shape->num_q_heads * kHeadDim;
+    if (cudaMemcpyAsync(q_dev, q_host, n * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOIRA_ECUDA;
+    st = moira_decode_step(shape, num_layers, q_dev, k_pool_all, v_pool_all, summ_all, page_table,
+                           seq_lens, batch, max_pages, gamma, sm_scale, lists, lengths_all, out_dev,
+                           workspace, ws_bytes, stream);
+    if (st != MOIRA_OK) return st;
+    return cuda_status(cudaMemcpyAsync(out_host, out_dev, n * 4, cudaMemcpyDeviceToHost, s));
+}
+
+moira_status moira_read_device_status(void *workspace, size_t ws_bytes, uint32_t *status_out,
+                                      int32_t clear, moira_stream_t stream)
+{
+    if (!workspace || ws_bytes < 256) return MOIRA_EWORKSPACE;
+    if (!status_out) return MOIRA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOIRA_ECUDA;
+    if (cudaMemcpy(status_out, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MOIRA_ECUDA;
+    if (clear) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return MOIRA_ECUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOIRA_ECUDA;
+    }
+    return MOIRA_OK;
+}
+
+int32_t moira_attend_grid_blocks(void) { return attend_blocks(); }
+
+const char *moira_status_string(moira_status status)
+{
+    switch (status) {
+    case MOIRA_OK: return "ok";
+    case MOIRA_EINVAL: return "invalid argument";
+    case MOIRA_EWORKSPACE: return "workspace missing, misaligned or too small";
+    case MOIRA_ECUDA: return "CUDA runtime error";
+    case MOIRA_EUNSUPPORTED: return "shape not supported by this build";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,457 @@
+// Self-planning ragged paged attention ("MOIRA: Mass-Oriented Indexing with
+// Ragged Attention for Long-Context Decoding", abstract: "each thread block
+// derive[s] its own share of the work from the list lengths, so the whole
+// decode step stays inside the CUDA graph"), with sequence-split partials
+// merged by log-sum-exp (FlashDecoding, "Faster Flash Decoding" section 2).
+//
+// Work plan, computed by every block from device data only:
+//   W = sum of the list lengths (block-wide scan of `lengths` in shared
+//   memory); n = min(grid, W) active blocks; block b takes pages
+//   [b*W/n, (b+1)*W/n) of the lists laid end to end and splits its range at
+//   list boundaries into segments.  A segment's partial goes to slot b + u
+//   (u = list index), which is unique.  The last block to finish a list
+//   (arrival counter, self-resetting) merges that list's partials; a list
+//   held by one block is written directly.
+//
+// Data path per block (1 producer warp + 4 consumer warps, 2 blocks per SM):
+//   the producer looks up a batch of 32 list entries while it issues the
+//   previous batch, and issues 2-D TMA tensor loads of each kept page's K and
+//   V blocks (16 tokens x 128 dims bf16 = 4 KB each, two 128-byte-swizzled
+//   boxes per block) into a 12-slot (8 for very large batches) ring tracked
+//   by mbarriers, i.e. up to 192 KB in flight per SM; consumer warp w takes
+//   pages w, w+4, ... of the block's range.  The G = 4 query heads of
+//   the KV head share every page load:
+//     S^T[h][t] = q_h . k_t   : mma.m16n8k16, A = q (rows 0-3 and 4-7 both
+//                               hold the 4 heads), B = K^T via ldmatrix
+//     O^T[d][n] += V^T P^T    : mma.m16n8k16, A = V^T via ldmatrix.trans,
+//                               B columns 0-3 = bf16(P), columns 4-7 = the
+//                               bf16 residual P - bf16(P), so P enters the
+//                               product with ~16 significant bits
+//   with an fp32 online softmax in the log2 domain.
+#include "moira_device.cuh"
+#include "moira_launch.h"
+
+namespace moira {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kAttThreads = (kConsumerWarps + 1) * 32;
+constexpr int kSlotBytes = 2 * kPageSize * kHeadDim * 2;          // K + V block, 8 KB
+constexpr int kHalfBox = kPageSize * 64 * 2;                        // 16 rows x 128 B
+constexpr int kBlocksPerSm = 2;
+constexpr int kDeepSlots = 12, kShallowSlots = 8;
+constexpr int kDeepMaxUnits = 1024;       // s_off of the deep ring must leave room for 2 blocks/SM
+
+template <int NS>
+struct AttendSmem {
+    float co[kConsumerWarps][kGroup][kHeadDim];
+    float cm[kConsumerWarps][kGroup];
+    float cl[kConsumerWarps][kGroup];
+    unsigned long long full[NS];
+    unsigned long long empty[NS];
+    int2 meta[NS];            // (unit, valid tokens; 0 = skip)
+    int flag;
+    int pad[3];
+};
+
+template <int NS>
+__host__ __device__ inline size_t attend_smem_bytes(int units)
+{
+    return 1024 + static_cast<size_t>(NS) * kSlotBytes + sizeof(AttendSmem<NS>) +
+           sizeof(int) * static_cast<size_t>(units + 1);
+}
+
+// Largest b with floor(b*W/n) <= g: the block whose range holds page g.
+__device__ __forceinline__ int block_of(long long g, long long W, long long n)
+{
+    return static_cast<int>(((g + 1) * n - 1) / W);
+}
+
+template <int kSlots>
+__global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
+    k_attend(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+             const AttendArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *stage = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    AttendSmem<kSlots> &sm = *reinterpret_cast<AttendSmem<kSlots> *>(stage + kSlots * kSlotBytes);
+    int *s_off = reinterpret_cast<int *>(&sm + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int units = a.units;
+
+    if (tid == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(smem_u32(&sm.full[s]), 1);
+            mbar_init(smem_u32(&sm.empty[s]), 1);
+        }
+        mbar_fence_init();
+    }
+    if (warp == kConsumerWarps && lane == 0) {
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+    }
+    pdl_trigger();
+    pdl_wait();                               // lists and lengths come from k_select
+
+    // ---- self-planning: exclusive scan of the list lengths -----------------
+    {
+        const int per = (units + kAttThreads - 1) / kAttThreads;
+        const int ub = min(units, tid * per), ue = min(units, ub + per);
+        int mine = 0;
+        bool bad = false;
+        for (int u = ub; u < ue; ++u) {
+            int len = a.lengths[u];
+            if (len < 0 || len > a.max_pages) {
+                bad = true;
+                len = len < 0 ? 0 : a.max_pages;
+            }
+            mine += len;
+        }
+        if (bad) raise_status(a.status, kDevBadLen);
+        int x = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __shared__ int s_wsum[kConsumerWarps + 1];
+        if (lane == 31) s_wsum[warp] = x;
+        __syncthreads();
+        int off = 0;
+        for (int w = 0; w < warp; ++w) off += s_wsum[w];
+        int run = off + x - mine;
+        for (int u = ub; u < ue; ++u) {
+            s_off[u] = run;
+            int len = a.lengths[u];
+            run += len < 0 ? 0 : (len > a.max_pages ? a.max_pages : len);
+        }
+        if (tid == kAttThreads - 1) s_off[units] = run;
+    }
+    __syncthreads();
+
+    const long long W = s_off[units];
+    const long long n = min(static_cast<long long>(gridDim.x), W);
+    const int b = blockIdx.x;
+    const long long g0 = b < n ? b * W / n : 0;
+    const long long g1 = b < n ? (b + 1) * W / n : 0;
+
+    if (warp == kConsumerWarps) {
+        // ===================== producer warp =====================
+        // Lane i resolves page base+i of a batch of 32: its list, physical id
+        // and valid-token count.  The next batch's lookups are in flight while
+        // the current batch's copies are issued, so list reads do not stall
+        // the ring.
+        auto lookup = [&](long long k, int &u, int &ntok, int &pid) {
+            u = 0;
+            ntok = 0;
+            pid = 0;
+            if (k >= g1) return;
+            int lo = 0, hi = units;                     // largest u with s_off[u] <= k
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_off[mid] <= k) lo = mid; else hi = mid;
+            }
+            u = lo;
+            const int i = static_cast<int>(k - s_off[u]);
+            const int len = s_off[u + 1] - s_off[u];
+            pid = a.lists[static_cast<size_t>(u) * a.max_pages + i];
+            int L = a.seq_lens[u / a.hkv];
+            L = L < 0 ? 0 : (L > a.max_pages * kPageSize ? a.max_pages * kPageSize : L);
+            const int tail = L % kPageSize;
+            ntok = (i == len - 1 && tail) ? tail : kPageSize;
+        };
+        int cu, cn, cp;
+        lookup(g0 + lane, cu, cn, cp);
+        for (long long base = g0; base < g1; base += 32) {
+            int nu, nn, np;
+            lookup(base + 32 + lane, nu, nn, np);
+            if (cn > 0 && (cp < 0 || cp >= a.num_pages)) {
+                cn = 0;
+                raise_status(a.status, kDevBadPage);
+            }
+            const int cnt = static_cast<int>(min(32LL, g1 - base));
+            for (int qi = 0; qi < cnt; ++qi) {
+                if (lane == qi) {
+                    const long long idx = base + qi - g0;
+                    const int slot = static_cast<int>(idx % kSlots);
+                    const uint32_t round = static_cast<uint32_t>(idx / kSlots);
+                    if (!mbar_wait(smem_u32(&sm.empty[slot]), (round & 1u) ^ 1u))
+                        raise_status(a.status, kDevTimeout);
+                    sm.meta[slot] = make_int2(cu, cn);
+                    const uint32_t full = smem_u32(&sm.full[slot]);
+                    if (cn > 0) {
+                        const uint32_t dst = smem_u32(stage + slot * kSlotBytes);
+                        const int row = (cp * a.hkv + cu % a.hkv) * kPageSize;
+                        mbar_arrive_expect_tx(full, kSlotBytes);
+                        tma_load_2d(dst, &tmap_k, 0, row, full);
+                        tma_load_2d(dst + kHalfBox, &tmap_k, 64, row, full);
+                        tma_load_2d(dst + 2 * kHalfBox, &tmap_v, 0, row, full);
+                        tma_load_2d(dst + 3 * kHalfBox, &tmap_v, 64, row, full);
+                    } else {
+                        mbar_arrive(full);
+                    }
+                }
+                __syncwarp();
+            }
+            cu = nu;
+            cn = nn;
+            cp = np;
+        }
+        return;
+    }
+
+    // ===================== consumer warps =====================
+    // empty lists produce zeros (no block would otherwise touch them)
+    if (b == 0) {
+        for (int u = 0; u < units; ++u) {
+            if (s_off[u + 1] != s_off[u]) continue;
+            const int r = u / a.hkv, j = u % a.hkv;
+            for (int e = tid; e < kGroup * kHeadDim; e += kConsumerWarps * 32)
+                a.out[(static_cast<size_t>(r) * a.hq + j * kGroup) * kHeadDim + e] = 0.f;
+        }
+    }
+    if (g0 >= g1) return;
+
+    // this lane's row head in the S^T fragments and its two output columns
+    const int hq_row = (lane >> 2) & 3;
+    const int tq = 2 * (lane & 3);
+    const int hn0 = (2 * (lane & 3)) & 3;
+    const bool lo_lane = lane >= 16;      // holds the bf16 residual column of P
+    const float c = a.scale_log2;
+
+    int u;
+    {
+        int lo = 0, hi = units;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_off[mid] <= g0) lo = mid; else hi = mid;
+        }
+        u = lo;
+    }
+
+    while (true) {
+        const long long seg_lo = max(g0, static_cast<long long>(s_off[u]));
+        const long long seg_hi = min(g1, static_cast<long long>(s_off[u + 1]));
+        if (seg_lo < seg_hi) {
+            const int r = u / a.hkv, j = u % a.hkv;
+            // q fragments (A operand rows 0-7 = heads 0-3 twice, rows 8-15 zero)
+            uint32_t aq[8][2];
+            {
+                const uint16_t *qrow = static_cast<const uint16_t *>(a.q) +
+                                       (static_cast<size_t>(r) * a.hq + j * kGroup + hq_row) * kHeadDim + tq;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    aq[ks][0] = __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16));
+                    aq[ks][1] = __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8));
+                }
+            }
+            float m_run = -INFINITY, l_run = 0.f;
+            float D[8][4];
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) D[mt][0] = D[mt][1] = D[mt][2] = D[mt][3] = 0.f;
+
+            const long long first = seg_lo + ((warp - (seg_lo - g0) % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
+            for (long long g = first; g < seg_hi; g += kConsumerWarps) {
+                const long long idx = g - g0;
+                const int slot = static_cast<int>(idx % kSlots);
+                const uint32_t round = static_cast<uint32_t>(idx / kSlots);
+                if (!mbar_wait(smem_u32(&sm.full[slot]), round & 1u) && lane == 0)
+                    raise_status(a.status, kDevTimeout);
+                const int ntok = sm.meta[slot].y;
+                if (ntok > 0) {
+                    const uint32_t kb = smem_u32(stage + slot * kSlotBytes);
+                    const uint32_t vb = kb + 2 * kHalfBox;
+                    // ---- S^T = q K^T for the 4 heads x 16 tokens ----
+                    float acc[4][4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+                    {
+                        const int t = (lane & 7) + ((lane >> 4) << 3);
+                        const int sw = t & 7;
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const int ch = 2 * ks + ((lane >> 3) & 1);
+                            const uint32_t addr = kb + (ch >> 3) * kHalfBox + t * 128 + (((ch & 7) ^ sw) << 4);
+                            uint32_t b0, b1, b2, b3;
+                            ldsm_x4(addr, b0, b1, b2, b3);
+                            const int par = (ks & 1) * 2;
+                            mma_bf16_16816(acc[par], aq[ks][0], 0u, aq[ks][1], 0u, b0, b1);
+                            mma_bf16_16816(acc[par + 1], aq[ks][0], 0u, aq[ks][1], 0u, b2, b3);
+                        }
+                    }
+                    float s[4] = {(acc[0][0] + acc[2][0]) * c, (acc[0][1] + acc[2][1]) * c,
+                                  (acc[1][0] + acc[3][0]) * c, (acc[1][1] + acc[3][1]) * c};
+                    const bool tail = ntok < kPageSize;
+                    if (tail) {
+                        if (tq >= ntok) s[0] = -INFINITY;
+                        if (tq + 1 >= ntok) s[1] = -INFINITY;
+                        if (tq + 8 >= ntok) s[2] = -INFINITY;
+                        if (tq + 9 >= ntok) s[3] = -INFINITY;
+                    }
+                    float pm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+                    const float m_new = fmaxf(m_run, pm);
+                    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                    const float alpha = exp2f(m_run - m_use);
+                    float p[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) p[x] = exp2f(s[x] - m_use);
+                    l_run = l_run * alpha + (p[0] + p[1]) + (p[2] + p[3]);
+                    m_run = m_new;
+                    // B operand: columns 0-3 bf16(P), columns 4-7 residual
+                    uint32_t bp0, bp1;
+                    {
+                        uint32_t h[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            const uint32_t hb = f32_to_bf16_rne(p[x]);
+                            h[x] = lo_lane ? f32_to_bf16_rne(p[x] - __uint_as_float(hb << 16)) : hb;
+                        }
+                        bp0 = h[0] | (h[1] << 16);
+                        bp1 = h[2] | (h[3] << 16);
+                    }
+                    // rescale the running O^T columns (heads hn0, hn0+1)
+                    const float al0 = __shfl_sync(0xffffffffu, alpha, 4 * hn0);
+                    const float al1 = __shfl_sync(0xffffffffu, alpha, 4 * (hn0 + 1));
+                    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            D[mt][0] *= al0;
+                            D[mt][1] *= al1;
+                            D[mt][2] *= al0;
+                            D[mt][3] *= al1;
+                        }
+                    }
+                    // ---- O^T += V^T P^T ----
+                    uint32_t msk01 = 0xFFFFFFFFu, msk23 = 0xFFFFFFFFu;
+                    if (tail) {
+                        msk01 = (tq < ntok ? 0x0000FFFFu : 0u) | (tq + 1 < ntok ? 0xFFFF0000u : 0u);
+                        msk23 = (tq + 8 < ntok ? 0x0000FFFFu : 0u) | (tq + 9 < ntok ? 0xFFFF0000u : 0u);
+                    }
+                    {
+                        const int mi = lane >> 3;
+                        const int t = (lane & 7) + ((mi >> 1) << 3);
+                        const int sw = t & 7;
+#pragma unroll
+                        for (int mt = 0; mt < 8; ++mt) {
+                            const int ch = 2 * mt + (mi & 1);
+                            const uint32_t addr = vb + (ch >> 3) * kHalfBox + t * 128 + (((ch & 7) ^ sw) << 4);
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4_trans(addr, a0, a1, a2, a3);
+                            mma_bf16_16816(D[mt], a0 & msk01, a1 & msk01, a2 & msk23, a3 & msk23, bp0, bp1);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
+            }
+
+            // ---- warp result -> shared memory ----
+            float lsum = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+            lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const float v = D[mt][x] + __shfl_xor_sync(0xffffffffu, D[mt][x], 2);
+                    if ((lane & 3) < 2) {
+                        const int h = 2 * (lane & 3) + (x & 1);
+                        const int d = 16 * mt + (lane >> 2) + (x >= 2 ? 8 : 0);
+                        sm.co[warp][h][d] = v;
+                    }
+                }
+            }
+            if (lane < 16 && (lane & 3) == 0) {
+                sm.cm[warp][lane >> 2] = m_run;
+                sm.cl[warp][lane >> 2] = lsum;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+
+            // ---- block result: thread -> (head, 4 dims) ----
+            const int h = tid >> 5, d0 = (tid & 31) * 4;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.cm[w][h]);
+            const float Ms = M == -INFINITY ? 0.f : M;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            float Lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float e = exp2f(sm.cm[w][h] - Ms);
+                const float4 v = *reinterpret_cast<const float4 *>(&sm.co[w][h][d0]);
+                o.x += e * v.x; o.y += e * v.y; o.z += e * v.z; o.w += e * v.w;
+                Lsum += e * sm.cl[w][h];
+            }
+            const long long ua = s_off[u], ue = s_off[u + 1];
+            const int bfirst = block_of(ua, W, n), blast = block_of(ue - 1, W, n);
+            float *orow = a.out + (static_cast<size_t>(r) * a.hq + j * kGroup + h) * kHeadDim + d0;
+            if (bfirst == blast) {
+                const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+                *reinterpret_cast<float4 *>(orow) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            } else {
+                float *part = a.partials + static_cast<size_t>(b + u) * kPartFloats;
+                *reinterpret_cast<float4 *>(part + 2 * kGroup + h * kHeadDim + d0) = o;
+                if ((tid & 31) == 0) {
+                    part[h] = M;
+                    part[kGroup + h] = Lsum;
+                }
+                __threadfence();
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                if (tid == 0) {
+                    const unsigned prev = atomicAdd(&a.counters[u], 1u);
+                    sm.flag = (prev == static_cast<unsigned>(blast - bfirst)) ? 1 : 0;
+                }
+                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                if (sm.flag) {
+                    // last block of this list: merge every segment's partial
+                    __threadfence();
+                    float Mall = -INFINITY;
+                    for (int bb = bfirst; bb <= blast; ++bb)
+                        Mall = fmaxf(Mall, __ldcg(a.partials + static_cast<size_t>(bb + u) * kPartFloats + h));
+                    const float Ma = Mall == -INFINITY ? 0.f : Mall;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float la = 0.f;
+                    for (int bb = bfirst; bb <= blast; ++bb) {
+                        const float *pp = a.partials + static_cast<size_t>(bb + u) * kPartFloats;
+                        const float e = exp2f(__ldcg(pp + h) - Ma);
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp + 2 * kGroup + h * kHeadDim + d0));
+                        acc.x += e * v.x; acc.y += e * v.y; acc.z += e * v.z; acc.w += e * v.w;
+                        la += e * __ldcg(pp + kGroup + h);
+                    }
+                    const float inv = la > 0.f ? 1.f / la : 0.f;
+                    *reinterpret_cast<float4 *>(orow) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                    if (tid == 0) a.counters[u] = 0u;      // ready for the next launch
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+        }
+        if (static_cast<long long>(s_off[u + 1]) >= g1) break;
+        ++u;
+    }
+}
+
+int attend_blocks_per_sm() { return kBlocksPerSm; }
+
+template <int NS>
+static cudaError_t launch_attend_ns(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                    const AttendArgs &args, int blocks, cudaStream_t stream)
+{
+    const size_t smem = attend_smem_bytes<NS>(args.units);
+    cudaError_t e = cudaFuncSetAttribute(k_attend<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_attend<NS>, dim3(blocks), dim3(kAttThreads), smem, stream, tmap_k, tmap_v,
+                      args);
+}
+
+cudaError_t launch_attend(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                          const AttendArgs &args, int blocks, cudaStream_t stream)
+{
+    if (args.units <= kDeepMaxUnits)
+        return launch_attend_ns<kDeepSlots>(tmap_k, tmap_v, args, blocks, stream);
+    return launch_attend_ns<kShallowSlots>(tmap_k, tmap_v, args, blocks, stream);
+}
+
+}  // namespace moira

@@ -1,0 +1,188 @@
+// Device-side building blocks shared by the MOIRA kernels (sm_103a).
+// Inline PTX for the Blackwell data path: mbarrier-tracked TMA tensor loads,
+// ldmatrix and warp-level bf16 tensor-core MMA.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moira {
+
+constexpr int kHeadDim = 128;           // d
+constexpr int kPageSize = 16;           // S
+constexpr int kGroup = 4;               // G = Hq / Hkv
+constexpr int kMaxPagesPerSeq = 32768;
+constexpr int kMaxUnits = 4096;
+
+constexpr uint32_t kDevBadPage = 0x1u;
+constexpr uint32_t kDevBadLen = 0x2u;
+constexpr uint32_t kDevTimeout = 0x4u;
+
+// A bounded device wait gives up after this long (ns of %globaltimer).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ---- workspace layout ------------------------------------------------------
+// [0, 256)                    : uint32 status word (+ padding)
+// counters                    : uint32 [kMaxUnits]  merge arrival counters
+// scores                      : fp32 [batch][Hq][max_pages]  (log2-domain logits)
+// chunk stats                 : fp32 [batch][Hq][n_chunks][2] (max, sum 2^(s-max))
+// partials                    : fp32 [n_blocks + units][kPartFloats]
+constexpr int kScoreChunk = 32;                    // pages per score block
+constexpr int kPartFloats = 2 * kGroup + kGroup * kHeadDim;   // m[G], l[G], o[G][d]
+
+struct WsLayout {
+    size_t status, counters, scores, chunks, partials, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline WsLayout ws_layout(int batch, int hq, int max_pages, int units, int blocks)
+{
+    WsLayout w;
+    size_t o = 0;
+    w.status = o;   o += 256;
+    w.counters = o; o = align_up(o + sizeof(uint32_t) * kMaxUnits, 256);
+    w.scores = o;   o = align_up(o + sizeof(float) * (size_t)batch * hq * max_pages, 256);
+    int nch = (max_pages + kScoreChunk - 1) / kScoreChunk;
+    w.chunks = o;   o = align_up(o + sizeof(float) * 2 * (size_t)batch * hq * nch, 256);
+    w.partials = o; o = align_up(o + sizeof(float) * kPartFloats * (size_t)(blocks + units), 256);
+    w.total = o;
+    return w;
+}
+
+// ---- small helpers -----------------------------------------------------------
+__device__ __forceinline__ void raise_status(uint32_t *status, uint32_t bits) { atomicOr(status, bits); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// fp32 -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---- mbarrier ------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete, giving up after kWaitLimitNs.
+// Returns false on timeout (the caller records MOIRA_DEV_TIMEOUT and goes on,
+// so the control flow of the block never changes and nothing hangs).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// ---- programmatic dependent launch -------------------------------------------------
+// A kernel launched with programmatic stream serialisation may start while its
+// predecessor in the stream is still running.  pdl_wait() blocks until the
+// predecessor grid has completed and its memory is visible; everything that
+// reads or writes data shared with earlier kernels must come after it.
+// pdl_trigger() lets the successor's blocks be scheduled early.  Both are
+// no-ops for a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---- TMA ---------------------------------------------------------------------------
+// 2-D tiled tensor load into this CTA's shared memory, completion counted in
+// bytes on `bar`.  c0 is the inner (contiguous) coordinate in elements.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int32_t c0,
+                                            int32_t c1, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- ldmatrix / mma ----------------------------------------------------------------
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                              uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D[16x8] += A[16x16] (row) * B[16x8] (col), bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+}  // namespace moira

@@ -1,0 +1,60 @@
+// Internal launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moira {
+
+cudaError_t launch_summarize(const void *k_pool, void *summ, const int32_t *phys_pages, int n,
+                             int hkv, long long num_pages, uint32_t *status, cudaStream_t stream);
+
+cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_table,
+                         const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
+                         long long num_pages, float scale_log2, float *scores, float *chunks,
+                         uint32_t *status, cudaStream_t stream);
+
+cudaError_t launch_select(const float *scores, const float *chunks, const int32_t *page_table,
+                          const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
+                          long long num_pages, unsigned long long gamma_fx, bool dense,
+                          int32_t *lists, int32_t *lengths, uint32_t *status, cudaStream_t stream);
+
+struct AttendArgs {
+    const void *q;
+    const int32_t *lists;
+    const int32_t *lengths;
+    const int32_t *seq_lens;
+    float *out;
+    float *partials;
+    uint32_t *counters;
+    uint32_t *status;
+    int hq, hkv, units, max_pages;
+    long long num_pages;
+    float scale_log2;
+};
+
+cudaError_t launch_attend(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                          const AttendArgs &args, int blocks, cudaStream_t stream);
+
+int attend_blocks_per_sm();
+
+// Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
+}  // namespace moira

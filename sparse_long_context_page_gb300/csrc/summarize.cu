@@ -1,0 +1,77 @@
+// Page summaries: the bf16 mean key of every (page, KV head) block.
+//
+// "MOIRA: Mass-Oriented Indexing with Ragged Attention for Long-Context
+// Decoding", abstract: the coverage rule works on an *estimated* attention
+// mass per page, which needs per-page metadata.  The form used here is the
+// mean vector of the page's keys, one of the block summaries named in
+// "Faster Flash Decoding", section 2 (related work).
+//
+// The 16 keys are summed in fp64 (exact for bf16 inputs of moderate range)
+// and the mean is rounded once to bf16, ties to even.  This runs when a page
+// fills, outside the decode step, so fp64 throughput does not matter here.
+#include "moira_device.cuh"
+#include "moira_launch.h"
+
+namespace moira {
+
+// Round a double to the nearest bf16 (ties to even) in one step, by integer
+// arithmetic on the binary64 encoding: keep sign, exponent and the top 7
+// fraction bits, adding half an ulp minus one plus the kept lsb before
+// truncating.  Magnitudes below 2^-126 land on the bf16 subnormal grid
+// (multiples of 2^-133), reached by exact scaling and rint().
+__device__ __forceinline__ uint32_t f64_to_bf16_rne(double x)
+{
+    const unsigned long long u = static_cast<unsigned long long>(__double_as_longlong(x));
+    const uint32_t sign = static_cast<uint32_t>(u >> 48) & 0x8000u;
+    const unsigned long long a = u & 0x7FFFFFFFFFFFFFFFull;
+    if (a > 0x7FF0000000000000ull) return 0x7FC0u;                  // NaN
+    const int biased = static_cast<int>(a >> 52);
+    if (biased >= 1023 - 126) {                                       // |x| >= 2^-126
+        const unsigned long long r = a + ((1ull << 44) - 1ull) + ((a >> 45) & 1ull);
+        const int e_bf = static_cast<int>(r >> 52) - 1023 + 127;
+        if (e_bf >= 255) return sign | 0x7F80u;                       // overflow / inf
+        return sign | (static_cast<uint32_t>(e_bf) << 7) | static_cast<uint32_t>((r >> 45) & 0x7Full);
+    }
+    const double grid = rint(fabs(x) * 0x1p133);                      // in [0, 128]
+    return sign | static_cast<uint32_t>(grid);
+}
+
+// One block per (listed page, KV head); 64 threads, two dimensions each.
+__global__ void __launch_bounds__(64) k_summarize(const uint32_t *__restrict__ k_pool,
+                                                  uint32_t *__restrict__ summ,
+                                                  const int32_t *__restrict__ phys_pages, int hkv,
+                                                  long long num_pages, uint32_t *status)
+{
+    const int item = blockIdx.x;
+    const int j = item % hkv;
+    const int idx = item / hkv;
+    const int p = phys_pages[idx];
+    if (p < 0 || p >= num_pages) {
+        if (threadIdx.x == 0 && status != nullptr) raise_status(status, kDevBadPage);
+        return;
+    }
+    const size_t blk = (static_cast<size_t>(p) * hkv + j);
+    const uint32_t *src = k_pool + blk * (kPageSize * kHeadDim / 2) + threadIdx.x;
+    double lo = 0.0, hi = 0.0;
+#pragma unroll
+    for (int t = 0; t < kPageSize; ++t) {
+        const uint32_t v = __ldg(src + t * (kHeadDim / 2));
+        lo += static_cast<double>(bf16_lo(v));
+        hi += static_cast<double>(bf16_hi(v));
+    }
+    const uint32_t blo = f64_to_bf16_rne(lo * (1.0 / kPageSize));
+    const uint32_t bhi = f64_to_bf16_rne(hi * (1.0 / kPageSize));
+    summ[blk * (kHeadDim / 2) + threadIdx.x] = blo | (bhi << 16);
+}
+
+cudaError_t launch_summarize(const void *k_pool, void *summ, const int32_t *phys_pages, int n,
+                             int hkv, long long num_pages, uint32_t *status, cudaStream_t stream)
+{
+    if (n <= 0) return cudaSuccess;
+    k_summarize<<<static_cast<unsigned>(n) * hkv, 64, 0, stream>>>(
+        static_cast<const uint32_t *>(k_pool), static_cast<uint32_t *>(summ), phys_pages, hkv,
+        num_pages, status);
+    return cudaGetLastError();
+}
+
+}  // namespace moira

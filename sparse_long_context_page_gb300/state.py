@@ -1,0 +1,63 @@
+"""Device buffers for one decode workload, driven through the C ABI.
+
+Holds the per-layer summaries, page table, lists, lengths, outputs and the
+workspace that ``moira_select`` / ``moira_attend`` need, so that a caller can
+run a whole decode-attention step with one call (or capture it in a graph).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as mb
+from .workloads import Workload
+
+
+class DecodeState:
+    def __init__(self, w: Workload, max_pages: int | None = None):
+        sp = w.spec
+        dev = w.q.device
+        self.w = w
+        self.device = dev
+        self.layers, self.batch = sp.layers, sp.batch
+        self.max_pages = w.max_pages if max_pages is None else max_pages
+        self.shape = mb.Shape.of(sp.q_heads, sp.kv_heads, w.num_phys_pages)
+        self.sm_scale = w.sm_scale
+        pt = torch.full((sp.batch, self.max_pages), -1, dtype=torch.int32)
+        pt[:, :w.max_pages] = torch.from_numpy(w.page_table)
+        self.page_table = pt.to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.summ = torch.zeros((sp.layers, w.num_phys_pages, sp.kv_heads, sp.head_dim),
+                                dtype=torch.bfloat16, device=dev)
+        self.lists = torch.zeros((sp.batch, sp.kv_heads, self.max_pages), dtype=torch.int32, device=dev)
+        self.lengths = torch.zeros((sp.layers, sp.batch, sp.kv_heads), dtype=torch.int32, device=dev)
+        self.out = torch.zeros((sp.layers, sp.batch, sp.q_heads, sp.head_dim), dtype=torch.float32,
+                               device=dev)
+        self.ws = mb.make_workspace(self.shape, sp.batch, self.max_pages, device=dev)
+
+    def summarize(self):
+        """Summaries of every physical page of every layer (after prefill)."""
+        pages = torch.arange(self.w.num_phys_pages, dtype=torch.int32, device=self.device)
+        for l in range(self.layers):
+            mb.update_summaries(self.shape, self.w.k_pool[l], self.summ[l], pages)
+
+    def step(self, gamma: float):
+        """One decode-attention step over all layers (select + attend per layer)."""
+        mb.decode_step(self.shape, self.w.q, self.w.k_pool, self.w.v_pool, self.summ,
+                       self.page_table, self.seq_lens, gamma, self.sm_scale, self.lists,
+                       self.lengths, self.out, self.ws)
+
+    def select_layer(self, l: int, gamma: float, lists=None, lengths=None):
+        lists = self.lists if lists is None else lists
+        lengths = self.lengths[l] if lengths is None else lengths
+        mb.select(self.shape, self.w.q[l], self.summ[l], self.page_table, self.seq_lens, gamma,
+                  self.sm_scale, lists, lengths, self.ws)
+        return lists, lengths
+
+    def attend_layer(self, l: int, lists, lengths, out=None):
+        out = self.out[l] if out is None else out
+        mb.attend(self.shape, self.w.q[l], self.w.k_pool[l], self.w.v_pool[l], lists, lengths,
+                  self.seq_lens, self.max_pages, self.sm_scale, out, self.ws)
+        return out
+
+    def device_status(self) -> int:
+        return mb.read_device_status(self.ws)

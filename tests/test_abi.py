@@ -1,0 +1,90 @@
+"""The C ABI without a GPU: the library builds and loads, exports every
+function include/moira.h declares, and its host-side checks reject bad
+arguments before any CUDA call (fake, never-dereferenced pointers)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_long_context_page_gb300 as moira
+from sparse_long_context_page_gb300 import _binding as mb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000          # 64 KiB-aligned fake device address; never dereferenced
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "moira.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moira_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    lib = moira.load_library()
+    decl = declared_functions()
+    assert len(decl) >= 10
+    for name in decl:
+        assert hasattr(lib, name), f"{name} declared in moira.h but not exported"
+    assert set(decl) == set(mb.EXPORTS)
+
+
+def test_status_strings():
+    lib = moira.load_library()
+    for code in range(5):
+        assert lib.moira_status_string(code)
+    assert lib.moira_status_string(99) == b"unknown status"
+
+
+def _select(lib, shape, gamma=0.9, sm=0.088, q=FAKE, batch=1, max_pages=64):
+    return lib.moira_select(ctypes.byref(shape), q, FAKE, FAKE, FAKE, batch, max_pages, gamma, sm,
+                            FAKE, FAKE, FAKE, 1 << 30, None)
+
+
+def test_select_rejects_bad_arguments_on_host():
+    lib = moira.load_library()
+    ok = moira.Shape.of(32, 8, 1024)
+    assert _select(lib, ok, gamma=0.0) == 1
+    assert _select(lib, ok, gamma=1.5) == 1
+    assert _select(lib, ok, gamma=float("nan")) == 1
+    assert _select(lib, ok, sm=-1.0) == 1
+    assert _select(lib, ok, sm=float("inf")) == 1
+    assert _select(lib, ok, q=0) == 1                         # null pointer
+    assert _select(lib, ok, q=FAKE + 2) == 1                  # misaligned
+    assert _select(lib, ok, batch=0) == 1
+    assert _select(lib, ok, max_pages=mb.MAX_PAGES_PER_SEQ + 1) == 4
+    assert _select(lib, ok, batch=mb.MAX_UNITS // 8 + 1) == 4
+    assert _select(lib, moira.Shape.of(32, 8, 1024, head_dim=64)) == 4
+    assert _select(lib, moira.Shape.of(32, 8, 1024, page_size=32)) == 4
+    assert _select(lib, moira.Shape.of(16, 8, 1024)) == 4     # group of 2
+    assert _select(lib, moira.Shape.of(30, 8, 1024)) == 1     # not a multiple
+    assert _select(lib, moira.Shape.of(32, 8, 0)) == 1
+    assert _select(lib, moira.Shape.of(32, 8, 1 << 25)) == 4  # TMA rows beyond 2^31
+
+
+def test_attend_and_step_reject_bad_arguments_on_host():
+    lib = moira.load_library()
+    ok = moira.Shape.of(32, 8, 1024)
+    sp = ctypes.byref(ok)
+    assert lib.moira_attend(sp, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 0.0, FAKE, FAKE, 1 << 30, None) == 1
+    assert lib.moira_attend(sp, FAKE, FAKE + 8, FAKE, FAKE, FAKE, FAKE, 1, 64, 0.1, FAKE, FAKE, 1 << 30, None) == 1
+    assert lib.moira_attend(sp, FAKE, FAKE, 0, FAKE, FAKE, FAKE, 1, 64, 0.1, FAKE, FAKE, 1 << 30, None) == 1
+    assert lib.moira_decode_step(sp, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 0.9, 0.1,
+                                 FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert lib.moira_decode_step(sp, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 1.01, 0.1,
+                                 FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert lib.moira_update_summaries(sp, FAKE, FAKE, FAKE, -1, None) == 1
+    assert lib.moira_update_summaries(sp, FAKE, FAKE + 4, FAKE, 3, None) == 1
+    assert lib.moira_update_summaries(sp, FAKE, FAKE, FAKE, 0, None) == 0      # nothing to do
+    assert lib.moira_workspace_init(None, 100, None) == 2
+    st = ctypes.c_uint32(0)
+    assert lib.moira_read_device_status(None, 1024, ctypes.byref(st), 0, None) == 2
+    assert lib.moira_workspace_bytes(ctypes.byref(moira.Shape.of(30, 8, 16)), 1, 64) == 0
+
+
+def test_binding_rejects_host_tensors():
+    torch = pytest.importorskip("torch")
+    shape = moira.Shape.of(8, 2, 16)
+    t = torch.zeros(4, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        moira.update_summaries(shape, t, t, torch.zeros(1, dtype=torch.int32))

@@ -1,0 +1,274 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Inputs are the seeded synthetic workloads; sizes here keep the oracle at
+seconds while spanning many score chunks, many attention blocks, ragged
+tails and every selection regime.  Comparison rules: see helpers.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import helpers as H
+from sparse_long_context_page_gb300 import _binding as mb
+from sparse_long_context_page_gb300 import workloads as W
+from sparse_long_context_page_gb300.state import DecodeState
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():          # collected on CPU machines, never run there
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+
+def _state(name, seed=0, max_pages=None, **over):
+    w = W.make_workload(name, seed=seed, device="cuda", **over)
+    st = DecodeState(w, max_pages=max_pages)
+    st.summarize()
+    return w, st
+
+
+def _check_layer(w, st, l, gamma, units=None, check_out=True):
+    """Select + attend one layer on the GPU and compare every (or the given)
+    unit with the oracle.  Returns (units checked, outputs compared)."""
+    lists = torch.zeros_like(st.lists)
+    lengths = torch.zeros((w.spec.batch, w.spec.kv_heads), dtype=torch.int32, device="cuda")
+    st.select_layer(l, gamma, lists, lengths)
+    out = torch.zeros_like(st.out[l])
+    st.attend_layer(l, lists, lengths, out)
+    torch.cuda.synchronize()
+    assert st.device_status() == 0
+    lists_h, len_h, out_h = lists.cpu().numpy(), lengths.cpu().numpy(), out.cpu().numpy()
+    G = w.group
+    units = units or [(r, j) for r in range(w.spec.batch) for j in range(w.spec.kv_heads)]
+    n_out = 0
+    for (r, j) in units:
+        ud = H.UnitData(w, l, r, j)
+        gl = lists_h[r, j, :len_h[r, j]]
+        why = H.check_list(ud, gl, gamma)
+        assert why is None, f"layer {l} req {r} kv {j} gamma {gamma}: {why}"
+        o_list = ud.select(gamma)[0]
+        if check_out and np.array_equal(ud.to_logical(gl), o_list):
+            ref = ud.attend(o_list)
+            ma, rl = H.out_errors(out_h[r, j * G:(j + 1) * G], ref)
+            assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"l{l} r{r} j{j}: max-abs {ma:.3g} rel-L2 {rl:.3g}"
+            n_out += 1
+    return len(units), n_out
+
+
+# ------------------------------------------------------------------ summaries
+
+def test_summaries_bit_exact():
+    w, st = _state("llama8b_128k", seed=3, layers=2, context=(16 * 700 + 9,))
+    torch.cuda.synchronize()
+    got = H.u16(st.summ)                                           # [L][P][Hkv][d]
+    k = H.u16(w.k_pool)                                            # [L][P][Hkv][S][d]
+    ref = H.oracle.summaries(k.reshape(-1, 16, 128)).reshape(got.shape)
+    diff = np.count_nonzero(got != ref)
+    assert diff == 0, f"{diff} of {got.size} summary elements differ"
+
+
+# ------------------------------------------------------------------ selection + attention
+
+@pytest.mark.parametrize("gamma", [0.9, 0.99, 1.0])
+def test_tiny_select_and_attend(gamma):
+    w, st = _state("tiny", seed=0)
+    n_units, n_out = _check_layer(w, st, 0, float(np.float32(gamma)))
+    assert n_out == n_units
+
+
+@pytest.mark.parametrize("name,over,gamma", [
+    ("llama8b_32k", dict(layers=2), 0.99),
+    ("llama8b_128k", dict(layers=1), 0.98),
+    ("llama8b_128k", dict(layers=1), 0.99),
+    ("serving_ragged", dict(batch=4, layers=1), 0.99),
+    ("stress_regimes", dict(batch=6, context=(16 * 4000 + 7,)), 0.99),
+])
+def test_config_select_and_attend(name, over, gamma):
+    w, st = _state(name, seed=11, **over)
+    total_u = total_o = 0
+    for l in range(w.spec.layers):
+        nu, no = _check_layer(w, st, l, float(np.float32(gamma)))
+        total_u += nu
+        total_o += no
+    # units whose lists differ only at the boundary skip the output check; they must be few
+    assert total_o >= 0.8 * total_u, f"only {total_o}/{total_u} outputs compared"
+
+
+def test_select_edge_lengths():
+    """Empty, sub-page, exact-page and tail-only contexts in one ragged batch,
+    with max_pages larger than any request needs."""
+    sp = W.spec("llama8b_128k", batch=8, layers=1, context=(0, 1, 15, 16, 17, 16 * 33, 16 * 257 + 3, 5000))
+    w = W.make_workload(sp, seed=5, device="cuda")
+    st = DecodeState(w, max_pages=w.max_pages + 37)
+    st.summarize()
+    for gamma in (1e-6, 0.5, 0.99, 1.0):
+        _check_layer(w, st, 0, float(np.float32(gamma)))
+
+
+def test_attend_random_lists_isolated():
+    """Attention alone on seeded random lists (neither side's selection)."""
+    w = W.make_workload("serving_ragged", seed=21, device="cuda", batch=5, layers=1)
+    st = DecodeState(w)
+    G = w.group
+    for trial, frac in enumerate([(0.0, 1.0), (0.0, 0.02), (0.9, 1.0)]):
+        logical, phys, lengths = W.random_lists(w, seed=100 + trial, keep_frac=frac)
+        lists = torch.from_numpy(phys).cuda()
+        lens = torch.from_numpy(lengths).cuda()
+        out = torch.zeros_like(st.out[0])
+        st.attend_layer(0, lists, lens, out)
+        torch.cuda.synchronize()
+        assert st.device_status() == 0
+        oh = out.cpu().numpy()
+        for r in range(w.spec.batch):
+            for j in range(w.spec.kv_heads):
+                ud = H.UnitData(w, 0, r, j)
+                ref = ud.attend(logical[r][j])
+                ma, rl = H.out_errors(oh[r, j * G:(j + 1) * G], ref)
+                assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"{frac} r{r} j{j}: {ma:.3g} {rl:.3g}"
+
+
+def test_attend_empty_and_single_lists():
+    w = W.make_workload("tiny", seed=2, device="cuda", batch=3, context=(16 * 40, 16 * 40 + 3, 16 * 40))
+    st = DecodeState(w)
+    B, Hkv = 3, 2
+    phys = np.full((B, Hkv, w.max_pages), -1, np.int32)
+    lengths = np.zeros((B, Hkv), np.int32)
+    logical = [[np.zeros(0, np.int32) for _ in range(Hkv)] for _ in range(B)]
+    logical[0][1] = np.array([7], np.int32)                         # one full page
+    logical[1][0] = np.array([40], np.int32)                        # the tail page alone (3 tokens)
+    logical[2][1] = np.arange(40, dtype=np.int32)                   # everything
+    for r in range(B):
+        for j in range(Hkv):
+            lst = logical[r][j]
+            phys[r, j, :len(lst)] = w.page_table[r, lst]
+            lengths[r, j] = len(lst)
+    out = torch.full_like(st.out[0], 7.0)
+    st.attend_layer(0, torch.from_numpy(phys).cuda(), torch.from_numpy(lengths).cuda(), out)
+    torch.cuda.synchronize()
+    oh = out.cpu().numpy()
+    for r in range(B):
+        for j in range(Hkv):
+            ref = H.UnitData(w, 0, r, j).attend(logical[r][j])
+            ma, rl = H.out_errors(oh[r, j * 4:(j + 1) * 4], ref)
+            assert ma <= H.MAX_ABS and rl <= H.REL_L2
+    assert np.all(oh[0, 0:4] == 0.0)                                # empty list -> zeros
+
+
+# ------------------------------------------------------------------ graph, status, determinism
+
+def test_graph_capture_matches_eager_bit_for_bit():
+    w, st = _state("llama8b_32k", seed=4, layers=4)
+    st.step(0.99)
+    torch.cuda.synchronize()
+    out_e, len_e = st.out.clone(), st.lengths.clone()
+    st.out.zero_()
+    st.lengths.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            st.step(0.99)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(st.lengths, len_e)
+    assert torch.equal(st.out, out_e)
+    assert st.device_status() == 0
+
+
+def test_device_status_flags_bad_pages_and_lengths():
+    w, st = _state("tiny", seed=6)
+    pt = st.page_table.clone()
+    st.page_table[0, 3] = w.num_phys_pages + 5                     # out of the pool
+    lists, lengths = st.select_layer(0, 0.99)
+    out = st.attend_layer(0, lists, lengths)
+    torch.cuda.synchronize()
+    assert st.device_status() & mb.DEV_BADPAGE
+    st.page_table.copy_(pt)
+    bad_len = torch.full_like(st.lengths[0], st.max_pages + 100)
+    st.attend_layer(0, st.lists, bad_len)
+    torch.cuda.synchronize()
+    assert st.device_status() & mb.DEV_BADLEN
+    # the context is still usable and clean afterwards
+    st.step(0.99)
+    torch.cuda.synchronize()
+    assert st.device_status() == 0
+
+
+def test_host_checks_launch_nothing():
+    w, st = _state("tiny", seed=7)
+    with pytest.raises(mb.MoiraError):
+        st.select_layer(0, 1.5)
+    with pytest.raises(mb.MoiraError):
+        st.select_layer(0, 0.0)
+    small = st.ws[: st.ws.numel() // 2]
+    with pytest.raises(mb.MoiraError):
+        mb.select(st.shape, w.q[0], st.summ[0], st.page_table, st.seq_lens, 0.9, st.sm_scale,
+                  st.lists, st.lengths[0], small)
+
+
+def test_host_buffers_step_matches_device_step():
+    w, st = _state("llama8b_32k", seed=8, layers=2)
+    st.step(0.99)
+    torch.cuda.synchronize()
+    ref = st.out.clone()
+    q_host = w.q.cpu().pin_memory()
+    out_host = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
+    q_dev = torch.empty_like(w.q)
+    out_dev = torch.empty_like(st.out)
+    mb.decode_step_host(st.shape, q_host, q_dev, w.k_pool, w.v_pool, st.summ, st.page_table,
+                        st.seq_lens, 0.99, st.sm_scale, st.lists, st.lengths, out_dev, out_host, st.ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host, ref.cpu())
+
+
+# ------------------------------------------------------------------ full sizes, sampled units
+
+FULL = [("llama8b_32k", 0.99), ("llama8b_128k", 0.99), ("llama8b_128k", 0.98),
+        ("stress_regimes", 0.99), ("serving_ragged", 0.99)]
+
+
+@pytest.mark.parametrize("name,gamma", FULL)
+def test_full_size_sampled_units(name, gamma):
+    """The full configuration, whole step in one graph (as the benchmark runs
+    it); sampled units are checked against the oracle one by one."""
+    torch.cuda.empty_cache()
+    w, st = _state(name, seed=0)
+    g32 = float(np.float32(gamma))
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        st.step(g32)                                               # warm-up (sets attributes)
+        with torch.cuda.graph(g, stream=s):
+            st.step(g32)
+    torch.cuda.current_stream().wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert st.device_status() == 0
+    rng = np.random.default_rng(123)
+    L, B, Hkv, G = w.spec.layers, w.spec.batch, w.spec.kv_heads, w.group
+    picks = {(int(rng.integers(L)), int(rng.integers(B)), int(rng.integers(Hkv))) for _ in range(10)}
+    out_h = st.out.cpu().numpy()
+    len_h = st.lengths.cpu().numpy()
+    lists = torch.zeros_like(st.lists)
+    compared = 0
+    for (l, r, j) in sorted(picks):
+        lengths = torch.zeros((B, Hkv), dtype=torch.int32, device="cuda")
+        st.select_layer(l, g32, lists, lengths)
+        torch.cuda.synchronize()
+        lh = lengths.cpu().numpy()
+        assert lh[r, j] == len_h[l, r, j]
+        gl = lists[r, j, :lh[r, j]].cpu().numpy()
+        ud = H.UnitData(w, l, r, j)
+        why = H.check_list(ud, gl, g32)
+        assert why is None, f"{name} l{l} r{r} j{j}: {why}"
+        o_list = ud.select(g32)[0]
+        if np.array_equal(ud.to_logical(gl), o_list):
+            ma, rl = H.out_errors(out_h[l, r, j * G:(j + 1) * G], ud.attend(o_list))
+            assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"{name} l{l} r{r} j{j}: {ma:.3g} {rl:.3g}"
+            compared += 1
+    assert compared >= len(picks) - 2
+    del st, w
+    torch.cuda.empty_cache()
