@@ -405,20 +405,41 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
                 }
                 asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
                 if (sm.flag) {
-                    // last block of this list: merge every segment's partial
+                    // last block of this list: merge every segment's partial in
+                    // one online pass, kMergeBatch segments' loads in flight at once
                     __threadfence();
-                    float Mall = -INFINITY;
-                    for (int bb = bfirst; bb <= blast; ++bb)
-                        Mall = fmaxf(Mall, __ldcg(a.partials + static_cast<size_t>(bb + u) * kPartFloats + h));
-                    const float Ma = Mall == -INFINITY ? 0.f : Mall;
+                    constexpr int kMergeBatch = 16;
+                    float Mrun = -INFINITY, la = 0.f;
                     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    float la = 0.f;
-                    for (int bb = bfirst; bb <= blast; ++bb) {
-                        const float *pp = a.partials + static_cast<size_t>(bb + u) * kPartFloats;
-                        const float e = exp2f(__ldcg(pp + h) - Ma);
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(pp + 2 * kGroup + h * kHeadDim + d0));
-                        acc.x += e * v.x; acc.y += e * v.y; acc.z += e * v.z; acc.w += e * v.w;
-                        la += e * __ldcg(pp + kGroup + h);
+                    for (int b0 = bfirst; b0 <= blast; b0 += kMergeBatch) {
+                        float mv[kMergeBatch], lv[kMergeBatch];
+                        float4 ov[kMergeBatch];
+#pragma unroll
+                        for (int k = 0; k < kMergeBatch; ++k) {
+                            mv[k] = -INFINITY;
+                            lv[k] = 0.f;
+                            ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (b0 + k <= blast) {
+                                const float *pp = a.partials + static_cast<size_t>(b0 + k + u) * kPartFloats;
+                                mv[k] = __ldcg(pp + h);
+                                lv[k] = __ldcg(pp + kGroup + h);
+                                ov[k] = __ldcg(reinterpret_cast<const float4 *>(pp + 2 * kGroup + h * kHeadDim + d0));
+                            }
+                        }
+                        float mb = Mrun;
+#pragma unroll
+                        for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, mv[k]);
+                        const float ms = mb == -INFINITY ? 0.f : mb;
+                        const float sc = exp2f(Mrun - ms);
+                        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+                        la *= sc;
+#pragma unroll
+                        for (int k = 0; k < kMergeBatch; ++k) {
+                            const float e = exp2f(mv[k] - ms);
+                            acc.x += e * ov[k].x; acc.y += e * ov[k].y; acc.z += e * ov[k].z; acc.w += e * ov[k].w;
+                            la += e * lv[k];
+                        }
+                        Mrun = mb;
                     }
                     const float inv = la > 0.f ? 1.f / la : 0.f;
                     *reinterpret_cast<float4 *>(orow) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);

@@ -32,7 +32,7 @@ constexpr int kScoreItemsPerLane = 8;     // 32 pages * Hkv(<= 8) / 32 items per
 // lane; 4 items per warp and 32 per block pass.  Because 32 is a multiple of
 // Hkv, a lane always serves the same KV head and keeps that head's G=4 query
 // slices (64 floats) in registers for the whole block.
-__global__ void __launch_bounds__(kScoreThreads) k_score(
+__global__ void __launch_bounds__(kScoreThreads, 2) k_score(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ summ,
     const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
     int max_pages, long long num_pages, float scale_log2, float *__restrict__ scores,
@@ -70,55 +70,61 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(
 
     const int n_items = np * hkv;
     const int32_t *row = page_table + static_cast<size_t>(r) * max_pages + p0;
-    uint4 buf[kScoreItemsPerLane][2];
-    bool bad[kScoreItemsPerLane];
+    // two passes of 4 items per lane: 4 x 32 B loads in flight per lane
 #pragma unroll
-    for (int k = 0; k < kScoreItemsPerLane; ++k) {
-        const int it = warp * 4 + (lane >> 3) + 32 * k;
-        bad[k] = false;
-        buf[k][0] = buf[k][1] = make_uint4(0, 0, 0, 0);
-        if (it < n_items) {
-            const int phys = __ldg(row + it / hkv);
-            if (phys < 0 || phys >= num_pages) {
-                bad[k] = true;
-            } else {
-                const uint4 *sp = reinterpret_cast<const uint4 *>(
-                    summ + (static_cast<size_t>(phys) * hkv + j) * kHeadDim + sub * 16);
-                buf[k][0] = __ldg(sp);
-                buf[k][1] = __ldg(sp + 1);
+    for (int k0 = 0; k0 < kScoreItemsPerLane; k0 += 4) {
+        if (warp * 4 + 32 * k0 >= n_items) break;            // warp-uniform
+        uint4 buf[4][2];
+        bool bad[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int it = warp * 4 + (lane >> 3) + 32 * (k0 + k);
+            bad[k] = false;
+            buf[k][0] = buf[k][1] = make_uint4(0, 0, 0, 0);
+            if (it < n_items) {
+                const int phys = __ldg(row + it / hkv);
+                if (phys < 0 || phys >= num_pages) {
+                    bad[k] = true;
+                } else {
+                    const uint4 *sp = reinterpret_cast<const uint4 *>(
+                        summ + (static_cast<size_t>(phys) * hkv + j) * kHeadDim + sub * 16);
+                    buf[k][0] = __ldg(sp);
+                    buf[k][1] = __ldg(sp + 1);
+                }
             }
         }
-    }
 #pragma unroll
-    for (int k = 0; k < kScoreItemsPerLane; ++k) {
-        const int it = warp * 4 + (lane >> 3) + 32 * k;
-        if (warp * 4 + 32 * k >= n_items) break;        // warp-uniform
-        const uint32_t w[8] = {buf[k][0].x, buf[k][0].y, buf[k][0].z, buf[k][0].w,
-                               buf[k][1].x, buf[k][1].y, buf[k][1].z, buf[k][1].w};
-        float dot[kGroup];
+        for (int k = 0; k < 4; ++k) {
+            const int it = warp * 4 + (lane >> 3) + 32 * (k0 + k);
+            if (warp * 4 + 32 * (k0 + k) >= n_items) break;  // warp-uniform
+            const uint32_t w[8] = {buf[k][0].x, buf[k][0].y, buf[k][0].z, buf[k][0].w,
+                                   buf[k][1].x, buf[k][1].y, buf[k][1].z, buf[k][1].w};
+            float dot[kGroup];
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) dot[g] = 0.f;
+            for (int g = 0; g < kGroup; ++g) dot[g] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
+            for (int i = 0; i < 8; ++i) {
+                const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
 #pragma unroll
-            for (int g = 0; g < kGroup; ++g) dot[g] = fmaf(qr[g][2 * i + 1], x1, fmaf(qr[g][2 * i], x0, dot[g]));
-        }
-#pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-            dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 1);
-            dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 2);
-            dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 4);
-        }
-        if (sub == 0 && it < n_items) {
-            const int pl = it / hkv;
-            if (bad[k]) raise_status(status, kDevBadPage);
+                for (int g = 0; g < kGroup; ++g)
+                    dot[g] = fmaf(qr[g][2 * i + 1], x1, fmaf(qr[g][2 * i], x0, dot[g]));
+            }
 #pragma unroll
             for (int g = 0; g < kGroup; ++g) {
-                const int h = j * kGroup + g;
-                const float s = bad[k] ? -INFINITY : dot[g] * scale_log2;
-                s_s[h * kScoreChunk + pl] = s;
-                scores[(static_cast<size_t>(r) * hq + h) * max_pages + p0 + pl] = s;
+                dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 1);
+                dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 2);
+                dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 4);
+            }
+            if (sub == 0 && it < n_items) {
+                const int pl = it / hkv;
+                if (bad[k]) raise_status(status, kDevBadPage);
+#pragma unroll
+                for (int g = 0; g < kGroup; ++g) {
+                    const int h = j * kGroup + g;
+                    const float sv = bad[k] ? -INFINITY : dot[g] * scale_log2;
+                    s_s[h * kScoreChunk + pl] = sv;
+                    scores[(static_cast<size_t>(r) * hq + h) * max_pages + p0 + pl] = sv;
+                }
             }
         }
     }
@@ -260,17 +266,37 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     if (tid == 0) { sh.found = 0; sh.above = 0ull; }
     __syncthreads();
 
-    // 2. masses and the level-1 histogram
+    // 2. masses and the level-1 histogram (logits of 8 pages per thread are
+    //    loaded together before any arithmetic)
     const float *sc = scores + (static_cast<size_t>(r) * hq + j * kGroup) * max_pages;
-    for (int p = tid; p < F; p += kSelThreads) {
-        float m = 0.f;
+    float mm[kGroup], ww[kGroup];
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g)
-            m += exp2f(sc[static_cast<size_t>(g) * max_pages + p] - sh.mmax[g]) * sh.wgt[g];
-        m = fminf(fmaxf(m, 0.f), 1.5f);            // NaN -> 0
-        const uint32_t x = __float_as_uint(m);
-        s_bits[p] = x;
-        atomicAdd(&sh.h1[l1_bin(x)], to_fx(x));
+    for (int g = 0; g < kGroup; ++g) {
+        mm[g] = sh.mmax[g];
+        ww[g] = sh.wgt[g];
+    }
+    for (int p0 = 0; p0 < F; p0 += 8 * kSelThreads) {
+        float v[8][kGroup];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int p = p0 + k * kSelThreads + tid;
+#pragma unroll
+            for (int g = 0; g < kGroup; ++g)
+                v[k][g] = p < F ? __ldcg(sc + static_cast<size_t>(g) * max_pages + p) : -INFINITY;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int p = p0 + k * kSelThreads + tid;
+            if (p < F) {
+                float m = 0.f;
+#pragma unroll
+                for (int g = 0; g < kGroup; ++g) m += exp2f(v[k][g] - mm[g]) * ww[g];
+                m = fminf(fmaxf(m, 0.f), 1.5f);        // NaN -> 0
+                const uint32_t x = __float_as_uint(m);
+                s_bits[p] = x;
+                atomicAdd(&sh.h1[l1_bin(x)], to_fx(x));
+            }
+        }
     }
     __syncthreads();
 
@@ -368,9 +394,13 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         need_tied = 0xFFFFFFFFull;
     }
 
-    // 6. ordered compaction: thread t owns a contiguous run of pages
+    // 6. ordered compaction: thread t owns a contiguous run of pages; the
+    //    physical ids of the first 8 are fetched before the scan
     const int ept = (F + kSelThreads - 1) / kSelThreads;
     const int pb = min(F, tid * ept), pe = min(F, pb + ept);
+    int32_t pref[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pref[k] = (pb + k < pe) ? __ldg(row + pb + k) : 0;
     uint32_t gt = 0, eq = 0;
     for (int p = pb; p < pe; ++p) {
         const uint32_t x = s_bits[p];
@@ -384,7 +414,23 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     unsigned long long eq_run = eq_pre;
     int pos = static_cast<int>(gt_pre + (eq_pre < need_tied ? eq_pre : need_tied));
     bool badp = false;
-    for (int p = pb; p < pe; ++p) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int p = pb + k;
+        if (p < pe) {
+            const uint32_t x = s_bits[p];
+            bool keep = x > cut;
+            if (x == cut) {
+                keep = eq_run < need_tied;
+                ++eq_run;
+            }
+            if (keep) {
+                badp |= (pref[k] < 0 || pref[k] >= num_pages);
+                out[pos++] = pref[k];
+            }
+        }
+    }
+    for (int p = pb + 8; p < pe; ++p) {
         const uint32_t x = s_bits[p];
         bool keep = x > cut;
         if (x == cut) {
