@@ -191,6 +191,27 @@ moira_status moira_decode_step_host(const moira_shape *shape, int32_t num_layers
                                     float *out_host, void *workspace, size_t ws_bytes,
                                     moira_stream_t stream);
 
+/* The coverage selection of moira_select for callers that cannot allocate
+ * device memory (a plug-in handed only its input and output buffers, a host
+ * runtime whose device memory belongs to another allocator, or a decode loop
+ * that must never call cudaMalloc).  The paper has no counterpart: it is a
+ * deployment variant of moira_select.  Arguments and results are those of
+ * moira_select without the workspace.  Its scratch (page logits and
+ * per-chunk softmax normalisers, about 4*batch*Hq*max_pages bytes) lives in
+ * a 4 MiB array compiled into the library, which every GPU that loads the
+ * library holds until the process exits; sizes that need more return
+ * MOIRA_EUNSUPPORTED and launch nothing.  The first call on a device looks
+ * up the array's device address with that device current, so make it before
+ * any stream capture.  All calls share the array: calls that overlap on the
+ * GPU (different streams, or a call still running when the next starts on
+ * another stream) race; calls in order on one stream do not.  Device-side
+ * range problems are skipped or clamped as in moira_select, but the status
+ * word is internal and not reported.  Never calls cudaMalloc or cudaFree. */
+moira_status moira_select_noalloc(const moira_shape *shape, const void *q, const void *summ,
+                                  const int32_t *page_table, const int32_t *seq_lens,
+                                  int32_t batch, int32_t max_pages, float gamma, float sm_scale,
+                                  int32_t *lists, int32_t *lengths, moira_stream_t stream);
+
 /* Synchronise `stream`, copy the device status word (MOIRA_DEV_* bits) to
  * *status_out (HOST pointer) and clear it when `clear` is non-zero.  A host
  * call: never issue it while `stream` is being captured. */

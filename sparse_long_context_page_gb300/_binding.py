@@ -30,7 +30,8 @@ MAX_PAGES_PER_SEQ, MAX_UNITS = 32768, 4096
 # every symbol include/moira.h declares
 EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summaries",
            "moira_select", "moira_attend", "moira_decode_step", "moira_decode_step_host",
-           "moira_read_device_status", "moira_attend_grid_blocks", "moira_status_string")
+           "moira_read_device_status", "moira_attend_grid_blocks", "moira_status_string",
+           "moira_select_noalloc")
 
 
 class MoiraError(RuntimeError):
@@ -90,6 +91,9 @@ def load_library(build_if_missing: bool = True):
     lib.moira_read_device_status.restype = ctypes.c_int
     lib.moira_attend_grid_blocks.argtypes = []
     lib.moira_attend_grid_blocks.restype = _i32
+    lib.moira_select_noalloc.argtypes = [sp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
+                                         ctypes.c_float, _vp, _vp, _vp]
+    lib.moira_select_noalloc.restype = ctypes.c_int
     lib.moira_status_string.argtypes = [ctypes.c_int]
     lib.moira_status_string.restype = ctypes.c_char_p
     _lib = lib
