@@ -73,7 +73,7 @@ typedef enum moira_status {
 #define MOIRA_HEAD_DIM 128               /* d */
 #define MOIRA_PAGE_SIZE 16               /* S, tokens per page */
 #define MOIRA_GROUP 4                    /* G = Hq / Hkv */
-#define MOIRA_MAX_PAGES_PER_SEQ 32768    /* max_pages: 512k tokens per request */
+#define MOIRA_MAX_PAGES_PER_SEQ 8192     /* max_pages: 128k tokens per request */
 #define MOIRA_MAX_UNITS 4096             /* batch * num_kv_heads */
 
 /* Model / cache geometry.  This build requires head_dim == 128,
@@ -196,7 +196,7 @@ moira_status moira_decode_step_host(const moira_shape *shape, int32_t num_layers
  * runtime whose device memory belongs to another allocator, or a decode loop
  * that must never call cudaMalloc).  The paper has no counterpart: it is a
  * deployment variant of moira_select.  Arguments and results are those of
- * moira_select without the workspace.  Its scratch (page logits and
+ * moira_select without the workspace.  Its scratch (page weights and
  * per-chunk softmax normalisers, about 4*batch*Hq*max_pages bytes) lives in
  * a 4 MiB array compiled into the library, which every GPU that loads the
  * library holds until the process exits; sizes that need more return

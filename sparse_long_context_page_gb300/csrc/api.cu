@@ -2,6 +2,7 @@
 // carving, TMA descriptor encoding and kernel launches.  Nothing here
 // allocates, synchronises or reads device memory inside select/attend/step.
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -25,7 +26,21 @@ int current_sm_count()
     return sms;
 }
 
-int attend_blocks() { return current_sm_count() * attend_blocks_per_sm(); }
+// The attention grid is a fixed multiple of the SM count: blocks_per_sm
+// resident blocks per SM times `waves` (MOIRA_ATTEND_WAVES, default 1).  More
+// waves give smaller page ranges, so SMs that finish early pick up pending
+// blocks; the value is read once per process.
+int attend_waves()
+{
+    static int waves = [] {
+        const char *e = std::getenv("MOIRA_ATTEND_WAVES");
+        const int v = e ? std::atoi(e) : 1;
+        return v < 1 ? 1 : (v > 16 ? 16 : v);
+    }();
+    return waves;
+}
+
+int attend_blocks() { return current_sm_count() * attend_blocks_per_sm() * attend_waves(); }
 
 moira_status check_shape(const moira_shape *s)
 {
@@ -140,6 +155,7 @@ moira_status attend_impl(const moira_shape *shape, const void *q, const void *k_
     a.out = out;
     a.partials = reinterpret_cast<float *>(w + L.partials);
     a.counters = reinterpret_cast<uint32_t *>(w + L.counters);
+    a.gcounters = reinterpret_cast<uint32_t *>(w + L.gcounters);
     a.status = reinterpret_cast<uint32_t *>(w + L.status);
     a.hq = shape->num_q_heads;
     a.hkv = shape->num_kv_heads;

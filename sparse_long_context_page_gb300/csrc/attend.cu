@@ -9,9 +9,11 @@
 //   memory); n = min(grid, W) active blocks; block b takes pages
 //   [b*W/n, (b+1)*W/n) of the lists laid end to end and splits its range at
 //   list boundaries into segments.  A segment's partial goes to slot b + u
-//   (u = list index), which is unique.  The last block to finish a list
-//   (arrival counter, self-resetting) merges that list's partials; a list
-//   held by one block is written directly.
+//   (u = list index), which is unique.  Partials are merged by
+//   log-sum-exp in two levels: the last block to finish in each group of 16
+//   consecutive blocks of a list merges the group, and the last group to
+//   finish writes the output (arrival counters, self-resetting); a list held
+//   by one block is written directly.
 //
 // Data path per block (1 producer warp + 4 consumer warps, 2 blocks per SM):
 //   the producer looks up a batch of 32 list entries while it issues the
@@ -58,6 +60,53 @@ __host__ __device__ inline size_t attend_smem_bytes(int units)
 {
     return 1024 + static_cast<size_t>(NS) * kSlotBytes + sizeof(AttendSmem<NS>) +
            sizeof(int) * static_cast<size_t>(units + 1);
+}
+
+constexpr int kMergeSpan = 16;            // partials merged per batch (and per group)
+
+// Online log-sum-exp merge of `count` partials stored at slots first,
+// first + stride, ... for this thread's head h and dims d0..d0+3: returns the
+// merged (max, sum, unnormalised o).  All loads of a batch are in flight
+// together; L2-only loads because other blocks wrote the partials.
+__device__ __forceinline__ void merge_partials(const float *partials, int first, int stride,
+                                               int count, int h, int d0, float &Mout,
+                                               float &Lout, float4 &Oout)
+{
+    float Mrun = -INFINITY, la = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k0 = 0; k0 < count; k0 += kMergeSpan) {
+        float mv[kMergeSpan], lv[kMergeSpan];
+        float4 ov[kMergeSpan];
+#pragma unroll
+        for (int k = 0; k < kMergeSpan; ++k) {
+            mv[k] = -INFINITY;
+            lv[k] = 0.f;
+            ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k0 + k < count) {
+                const float *pp = partials + static_cast<size_t>(first + (k0 + k) * stride) * kPartFloats;
+                mv[k] = __ldcg(pp + h);
+                lv[k] = __ldcg(pp + kGroup + h);
+                ov[k] = __ldcg(reinterpret_cast<const float4 *>(pp + 2 * kGroup + h * kHeadDim + d0));
+            }
+        }
+        float mb = Mrun;
+#pragma unroll
+        for (int k = 0; k < kMergeSpan; ++k) mb = fmaxf(mb, mv[k]);
+        const float ms = mb == -INFINITY ? 0.f : mb;
+        const float sc = exp2f(Mrun - ms);
+        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
+        la *= sc;
+#pragma unroll
+        for (int k = 0; k < kMergeSpan; ++k) {
+            const float e = exp2f(mv[k] - ms);
+            acc.x += e * ov[k].x; acc.y += e * ov[k].y; acc.z += e * ov[k].z; acc.w += e * ov[k].w;
+            la += e * lv[k];
+        }
+        Mrun = mb;
+    }
+    Mout = Mrun;
+    Lout = la;
+    Oout = acc;
 }
 
 // Largest b with floor(b*W/n) <= g: the block whose range holds page g.
@@ -391,59 +440,62 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
                 const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
                 *reinterpret_cast<float4 *>(orow) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
             } else {
+                // Two-level merge.  Blocks bfirst..blast of this list form groups
+                // of kMergeSpan; the last block to finish in a group merges the
+                // group's partials into the group's first slot, and the last
+                // group to finish merges the group partials into the output.
+                // Both merges read at most kMergeSpan partials in one batch.
                 float *part = a.partials + static_cast<size_t>(b + u) * kPartFloats;
                 *reinterpret_cast<float4 *>(part + 2 * kGroup + h * kHeadDim + d0) = o;
                 if ((tid & 31) == 0) {
                     part[h] = M;
                     part[kGroup + h] = Lsum;
                 }
-                __threadfence();
+                // the CTA barrier makes every thread's partial visible to thread 0,
+                // whose acq_rel atomic publishes it and acquires the others
                 asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                if (tid == 0) {
-                    const unsigned prev = atomicAdd(&a.counters[u], 1u);
-                    sm.flag = (prev == static_cast<unsigned>(blast - bfirst)) ? 1 : 0;
-                }
-                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                if (sm.flag) {
-                    // last block of this list: merge every segment's partial in
-                    // one online pass, kMergeBatch segments' loads in flight at once
-                    __threadfence();
-                    constexpr int kMergeBatch = 16;
-                    float Mrun = -INFINITY, la = 0.f;
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int b0 = bfirst; b0 <= blast; b0 += kMergeBatch) {
-                        float mv[kMergeBatch], lv[kMergeBatch];
-                        float4 ov[kMergeBatch];
-#pragma unroll
-                        for (int k = 0; k < kMergeBatch; ++k) {
-                            mv[k] = -INFINITY;
-                            lv[k] = 0.f;
-                            ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (b0 + k <= blast) {
-                                const float *pp = a.partials + static_cast<size_t>(b0 + k + u) * kPartFloats;
-                                mv[k] = __ldcg(pp + h);
-                                lv[k] = __ldcg(pp + kGroup + h);
-                                ov[k] = __ldcg(reinterpret_cast<const float4 *>(pp + 2 * kGroup + h * kHeadDim + d0));
-                            }
-                        }
-                        float mb = Mrun;
-#pragma unroll
-                        for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, mv[k]);
-                        const float ms = mb == -INFINITY ? 0.f : mb;
-                        const float sc = exp2f(Mrun - ms);
-                        acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
-                        la *= sc;
-#pragma unroll
-                        for (int k = 0; k < kMergeBatch; ++k) {
-                            const float e = exp2f(mv[k] - ms);
-                            acc.x += e * ov[k].x; acc.y += e * ov[k].y; acc.z += e * ov[k].z; acc.w += e * ov[k].w;
-                            la += e * lv[k];
-                        }
-                        Mrun = mb;
+                const int gfirst = bfirst + (b - bfirst) / kMergeSpan * kMergeSpan;
+                const int gn = min(kMergeSpan, blast - gfirst + 1);
+                if (gn > 1) {
+                    if (tid == 0) {
+                        const uint32_t prev = atomic_add_acq_rel_gpu(&a.gcounters[gfirst + u], 1u);
+                        sm.flag = (prev == static_cast<uint32_t>(gn - 1)) ? 1 : 0;
                     }
-                    const float inv = la > 0.f ? 1.f / la : 0.f;
-                    *reinterpret_cast<float4 *>(orow) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-                    if (tid == 0) a.counters[u] = 0u;      // ready for the next launch
+                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                    if (sm.flag) {
+                        float gm, gl;
+                        float4 go;
+                        merge_partials(a.partials, gfirst + u, 1, gn, h, d0, gm, gl, go);
+                        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                        float *gp = a.partials + static_cast<size_t>(gfirst + u) * kPartFloats;
+                        *reinterpret_cast<float4 *>(gp + 2 * kGroup + h * kHeadDim + d0) = go;
+                        if ((tid & 31) == 0) {
+                            gp[h] = gm;
+                            gp[kGroup + h] = gl;
+                        }
+                        if (tid == 0) a.gcounters[gfirst + u] = 0u;     // ready for the next launch
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                } else {
+                    if (tid == 0) sm.flag = 1;                     // a group of one is its own merge
+                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                }
+                if (sm.flag) {
+                    const int ngroups = (blast - bfirst) / kMergeSpan + 1;
+                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                    if (tid == 0) {
+                        const uint32_t prev = atomic_add_acq_rel_gpu(&a.counters[u], 1u);
+                        sm.flag = (prev == static_cast<uint32_t>(ngroups - 1)) ? 1 : 0;
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+                    if (sm.flag) {
+                        float fm, fl;
+                        float4 fo;
+                        merge_partials(a.partials, bfirst + u, kMergeSpan, ngroups, h, d0, fm, fl, fo);
+                        const float inv = fl > 0.f ? 1.f / fl : 0.f;
+                        *reinterpret_cast<float4 *>(orow) = make_float4(fo.x * inv, fo.y * inv, fo.z * inv, fo.w * inv);
+                        if (tid == 0) a.counters[u] = 0u;          // ready for the next launch
+                    }
                 }
             }
             asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");

@@ -12,7 +12,7 @@ namespace moira {
 constexpr int kHeadDim = 128;           // d
 constexpr int kPageSize = 16;           // S
 constexpr int kGroup = 4;               // G = Hq / Hkv
-constexpr int kMaxPagesPerSeq = 32768;
+constexpr int kMaxPagesPerSeq = 8192;       // the selection stages a whole group in shared memory
 constexpr int kMaxUnits = 4096;
 
 constexpr uint32_t kDevBadPage = 0x1u;
@@ -24,15 +24,24 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // ---- workspace layout ------------------------------------------------------
 // [0, 256)                    : uint32 status word (+ padding)
-// counters                    : uint32 [kMaxUnits]  merge arrival counters
-// scores                      : fp32 [batch][Hq][max_pages]  (log2-domain logits)
-// chunk stats                 : fp32 [batch][Hq][n_chunks][2] (max, sum 2^(s-max))
+// counters                    : uint32 [kMaxUnits]  per-list merge arrival counters
+// group counters              : uint32 [n_blocks + units] per-group arrival counters
+// weights                     : fp32 [batch][Hq][ld]   chunk-relative page weights 2^(s - M_c)
+// chunk stats                 : fp32 [batch][Hq][ldc]  (M_c, sum 2^(s - M_c)) per 32-page chunk
 // partials                    : fp32 [n_blocks + units][kPartFloats]
 constexpr int kScoreChunk = 32;                    // pages per score block
 constexpr int kPartFloats = 2 * kGroup + kGroup * kHeadDim;   // m[G], l[G], o[G][d]
 
+// Row strides: weights rows padded to 32 pages, chunk-stat rows to 16 bytes.
+__host__ __device__ inline int weights_ld(int max_pages) { return (max_pages + 31) / 32 * 32; }
+__host__ __device__ inline int chunks_ld(int max_pages)
+{
+    const int nch = (max_pages + kScoreChunk - 1) / kScoreChunk;
+    return (2 * nch + 3) / 4 * 4;
+}
+
 struct WsLayout {
-    size_t status, counters, scores, chunks, partials, total;
+    size_t status, counters, gcounters, scores, chunks, partials, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -43,9 +52,9 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int hq, int max_pages, 
     size_t o = 0;
     w.status = o;   o += 256;
     w.counters = o; o = align_up(o + sizeof(uint32_t) * kMaxUnits, 256);
-    w.scores = o;   o = align_up(o + sizeof(float) * (size_t)batch * hq * max_pages, 256);
-    int nch = (max_pages + kScoreChunk - 1) / kScoreChunk;
-    w.chunks = o;   o = align_up(o + sizeof(float) * 2 * (size_t)batch * hq * nch, 256);
+    w.gcounters = o; o = align_up(o + sizeof(uint32_t) * (size_t)(blocks + units), 256);
+    w.scores = o;   o = align_up(o + sizeof(float) * (size_t)batch * hq * weights_ld(max_pages), 256);
+    w.chunks = o;   o = align_up(o + sizeof(float) * (size_t)batch * hq * chunks_ld(max_pages), 256);
     w.partials = o; o = align_up(o + sizeof(float) * kPartFloats * (size_t)(blocks + units), 256);
     w.total = o;
     return w;
@@ -74,6 +83,17 @@ __device__ __forceinline__ uint64_t globaltimer()
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Atomic add at GPU scope with acquire-release semantics: the writes this
+// thread has observed (e.g. a CTA's writes made visible to it by a CTA
+// barrier) are released before the add, and the caller acquires what earlier
+// releasers published.  Returns the previous value.
+__device__ __forceinline__ uint32_t atomic_add_acq_rel_gpu(uint32_t *addr, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
 }
 
 // ---- mbarrier ------------------------------------------------------------------
@@ -149,6 +169,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// 1-D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory, counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
         : "memory");
 }
 

@@ -28,6 +28,7 @@ struct AttendArgs {
     float *out;
     float *partials;
     uint32_t *counters;
+    uint32_t *gcounters;
     uint32_t *status;
     int hq, hkv, units, max_pages;
     long long num_pages;

@@ -4,7 +4,7 @@
 // handed only their input and output buffers, runtimes whose device memory
 // is owned by another allocator, or a decode loop that must never call
 // cudaMalloc (it synchronises the device and is not allowed in every stream
-// capture mode).  moira_select needs scratch for the page logits and the
+// capture mode).  moira_select needs scratch for the page weights and the
 // per-chunk softmax normalisers; this entry point keeps that scratch in a
 // fixed array compiled into the library instead, so it allocates nothing.
 //
@@ -77,13 +77,12 @@ extern "C" moira_status moira_select_noalloc(const moira_shape *shape, const voi
     if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
     if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
 
-    // scratch: status word | logits [batch][Hq][max_pages] | chunk (max, sum)
+    // scratch: status word | page weights [batch][Hq][ld] | chunk (max, sum) [batch][Hq][ldc]
     const int hq = shape->num_q_heads;
-    const int nch = (max_pages + kScoreChunk - 1) / kScoreChunk;
     const size_t off_scores = 256;
     const size_t off_chunks =
-        align_up(off_scores + sizeof(float) * static_cast<size_t>(batch) * hq * max_pages, 256);
-    const size_t need = off_chunks + sizeof(float) * 2 * static_cast<size_t>(batch) * hq * nch;
+        align_up(off_scores + sizeof(float) * static_cast<size_t>(batch) * hq * weights_ld(max_pages), 256);
+    const size_t need = off_chunks + sizeof(float) * static_cast<size_t>(batch) * hq * chunks_ld(max_pages);
     if (need > kNoAllocBytes) return MOIRA_EUNSUPPORTED;     // beyond the compiled-in scratch
 
     void *base = nullptr;

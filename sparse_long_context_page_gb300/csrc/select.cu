@@ -4,16 +4,22 @@
 // mass reaches gamma.
 //
 // Two kernels per layer:
-//  k_score  : all SMs stream the page summaries once (16-byte loads, the G
-//             query rows of a KV head sharing each load) and write the
-//             log2-domain page logits plus per-chunk (max, sum 2^(s-max)).
-//  k_select : one 1024-thread block per (request, KV head).  It merges the
-//             chunk normalisers, forms m_p = (1/G) sum_h softmax_p(s_hp),
-//             finds the cut mass by a radix descent over the fp32 bit
-//             patterns (mass histograms kept as 2^-31 fixed-point integer
-//             sums in native 32-bit shared atomics, so the result does not
-//             depend on atomic order), then compacts the kept pages in
-//             ascending logical order.
+//  k_score  : all SMs stream the page summaries once (bulk copies into shared
+//             memory) and compute the page logits on the tensor cores, the G
+//             query rows of a KV head sharing every summary.  Per chunk of 32
+//             pages and query head it stores the chunk max M_c and sum
+//             Z_c = sum_p 2^(s_p - M_c), and per page the chunk-relative
+//             weight e_p = 2^(s_p - M_c) (log2-domain logits).
+//  k_select : one 1024-thread block per (request, KV head).  It bulk-copies
+//             the group's weights and chunk statistics into shared memory,
+//             merges the normalisers, forms
+//                 m_p = (1/G) sum_h e_hp 2^(M_hc - M_h) / Z_h
+//                     = (1/G) sum_h softmax_p(s_h.)
+//             and finds the cut mass by a radix descent over the fp32 bit
+//             patterns (mass histograms kept as 2^-31 fixed-point integer sums
+//             in native 32-bit shared atomics, so the result does not depend
+//             on atomic order), then compacts the kept pages in ascending
+//             logical order with warp ballots.
 // Top-p over pages needs the global softmax and a cumulative sum ("Faster
 // Flash Decoding", section 1 and figure 1); the histogram descent replaces a
 // full sort.
@@ -26,122 +32,135 @@ namespace moira {
 // k_score
 // ---------------------------------------------------------------------------
 constexpr int kScoreThreads = 256;        // 8 warps
-constexpr int kScoreItemsPerLane = 8;     // 32 pages * Hkv(<= 8) / 32 items per pass
+constexpr int kScoreMaxItems = 2;         // (KV head, half) work items per warp for Hkv <= 8
 
-// Lane layout: 8 lanes per (page, KV head) item, 16 dimensions (32 bytes) per
-// lane; 4 items per warp and 32 per block pass.  Because 32 is a multiple of
-// Hkv, a lane always serves the same KV head and keeps that head's G=4 query
-// slices (64 floats) in registers for the whole block.
+// One block scores kScoreChunk (32) consecutive full pages of one request for
+// every KV head.  The page-table slice and the queries are read first; each
+// listed page's summaries (Hkv x 256 B, contiguous per physical page) then
+// arrive by 1-D bulk copies on one mbarrier, at a padded shared-memory stride
+// of Hkv*256+16 bytes so that 8 consecutive pages fall in different banks.
+// Logits come from the tensor cores: for KV head j and 16 pages,
+//   S^T[h][p] = sum_d q_{4j+h}[d] * kbar_p[d]   (mma.m16n8k16, fp32 accumulate)
+// with A = the group's 4 query rows (repeated in rows 4-7) and B = the
+// summaries via ldmatrix, i.e. 8 k-steps x 2 MMAs per (head, 16 pages).
 __global__ void __launch_bounds__(kScoreThreads, 2) k_score(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ summ,
     const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
-    int max_pages, long long num_pages, float scale_log2, float *__restrict__ scores,
-    float *__restrict__ chunks, int n_chunks, uint32_t *status)
+    int max_pages, int ld, long long num_pages, float scale_log2, float *__restrict__ weights,
+    float *__restrict__ chunks, int ldc, uint32_t *status)
 {
-    __shared__ float s_s[32 * kScoreChunk];   // [Hq <= 32][32 pages]
+    extern __shared__ __align__(128) uint8_t s_summ[];     // [32 pages][stride]
+    __shared__ __align__(16) float s_s[32 * kScoreChunk];  // [Hq <= 32][32 pages] logits
+    __shared__ int s_phys[kScoreChunk];
+    __shared__ __align__(8) unsigned long long s_bar;
     pdl_trigger();
     pdl_wait();                               // q and the score buffers follow earlier kernels
     const int r = blockIdx.y;
     const int chunk = blockIdx.x;
-    int L = seq_lens[r];
-    L = L < 0 ? 0 : (L > max_pages * kPageSize ? max_pages * kPageSize : L);
-    const int F = L / kPageSize;
     const int p0 = chunk * kScoreChunk;
-    if (p0 >= F) return;
-    const int np = min(kScoreChunk, F - p0);
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane & 7;
-    const int j = (warp * 4 + (lane >> 3)) % hkv;
+    const uint32_t page_bytes = static_cast<uint32_t>(hkv) * kHeadDim * 2;
+    const uint32_t stride = page_bytes + 16;
+    const uint32_t bar = smem_u32(&s_bar);
+    const int hrow = (lane >> 2) & 3;
+    const int n_work = hkv * 2;               // (KV head, 16-page half)
 
-    float qr[kGroup][16];
+    // loads that do not need the sequence length first: page ids and the
+    // query fragments of this warp's work items
+    int L = seq_lens[r];
+    const int pid_pre = (threadIdx.x < kScoreChunk && p0 + static_cast<int>(threadIdx.x) < max_pages)
+                            ? __ldg(page_table + static_cast<size_t>(r) * max_pages + p0 + threadIdx.x)
+                            : -1;
+    uint32_t aq[kScoreMaxItems][8][2];
 #pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-        const uint4 *qp = reinterpret_cast<const uint4 *>(
-            q + (static_cast<size_t>(r) * hq + j * kGroup + g) * kHeadDim + sub * 16);
-        const uint4 a = __ldg(qp), b = __ldg(qp + 1);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    for (int it = 0; it < kScoreMaxItems; ++it) {
+        const int wi = warp + it * (kScoreThreads / 32);
+        const int j = wi < n_work ? (wi >> 1) : 0;
+        const uint16_t *qrow = q + (static_cast<size_t>(r) * hq + j * kGroup + hrow) * kHeadDim + 2 * (lane & 3);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            qr[g][2 * i] = bf16_lo(w[i]);
-            qr[g][2 * i + 1] = bf16_hi(w[i]);
+        for (int ks = 0; ks < 8; ++ks) {
+            aq[it][ks][0] = wi < n_work ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)) : 0u;
+            aq[it][ks][1] = wi < n_work ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)) : 0u;
         }
     }
+    L = L < 0 ? 0 : (L > max_pages * kPageSize ? max_pages * kPageSize : L);
+    const int F = L / kPageSize;
+    if (p0 >= F) return;
+    const int np = min(kScoreChunk, F - p0);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    if (threadIdx.x < kScoreChunk) s_phys[threadIdx.x] = static_cast<int>(threadIdx.x) < np ? pid_pre : -1;
+    __syncthreads();
+    if (warp == 0) {
+        const int phys = s_phys[lane];
+        const bool ok = lane < np && phys >= 0 && phys < num_pages;
+        const unsigned okm = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) mbar_arrive_expect_tx(bar, __popc(okm) * page_bytes);
+        __syncwarp();
+        if (ok)
+            bulk_load(smem_u32(s_summ + lane * stride),
+                      summ + static_cast<size_t>(phys) * hkv * kHeadDim, page_bytes, bar);
+        if (lane < np && !ok) raise_status(status, kDevBadPage);
+    }
+    if (!mbar_wait(bar, 0) && threadIdx.x == 0) raise_status(status, kDevTimeout);
 
-    const int n_items = np * hkv;
-    const int32_t *row = page_table + static_cast<size_t>(r) * max_pages + p0;
-    // two passes of 4 items per lane: 4 x 32 B loads in flight per lane
 #pragma unroll
-    for (int k0 = 0; k0 < kScoreItemsPerLane; k0 += 4) {
-        if (warp * 4 + 32 * k0 >= n_items) break;            // warp-uniform
-        uint4 buf[4][2];
-        bool bad[4];
+    for (int it = 0; it < kScoreMaxItems; ++it) {
+        const int wi = warp + it * (kScoreThreads / 32);
+        if (wi >= n_work) break;                              // warp-uniform
+        const int j = wi >> 1, half = wi & 1;
+        float acc[2][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int it = warp * 4 + (lane >> 3) + 32 * (k0 + k);
-            bad[k] = false;
-            buf[k][0] = buf[k][1] = make_uint4(0, 0, 0, 0);
-            if (it < n_items) {
-                const int phys = __ldg(row + it / hkv);
-                if (phys < 0 || phys >= num_pages) {
-                    bad[k] = true;
-                } else {
-                    const uint4 *sp = reinterpret_cast<const uint4 *>(
-                        summ + (static_cast<size_t>(phys) * hkv + j) * kHeadDim + sub * 16);
-                    buf[k][0] = __ldg(sp);
-                    buf[k][1] = __ldg(sp + 1);
-                }
-            }
+        for (int x = 0; x < 2; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+        // ldmatrix rows: matrices (pages 0-7, dims +0), (pages 0-7, +8), (pages 8-15, +0), (8-15, +8)
+        const int prow = half * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const uint32_t rbase = smem_u32(s_summ) + prow * stride + j * kHeadDim * 2 + (((lane >> 3) & 1) << 4);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(rbase + ks * 32, b0, b1, b2, b3);
+            mma_bf16_16816(acc[0], aq[it][ks][0], 0u, aq[it][ks][1], 0u, b0, b1);
+            mma_bf16_16816(acc[1], aq[it][ks][0], 0u, aq[it][ks][1], 0u, b2, b3);
         }
+        if (lane < 16) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int it = warp * 4 + (lane >> 3) + 32 * (k0 + k);
-            if (warp * 4 + 32 * (k0 + k) >= n_items) break;  // warp-uniform
-            const uint32_t w[8] = {buf[k][0].x, buf[k][0].y, buf[k][0].z, buf[k][0].w,
-                                   buf[k][1].x, buf[k][1].y, buf[k][1].z, buf[k][1].w};
-            float dot[kGroup];
-#pragma unroll
-            for (int g = 0; g < kGroup; ++g) dot[g] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float x0 = bf16_lo(w[i]), x1 = bf16_hi(w[i]);
-#pragma unroll
-                for (int g = 0; g < kGroup; ++g)
-                    dot[g] = fmaf(qr[g][2 * i + 1], x1, fmaf(qr[g][2 * i], x0, dot[g]));
-            }
-#pragma unroll
-            for (int g = 0; g < kGroup; ++g) {
-                dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 1);
-                dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 2);
-                dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 4);
-            }
-            if (sub == 0 && it < n_items) {
-                const int pl = it / hkv;
-                if (bad[k]) raise_status(status, kDevBadPage);
-#pragma unroll
-                for (int g = 0; g < kGroup; ++g) {
-                    const int h = j * kGroup + g;
-                    const float sv = bad[k] ? -INFINITY : dot[g] * scale_log2;
-                    s_s[h * kScoreChunk + pl] = sv;
-                    scores[(static_cast<size_t>(r) * hq + h) * max_pages + p0 + pl] = sv;
-                }
+            for (int nt = 0; nt < 2; ++nt) {
+                const int pl = half * 16 + nt * 8 + 2 * (lane & 3);
+                const int h = j * kGroup + hrow;
+                float s0 = acc[nt][0] * scale_log2, s1 = acc[nt][1] * scale_log2;
+                if (pl >= np || s_phys[pl] < 0 || s_phys[pl] >= num_pages) s0 = -INFINITY;
+                if (pl + 1 >= np || s_phys[pl + 1] < 0 || s_phys[pl + 1] >= num_pages) s1 = -INFINITY;
+                *reinterpret_cast<float2 *>(&s_s[h * kScoreChunk + pl]) = make_float2(s0, s1);
             }
         }
     }
     __syncthreads();
-    // per-head (max, sum 2^(s - max)) over this chunk
-    for (int h = warp; h < hq; h += kScoreThreads / 32) {
-        const float v = lane < np ? s_s[h * kScoreChunk + lane] : -INFINITY;
-        float mx = v;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float e = (lane < np && mx != -INFINITY) ? exp2f(v - mx) : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) e += __shfl_xor_sync(0xffffffffu, e, o);
-        if (lane == 0) {
-            float *c = chunks + ((static_cast<size_t>(r) * hq + h) * n_chunks + chunk) * 2;
-            c[0] = mx;
-            c[1] = e;
+    // per query head: chunk max, chunk sum and the chunk-relative weights;
+    // 8 lanes per head (4 pages each), 4 heads per warp instruction
+    for (int h0 = warp * 4; h0 < hq; h0 += 4 * (kScoreThreads / 32)) {
+        const int h = h0 + (lane >> 3);
+        const int sub = lane & 7;
+        float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (h < hq) v = *reinterpret_cast<const float4 *>(&s_s[h * kScoreChunk + sub * 4]);
+        float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        const float ms = mx == -INFINITY ? 0.f : mx;
+        const float4 e = make_float4(exp2f(v.x - ms), exp2f(v.y - ms), exp2f(v.z - ms), exp2f(v.w - ms));
+        float sum = (e.x + e.y) + (e.z + e.w);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if (h < hq) {
+            float *dst = weights + (static_cast<size_t>(r) * hq + h) * ld + p0 + sub * 4;
+            *reinterpret_cast<float4 *>(dst) = e;          // pages past F are never read
+            if (sub == 0) {
+                float *c = chunks + (static_cast<size_t>(r) * hq + h) * ldc + chunk * 2;
+                *reinterpret_cast<float2 *>(c) = make_float2(mx, sum);
+            }
         }
     }
 }
@@ -151,6 +170,7 @@ __global__ void __launch_bounds__(kScoreThreads, 2) k_score(
 // ---------------------------------------------------------------------------
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelStripes = kMaxPagesPerSeq / kSelThreads;   // stripes of 1024 pages
 // Level-1 bins: the fp32 bit pattern >> 16 (exponent + 7 fraction bits, 128
 // bins per octave) for masses in [2^-32, 2); bin 0 gathers everything below.
 constexpr uint32_t kKeyLo = 95u << 7;
@@ -168,15 +188,15 @@ __device__ __forceinline__ uint32_t l1_hi(int b) { return b == 0 ? (kKeyLo << 16
 
 // Mass as a 2^-31 fixed-point integer.  Masses sum to 1 (to fp32 rounding),
 // so every histogram bin and every partial sum fits in 32 bits; rounding each
-// mass costs at most 2^-32, i.e. < 1e-5 over 32768 pages.
+// mass costs at most 2^-32, i.e. < 1e-5 over 16384 pages.
 __device__ __forceinline__ uint32_t to_fx(uint32_t x)
 {
     return __float2uint_rn(__uint_as_float(x) * 0x1p31f);
 }
 
 // Exclusive scan over the block in thread order; *total gets the sum.
-__device__ unsigned long long block_excl_scan(unsigned long long v, unsigned long long *s_warp,
-                                              unsigned long long *total)
+__device__ unsigned long long sel_excl_scan(unsigned long long v, unsigned long long *s_warp,
+                                            unsigned long long *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned long long x = v;
@@ -203,104 +223,173 @@ __device__ unsigned long long block_excl_scan(unsigned long long v, unsigned lon
     return off + x - v;
 }
 
+constexpr int kCand = 2048;                 // crossing-bin pages refined by one warp
+constexpr int kPairMax = 256;               // crossing-bin pages resolved pairwise
+
 struct SelectShared {
     uint32_t h1[kL1Bins];
     uint32_t h2[kL2Bins];
+    uint32_t cand[kCand];                   // mass bits of the crossing bin's pages
+    uint16_t cand_idx[kCand];               // their page indices (pairwise path only)
+    int ncand;
     unsigned long long scan[32];
     unsigned long long above;
+    unsigned long long cnt[kSelStripes * kSelWarps];    // (stripe, warp): gt | eq << 32
     uint32_t lo, hi;
     int found;
-    int kept;
+    float red[kSelWarps];
+    float red2[kSelWarps];
     float mmax[kGroup];
-    float wgt[kGroup];
+    float zinv[kGroup];
+    unsigned long long bar;
 };
 
+// Dynamic shared memory of k_select: the group's weights, its chunk
+// statistics, per-chunk factors and the mass bit patterns.
+// Every row starts on a 16-byte boundary (bulk-copy destinations must).
+__host__ __device__ inline size_t select_smem_bytes(int max_pages, int ldc)
+{
+    const size_t wld = static_cast<size_t>(weights_ld(max_pages));
+    return sizeof(float) * kGroup * wld + sizeof(float) * kGroup * static_cast<size_t>(ldc) +
+           sizeof(float4) * static_cast<size_t>(ldc / 2) + sizeof(uint32_t) * wld;
+}
+
 __global__ void __launch_bounds__(kSelThreads) k_select(
-    const float *__restrict__ scores, const float *__restrict__ chunks,
+    const float *__restrict__ weights, const float *__restrict__ chunks,
     const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
-    int max_pages, int n_chunks, long long num_pages, unsigned long long gamma_fx, int dense,
+    int max_pages, int ld, int ldc, long long num_pages, unsigned long long gamma_fx, int dense,
     int32_t *__restrict__ lists, int32_t *__restrict__ lengths, uint32_t *status)
 {
-    extern __shared__ __align__(16) uint32_t s_bits[];       // [max_pages] mass bit patterns
+    extern __shared__ __align__(16) float s_dyn[];
     __shared__ SelectShared sh;
+    const int wld = ld;                                            // 32-page padded rows
+    float *s_w = s_dyn;                                            // [G][wld] page weights
+    float *s_c = s_w + kGroup * wld;                               // [G][ldc] (max, sum) pairs
+    float4 *s_f = reinterpret_cast<float4 *>(s_c + kGroup * ldc);  // [ldc/2] per-chunk factors
+    uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_f + ldc / 2);   // [wld] mass bits
+
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_trigger();
-    pdl_wait();                               // scores and chunk stats come from k_score
+    pdl_wait();                               // weights and chunk stats come from k_score
     const int u = blockIdx.x;
     const int r = u / hkv, j = u % hkv;
+    const int32_t *row = page_table + static_cast<size_t>(r) * max_pages;
+    int32_t *out = lists + static_cast<size_t>(u) * max_pages;
+    const uint32_t bar = smem_u32(&sh.bar);
     int L = seq_lens[r];
+    // page ids of this thread's pages (page k*1024 + tid) in flight early
+    int32_t pref[kSelStripes];
+#pragma unroll
+    for (int k = 0; k < kSelStripes; ++k) {
+        const int p = k * kSelThreads + tid;
+        pref[k] = p < max_pages ? __ldg(row + p) : 0;
+    }
+    const int32_t tail_pre = (tid == 0 && L > 0 && L <= max_pages * kPageSize && (L % kPageSize) != 0)
+                                 ? __ldg(row + L / kPageSize) : 0;
     if (L < 0 || L > max_pages * kPageSize) {
         if (tid == 0) raise_status(status, kDevBadLen);
         L = L < 0 ? 0 : max_pages * kPageSize;
     }
     const int F = L / kPageSize, T = (L % kPageSize) != 0;
-    const int32_t *row = page_table + static_cast<size_t>(r) * max_pages;
-    int32_t *out = lists + static_cast<size_t>(u) * max_pages;
-
-    if (dense || F == 0) {                         // every page, no estimate
+    if (dense || F == 0) {                    // every page, no estimate
         for (int p = tid; p < F + T; p += kSelThreads) out[p] = row[p];
         if (tid == 0) lengths[u] = F + T;
         return;
     }
-
-    // 1. merge the chunk normalisers of the group's G heads
     const int nch = (F + kScoreChunk - 1) / kScoreChunk;
-    if (warp < kGroup) {
-        const float *c = chunks + (static_cast<size_t>(r) * hq + j * kGroup + warp) * n_chunks * 2;
-        float mx = -INFINITY;
-        for (int i = lane; i < nch; i += 32) mx = fmaxf(mx, c[2 * i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float z = 0.f;
-        if (mx != -INFINITY)
-            for (int i = lane; i < nch; i += 32)
-                if (c[2 * i] != -INFINITY) z += c[2 * i + 1] * exp2f(c[2 * i] - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        if (lane == 0) {
-            sh.mmax[warp] = mx == -INFINITY ? 0.f : mx;
-            sh.wgt[warp] = z > 0.f ? 1.f / (kGroup * z) : 0.f;
+    const int nstripes = (F + kSelThreads - 1) / kSelThreads;
+
+    // 1. the group's weights and chunk statistics by bulk copies
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t wbytes = static_cast<uint32_t>((F + 3) & ~3) * 4;
+        const uint32_t cbytes = static_cast<uint32_t>((2 * nch + 3) & ~3) * 4;
+        if (lane == 0) mbar_arrive_expect_tx(bar, kGroup * (wbytes + cbytes));
+        __syncwarp();
+        if (lane < kGroup) {
+            const size_t hrow_i = static_cast<size_t>(r) * hq + j * kGroup + lane;
+            bulk_load(smem_u32(s_w + lane * wld), weights + hrow_i * ld, wbytes, bar);
+            bulk_load(smem_u32(s_c + lane * ldc), chunks + hrow_i * ldc, cbytes, bar);
         }
     }
     for (int b = tid; b < kL1Bins; b += kSelThreads) sh.h1[b] = 0u;
-    if (tid == 0) { sh.found = 0; sh.above = 0ull; }
-    __syncthreads();
-
-    // 2. masses and the level-1 histogram (logits of 8 pages per thread are
-    //    loaded together before any arithmetic)
-    const float *sc = scores + (static_cast<size_t>(r) * hq + j * kGroup) * max_pages;
-    float mm[kGroup], ww[kGroup];
-#pragma unroll
-    for (int g = 0; g < kGroup; ++g) {
-        mm[g] = sh.mmax[g];
-        ww[g] = sh.wgt[g];
+    if (tid == 0) {
+        sh.found = 0;
+        sh.above = 0ull;
     }
-    for (int p0 = 0; p0 < F; p0 += 8 * kSelThreads) {
-        float v[8][kGroup];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int p = p0 + k * kSelThreads + tid;
-#pragma unroll
-            for (int g = 0; g < kGroup; ++g)
-                v[k][g] = p < F ? __ldcg(sc + static_cast<size_t>(g) * max_pages + p) : -INFINITY;
+    if (!mbar_wait(bar, 0) && tid == 0) raise_status(status, kDevTimeout);
+
+    // 2. normalisers of the group's heads: (max, sum) pairs merged online,
+    //    thread -> head tid/256, chunks tid%256 + 256k
+    {
+        const int hg = tid >> 8, ci0 = tid & 255;
+        const float *cs = s_c + hg * ldc;
+        float mx = -INFINITY, z = 0.f;
+        for (int ci = ci0; ci < nch; ci += 256) {
+            const float cm = cs[2 * ci], cz = cs[2 * ci + 1];
+            if (cm == -INFINITY) continue;
+            const float nm = fmaxf(mx, cm);
+            z = z * exp2f(mx - nm) + cz * exp2f(cm - nm);
+            mx = nm;
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int p = p0 + k * kSelThreads + tid;
-            if (p < F) {
-                float m = 0.f;
+        for (int o = 16; o > 0; o >>= 1) {
+            const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+            const float oz = __shfl_xor_sync(0xffffffffu, z, o);
+            const float nm = fmaxf(mx, om);
+            z = (mx == -INFINITY ? 0.f : z * exp2f(mx - nm)) + (om == -INFINITY ? 0.f : oz * exp2f(om - nm));
+            mx = nm;
+        }
+        if (lane == 0) {
+            sh.red[warp] = mx;
+            sh.red2[warp] = z;
+        }
+        __syncthreads();
+        if ((tid & 255) == 0) {
+            float M = -INFINITY;
 #pragma unroll
-                for (int g = 0; g < kGroup; ++g) m += exp2f(v[k][g] - mm[g]) * ww[g];
-                m = fminf(fmaxf(m, 0.f), 1.5f);        // NaN -> 0
-                const uint32_t x = __float_as_uint(m);
-                s_bits[p] = x;
-                atomicAdd(&sh.h1[l1_bin(x)], to_fx(x));
-            }
+            for (int w = 0; w < 8; ++w) M = fmaxf(M, sh.red[hg * 8 + w]);
+            float Z = 0.f;
+            if (M != -INFINITY)
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    if (sh.red[hg * 8 + w] != -INFINITY) Z += sh.red2[hg * 8 + w] * exp2f(sh.red[hg * 8 + w] - M);
+            sh.mmax[hg] = M;
+            sh.zinv[hg] = Z > 0.f ? 1.f / (kGroup * Z) : 0.f;
         }
     }
     __syncthreads();
+    // per-chunk factors 2^(M_c - M) / (G Z) for the four heads
+    for (int ci = tid; ci < nch; ci += kSelThreads) {
+        float f[kGroup];
+#pragma unroll
+        for (int g = 0; g < kGroup; ++g) {
+            const float mc = s_c[g * ldc + 2 * ci];
+            f[g] = (mc == -INFINITY || sh.mmax[g] == -INFINITY) ? 0.f : exp2f(mc - sh.mmax[g]) * sh.zinv[g];
+        }
+        s_f[ci] = make_float4(f[0], f[1], f[2], f[3]);
+    }
+    __syncthreads();
 
-    // 3. level-1 cut: thread t owns bins (hi_t .. lo_t] counted from the top
+    // 3. masses (natural page order, no exponentials) and the level-1 histogram
+#pragma unroll
+    for (int k = 0; k < kSelStripes; ++k) {
+        const int p = k * kSelThreads + tid;
+        if (p >= F) break;
+        const float4 f = s_f[p / kScoreChunk];
+        float m = s_w[p] * f.x + s_w[wld + p] * f.y + s_w[2 * wld + p] * f.z + s_w[3 * wld + p] * f.w;
+        m = fminf(fmaxf(m, 0.f), 1.5f);            // NaN -> 0
+        const uint32_t x = __float_as_uint(m);
+        s_bits[p] = x;
+        atomicAdd(&sh.h1[l1_bin(x)], to_fx(x));
+    }
+    __syncthreads();
+
+    // 4. level-1 cut: thread t owns bins (top_t - kL1PerThread, top_t] from the top
     {
         const int top = kL1Bins - 1 - tid * kL1PerThread;
         unsigned long long mine = 0ull;
@@ -308,7 +397,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         for (int i = 0; i < kL1PerThread; ++i)
             if (top - i >= 0) mine += sh.h1[top - i];
         unsigned long long total;
-        unsigned long long acc = block_excl_scan(mine, sh.scan, &total);
+        unsigned long long acc = sel_excl_scan(mine, sh.scan, &total);
         if (acc < gamma_fx && acc + mine >= gamma_fx) {
 #pragma unroll
             for (int i = 0; i < kL1PerThread; ++i) {
@@ -327,127 +416,236 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     }
     __syncthreads();
 
-    // 4. refine inside [lo, hi) with 256-bin passes until one bit pattern is
-    //    left (at most 4 passes: 30 bits of range, 8 bits per pass)
-    for (int pass = 0; sh.found && sh.hi - sh.lo > 1u; ++pass) {
-        if (pass >= 6) {                                // cannot happen: exact integer sums
-            if (tid == 0) raise_status(status, kDevBadLen);
-            break;
-        }
+    // 5. refine inside [lo, hi) until one bit pattern is left.  The pages of
+    //    the crossing bin are gathered first; when they fit in kCand (the
+    //    usual case: a level-1 bin spans 1/128 of an octave) one warp refines
+    //    them without block barriers, otherwise 256-bin passes run over all
+    //    pages.  Both use the same integer sums, so the cut is identical.
+    if (tid == 0) sh.ncand = 0;
+    __syncthreads();
+    if (sh.found) {
         const uint32_t lo = sh.lo, hi = sh.hi;
-        const uint32_t width = hi - lo;
-        const int bits = 32 - __clz(width - 1u);
-        const int shift = bits > 8 ? bits - 8 : 0;
-        const int nb = static_cast<int>((width - 1u) >> shift) + 1;
-        if (tid < kL2Bins) sh.h2[tid] = 0u;
-        __syncthreads();
-        for (int p = tid; p < F; p += kSelThreads) {
-            const uint32_t x = s_bits[p];
-            if (x >= lo && x < hi) atomicAdd(&sh.h2[(x - lo) >> shift], to_fx(x));
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // lane owns bins [top-7, top] with top = nb-1-8*lane, walked downwards
-            const int top = nb - 1 - 8 * lane;
-            unsigned long long mine = 0ull;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (top - i >= 0) mine += sh.h2[top - i];
-            unsigned long long x = mine;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            unsigned long long acc = sh.above + x - mine;
-            const unsigned long long need = gamma_fx;
-            if (acc < need && acc + mine >= need) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int b = top - i;
-                    if (b < 0) break;
-                    if (acc + sh.h2[b] >= need) {
-                        const uint32_t nlo = lo + (static_cast<uint32_t>(b) << shift);
-                        const uint32_t span = 1u << shift;
-                        sh.lo = nlo;
-                        sh.hi = (hi - nlo < span) ? hi : nlo + span;
-                        sh.above = acc;
-                        break;
-                    }
-                    acc += sh.h2[b];
+        for (int k = 0; k < kSelStripes; ++k) {
+            const int p0 = k * kSelThreads + warp * 32;
+            if (p0 >= F) break;                              // warp-uniform
+            const int p = p0 + lane;
+            const uint32_t x = p < F ? s_bits[p] : 0u;
+            const bool in = p < F && x >= lo && x < hi;
+            const unsigned m = __ballot_sync(0xffffffffu, in);
+            if (m) {
+                int base = 0;
+                if (lane == 0) base = atomicAdd(&sh.ncand, __popc(m));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const int slot = base + __popc(m & ((1u << lane) - 1u));
+                if (in && slot < kCand) {
+                    sh.cand[slot] = x;
+                    sh.cand_idx[slot] = static_cast<uint16_t>(p);
                 }
             }
         }
+    }
+    __syncthreads();
+    const bool use_pair = sh.found && sh.ncand <= kPairMax;
+    const bool use_cand = sh.found && !use_pair && sh.ncand <= kCand;
+    if (use_pair) {
+        // candidate t: masses ranked before it (larger, or equal with a lower
+        // page index); the candidate whose running sum crosses gamma is the cut
+        const int nc = sh.ncand;
+        const unsigned long long above0 = sh.above;
+        __syncthreads();                                 // every thread has read `above`
+        if (tid < nc) {
+            const uint32_t x = sh.cand[tid];
+            const uint32_t xi = sh.cand_idx[tid];
+            unsigned long long gt_sum = 0ull, tie_before = 0ull;
+            for (int c = 0; c < nc; ++c) {
+                const uint32_t y = sh.cand[c];
+                const uint32_t fy = to_fx(y);
+                if (y > x) gt_sum += fy;
+                else if (y == x && sh.cand_idx[c] < xi) tie_before += fy;
+            }
+            const unsigned long long before = above0 + gt_sum + tie_before;
+            if (before < gamma_fx && before + to_fx(x) >= gamma_fx) {   // exactly one candidate
+                sh.lo = x;
+                sh.hi = x + 1u;
+                sh.above = above0 + gt_sum;
+            }
+        }
         __syncthreads();
+    } else if (use_cand) {
+        if (warp == 0) {
+            const int nc = sh.ncand;
+            uint32_t lo = sh.lo, hi = sh.hi;
+            unsigned long long above = sh.above;
+            for (int pass = 0; hi - lo > 1u && pass < 6; ++pass) {
+                const uint32_t width = hi - lo;
+                const int nbits = 32 - __clz(width - 1u);
+                const int shift = nbits > 8 ? nbits - 8 : 0;
+                const int nb = static_cast<int>((width - 1u) >> shift) + 1;
+#pragma unroll
+                for (int i = 0; i < kL2Bins / 32; ++i) sh.h2[lane + 32 * i] = 0u;
+                __syncwarp();
+                for (int c = lane; c < nc; c += 32) {
+                    const uint32_t x = sh.cand[c];
+                    if (x >= lo && x < hi) atomicAdd(&sh.h2[(x - lo) >> shift], to_fx(x));
+                }
+                __syncwarp();
+                const int top = nb - 1 - 8 * lane;
+                unsigned long long mine = 0ull;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (top - i >= 0) mine += sh.h2[top - i];
+                unsigned long long xs = mine;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(0xffffffffu, xs, o);
+                    if (lane >= o) xs += y;
+                }
+                unsigned long long acc = above + xs - mine;
+                int fb = -1;
+                unsigned long long fa = 0ull;
+                if (acc < gamma_fx && acc + mine >= gamma_fx) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int b = top - i;
+                        if (b < 0) break;
+                        if (acc + sh.h2[b] >= gamma_fx) {
+                            fb = b;
+                            fa = acc;
+                            break;
+                        }
+                        acc += sh.h2[b];
+                    }
+                }
+                const unsigned who = __ballot_sync(0xffffffffu, fb >= 0);
+                if (!who) break;                             // cannot happen: exact integer sums
+                const int src = __ffs(who) - 1;
+                fb = __shfl_sync(0xffffffffu, fb, src);
+                above = __shfl_sync(0xffffffffu, fa, src);
+                const uint32_t nlo = lo + (static_cast<uint32_t>(fb) << shift);
+                const uint32_t span = 1u << shift;
+                hi = (hi - nlo < span) ? hi : nlo + span;
+                lo = nlo;
+                __syncwarp();
+            }
+            if (lane == 0) {
+                sh.lo = lo;
+                sh.hi = hi;
+                sh.above = above;
+                if (hi - lo > 1u) raise_status(status, kDevBadLen);
+            }
+        }
+        __syncthreads();
+    } else {
+        for (int pass = 0; sh.found && sh.hi - sh.lo > 1u; ++pass) {
+            if (pass >= 6) {                               // cannot happen: exact integer sums
+                if (tid == 0) raise_status(status, kDevBadLen);
+                break;
+            }
+            const uint32_t lo = sh.lo, hi = sh.hi;
+            const uint32_t width = hi - lo;
+            const int nbits = 32 - __clz(width - 1u);
+            const int shift = nbits > 8 ? nbits - 8 : 0;
+            const int nb = static_cast<int>((width - 1u) >> shift) + 1;
+            if (tid < kL2Bins) sh.h2[tid] = 0u;
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < kSelStripes; ++k) {
+                const int p = k * kSelThreads + tid;
+                if (p >= F) break;
+                const uint32_t x = s_bits[p];
+                if (x >= lo && x < hi) atomicAdd(&sh.h2[(x - lo) >> shift], to_fx(x));
+            }
+            __syncthreads();
+            if (warp == 0) {
+                const int top = nb - 1 - 8 * lane;
+                unsigned long long mine = 0ull;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (top - i >= 0) mine += sh.h2[top - i];
+                unsigned long long x = mine;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                unsigned long long acc = sh.above + x - mine;
+                if (acc < gamma_fx && acc + mine >= gamma_fx) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int b = top - i;
+                        if (b < 0) break;
+                        if (acc + sh.h2[b] >= gamma_fx) {
+                            const uint32_t nlo = lo + (static_cast<uint32_t>(b) << shift);
+                            const uint32_t span = 1u << shift;
+                            sh.lo = nlo;
+                            sh.hi = (hi - nlo < span) ? hi : nlo + span;
+                            sh.above = acc;
+                            break;
+                        }
+                        acc += sh.h2[b];
+                    }
+                }
+            }
+            __syncthreads();
+        }
     }
 
-    // 5. cut value and how many pages tied at it are needed
+    // 6. cut value and how many pages tied at it are needed
     uint32_t cut;
     unsigned long long need_tied;
     if (sh.found) {
         cut = sh.lo;
         const unsigned long long cfx = to_fx(cut);
-        const unsigned long long rest = gamma_fx - sh.above;     // > 0
-        need_tied = (rest + cfx - 1ull) / cfx;                    // cfx > 0: it carried the crossing
+        need_tied = (gamma_fx - sh.above + cfx - 1ull) / cfx;   // cfx > 0: it carried the crossing
     } else {                                                      // total < gamma: keep all
         cut = 0u;
         need_tied = 0xFFFFFFFFull;
     }
 
-    // 6. ordered compaction: thread t owns a contiguous run of pages; the
-    //    physical ids of the first 8 are fetched before the scan
-    const int ept = (F + kSelThreads - 1) / kSelThreads;
-    const int pb = min(F, tid * ept), pe = min(F, pb + ept);
-    int32_t pref[8];
+    // 7. ordered compaction by stripes of 1024 pages: per (stripe, warp) counts
+    //    of pages above and at the cut, one block scan, then warp ballots
+    const unsigned lt_mask = (1u << lane) - 1u;
+    unsigned gt_m[kSelStripes], eq_m[kSelStripes];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) pref[k] = (pb + k < pe) ? __ldg(row + pb + k) : 0;
-    uint32_t gt = 0, eq = 0;
-    for (int p = pb; p < pe; ++p) {
-        const uint32_t x = s_bits[p];
-        gt += x > cut;
-        eq += x == cut;
+    for (int k = 0; k < kSelStripes; ++k) {
+        gt_m[k] = eq_m[k] = 0u;
+        if (k < nstripes) {
+            const int p = k * kSelThreads + tid;
+            const uint32_t x = p < F ? s_bits[p] : 0u;
+            gt_m[k] = __ballot_sync(0xffffffffu, p < F && x > cut);
+            eq_m[k] = __ballot_sync(0xffffffffu, p < F && x == cut);
+            if (lane == 0)
+                sh.cnt[k * kSelWarps + warp] =
+                    __popc(gt_m[k]) | (static_cast<unsigned long long>(__popc(eq_m[k])) << 32);
+        }
     }
-    unsigned long long total;
-    const unsigned long long pre = block_excl_scan(gt | (static_cast<unsigned long long>(eq) << 32),
-                                                   sh.scan, &total);
-    const uint32_t gt_pre = static_cast<uint32_t>(pre), eq_pre = static_cast<uint32_t>(pre >> 32);
-    unsigned long long eq_run = eq_pre;
-    int pos = static_cast<int>(gt_pre + (eq_pre < need_tied ? eq_pre : need_tied));
+    __syncthreads();
+    unsigned long long mine = 0ull, total;
+    if (tid < nstripes * kSelWarps) mine = sh.cnt[tid];
+    const unsigned long long pre = sel_excl_scan(mine, sh.scan, &total);
+    if (tid < nstripes * kSelWarps) sh.cnt[tid] = pre;
+    __syncthreads();
     bool badp = false;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int p = pb + k;
-        if (p < pe) {
-            const uint32_t x = s_bits[p];
-            bool keep = x > cut;
-            if (x == cut) {
-                keep = eq_run < need_tied;
-                ++eq_run;
-            }
-            if (keep) {
+    for (int k = 0; k < kSelStripes; ++k) {
+        if (k < nstripes && (gt_m[k] | eq_m[k]) != 0u) {     // warp-uniform
+            const unsigned long long base = sh.cnt[k * kSelWarps + warp];
+            const unsigned long long gt_before = (base & 0xFFFFFFFFull) + __popc(gt_m[k] & lt_mask);
+            const unsigned long long eq_before = (base >> 32) + __popc(eq_m[k] & lt_mask);
+            const bool is_gt = (gt_m[k] >> lane) & 1u, is_eq = (eq_m[k] >> lane) & 1u;
+            if (is_gt || (is_eq && eq_before < need_tied)) {
+                const int pos = static_cast<int>(gt_before + (eq_before < need_tied ? eq_before : need_tied));
                 badp |= (pref[k] < 0 || pref[k] >= num_pages);
-                out[pos++] = pref[k];
+                out[pos] = pref[k];
             }
-        }
-    }
-    for (int p = pb + 8; p < pe; ++p) {
-        const uint32_t x = s_bits[p];
-        bool keep = x > cut;
-        if (x == cut) {
-            keep = eq_run < need_tied;
-            ++eq_run;
-        }
-        if (keep) {
-            const int32_t phys = row[p];
-            badp |= (phys < 0 || phys >= num_pages);
-            out[pos++] = phys;
         }
     }
     if (badp) raise_status(status, kDevBadPage);
     if (tid == 0) {
         const unsigned long long gt_all = total & 0xFFFFFFFFull, eq_all = total >> 32;
         const int kept = static_cast<int>(gt_all + (eq_all < need_tied ? eq_all : need_tied));
-        if (T) out[kept] = row[F];
+        if (T) out[kept] = tail_pre;
         lengths[u] = kept + T;
     }
 }
@@ -455,32 +653,36 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
 // ---------------------------------------------------------------------------
 cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_table,
                          const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
-                         long long num_pages, float scale_log2, float *scores, float *chunks,
+                         long long num_pages, float scale_log2, float *weights, float *chunks,
                          uint32_t *status, cudaStream_t stream)
 {
     const int n_chunks = (max_pages + kScoreChunk - 1) / kScoreChunk;
     dim3 grid(n_chunks, batch);
-    return launch_pdl(k_score, grid, dim3(kScoreThreads), 0, stream,
+    const size_t smem = static_cast<size_t>(kScoreChunk) * (hkv * kHeadDim * 2 + 16);
+    cudaError_t e = cudaFuncSetAttribute(k_score, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_score, grid, dim3(kScoreThreads), smem, stream,
                       static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(summ),
-                      page_table, seq_lens, hq, hkv, max_pages, num_pages, scale_log2, scores,
-                      chunks, n_chunks, status);
+                      page_table, seq_lens, hq, hkv, max_pages, weights_ld(max_pages), num_pages,
+                      scale_log2, weights, chunks, chunks_ld(max_pages), status);
 }
 
-cudaError_t launch_select(const float *scores, const float *chunks, const int32_t *page_table,
+cudaError_t launch_select(const float *weights, const float *chunks, const int32_t *page_table,
                           const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
                           long long num_pages, unsigned long long gamma_fx, bool dense,
                           int32_t *lists, int32_t *lengths, uint32_t *status, cudaStream_t stream)
 {
-    const int n_chunks = (max_pages + kScoreChunk - 1) / kScoreChunk;
-    const size_t smem = dense ? 0 : sizeof(uint32_t) * static_cast<size_t>(max_pages);
+    const int ldc = chunks_ld(max_pages);
+    const size_t smem = dense ? 0 : select_smem_bytes(max_pages, ldc);
     if (!dense) {
         cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(k_select, dim3(batch * hkv), dim3(kSelThreads), smem, stream, scores, chunks,
-                      page_table, seq_lens, hq, hkv, max_pages, n_chunks, num_pages, gamma_fx,
-                      dense ? 1 : 0, lists, lengths, status);
+    return launch_pdl(k_select, dim3(batch * hkv), dim3(kSelThreads), smem, stream, weights, chunks,
+                      page_table, seq_lens, hq, hkv, max_pages, weights_ld(max_pages), ldc,
+                      num_pages, gamma_fx, dense ? 1 : 0, lists, lengths, status);
 }
 
 }  // namespace moira

@@ -272,3 +272,31 @@ def test_full_size_sampled_units(name, gamma):
     assert compared >= len(picks) - 2
     del st, w
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("F", [50, 500, 3000])
+def test_select_all_masses_tied(F):
+    """Identical keys give identical masses: the rule keeps the ceil(gamma*F)
+    lowest logical pages (plus the tail).  F = 50, 500 and 3000 take the
+    pairwise, single-warp and block-wide refinement paths respectively."""
+    L = 16 * F + 5
+    sp = W.spec("llama8b_128k", batch=1, layers=1, context=(L,))
+    w = W.make_workload(sp, seed=9, device="cuda")
+    key = torch.randn(128, generator=torch.Generator(device="cuda").manual_seed(1), device="cuda")
+    w.k_pool[:] = key.to(torch.bfloat16)
+    st = DecodeState(w)
+    st.summarize()
+    for gamma in (0.3, 0.7, 0.9, 0.99):
+        g = float(np.float32(gamma))
+        k = int(np.ceil(g * F))
+        lists, lengths = st.select_layer(0, g)
+        torch.cuda.synchronize()
+        assert st.device_status() == 0
+        lh, nh = lists.cpu().numpy(), lengths.cpu().numpy()
+        for j in range(w.spec.kv_heads):
+            ud = H.UnitData(w, 0, 0, j, with_v=False)
+            why = H.check_list(ud, lh[0, j, :nh[0, j]], g)
+            assert why is None, f"F={F} gamma={g} head {j}: {why}"
+            logical = ud.to_logical(lh[0, j, :nh[0, j]])
+            if abs(g * F - round(g * F)) > 1e-3:           # away from an integer: exact
+                assert list(logical) == list(range(k)) + [F], f"F={F} gamma={g}: {len(logical)} vs {k}+1"
