@@ -13,7 +13,7 @@
 //   log-sum-exp in two levels: the last block to finish in each group of 16
 //   consecutive blocks of a list merges the group, and the last group to
 //   finish writes the output (arrival counters, self-resetting); a list held
-//   by one block is written directly.
+//   by one block, or by one group, is written by that block or group merge.
 //
 // Data path per block (1 producer warp + 4 consumer warps, 2 blocks per SM):
 //   the producer looks up a batch of 32 list entries while it issues the
@@ -113,6 +113,92 @@ __device__ __forceinline__ void merge_partials(const float *partials, int first,
 __device__ __forceinline__ int block_of(long long g, long long W, long long n)
 {
     return static_cast<int>(((g + 1) * n - 1) / W);
+}
+
+// Named barrier of the 4 consumer warps (the producer warp never joins it).
+__device__ __forceinline__ void consumer_bar()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ float *out_row(const AttendArgs &a, int u, int h, int d0)
+{
+    const int r = u / a.hkv, j = u % a.hkv;
+    return a.out + (static_cast<size_t>(r) * a.hq + j * kGroup + h) * kHeadDim + d0;
+}
+
+// How list u is spread over the blocks: blocks bfirst..blast hold its pages;
+// block b's merge group starts at gfirst and has gn members; the list has
+// ngroups groups.
+struct ListSplit {
+    int bfirst, blast, gfirst, gn, ngroups;
+};
+
+__device__ __forceinline__ ListSplit list_split(const int *s_off, int u, int b, long long W, long long n)
+{
+    ListSplit ls;
+    ls.bfirst = block_of(s_off[u], W, n);
+    ls.blast = block_of(static_cast<long long>(s_off[u + 1]) - 1, W, n);
+    ls.gfirst = ls.bfirst + (b - ls.bfirst) / kMergeSpan * kMergeSpan;
+    ls.gn = min(kMergeSpan, ls.blast - ls.gfirst + 1);
+    ls.ngroups = (ls.blast - ls.bfirst) / kMergeSpan + 1;
+    return ls;
+}
+
+// Merges after this block's partial of a shared list u is published; prev is
+// the value thread 0's arrival atomic on the group counter returned (unused
+// for a group of one).  The last block to arrive in a group merges the group
+// (into the output when the list has one group); the last group to arrive
+// merges the groups into the output.  Called by all consumer threads.
+__device__ __forceinline__ void resolve_list(const AttendArgs &a, int &flag, int u, const ListSplit ls,
+                                          uint32_t prev, int h, int d0)
+{
+    const int tid = threadIdx.x;
+    int mine = 1;
+    if (ls.gn > 1) {
+        if (tid == 0) flag = (prev == static_cast<uint32_t>(ls.gn - 1)) ? 1 : 0;
+        consumer_bar();
+        mine = *const_cast<volatile int *>(&flag);
+        consumer_bar();                                  // every thread has read flag
+        if (mine) {
+            float gm, gl;
+            float4 go;
+            merge_partials(a.partials, ls.gfirst + u, 1, ls.gn, h, d0, gm, gl, go);
+            if (ls.ngroups == 1) {                       // the only group: write the output
+                const float inv = gl > 0.f ? 1.f / gl : 0.f;
+                *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
+                    make_float4(go.x * inv, go.y * inv, go.z * inv, go.w * inv);
+            } else {
+                consumer_bar();                          // the group's first slot is read
+                float *gp = a.partials + static_cast<size_t>(ls.gfirst + u) * kPartFloats;
+                *reinterpret_cast<float4 *>(gp + 2 * kGroup + h * kHeadDim + d0) = go;
+                if ((tid & 31) == 0) {
+                    gp[h] = gm;
+                    gp[kGroup + h] = gl;
+                }
+            }
+            if (tid == 0) a.gcounters[ls.gfirst + u] = 0u;      // ready for the next launch
+        }
+    }
+    if (mine && ls.ngroups > 1) {
+        consumer_bar();                                  // group partial written
+        if (tid == 0) {
+            const uint32_t p2 = atomic_add_acq_rel_gpu(&a.counters[u], 1u);
+            flag = (p2 == static_cast<uint32_t>(ls.ngroups - 1)) ? 1 : 0;
+        }
+        consumer_bar();
+        const int last = *const_cast<volatile int *>(&flag);
+        if (last) {
+            float fm, fl;
+            float4 fo;
+            merge_partials(a.partials, ls.bfirst + u, kMergeSpan, ls.ngroups, h, d0, fm, fl, fo);
+            const float inv = fl > 0.f ? 1.f / fl : 0.f;
+            *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
+                make_float4(fo.x * inv, fo.y * inv, fo.z * inv, fo.w * inv);
+            if (tid == 0) a.counters[u] = 0u;            // ready for the next launch
+        }
+    }
+    consumer_bar();                                      // flag is free again
 }
 
 template <int kSlots>
@@ -268,6 +354,21 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
     const int hn0 = (2 * (lane & 3)) & 3;
     const bool lo_lane = lane >= 16;      // holds the bf16 residual column of P
     const float c = a.scale_log2;
+    // this thread's (head, 4 dims) in the block result and the merges
+    const int h = tid >> 5, d0 = (tid & 31) * 4;
+
+    // q fragments of list v (A operand rows 0-7 = heads 0-3 twice, rows 8-15 zero)
+    uint32_t aq[8][2];
+    auto load_q = [&](int v) {
+        const int r = v / a.hkv, j = v % a.hkv;
+        const uint16_t *qrow = static_cast<const uint16_t *>(a.q) +
+                               (static_cast<size_t>(r) * a.hq + j * kGroup + hq_row) * kHeadDim + tq;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            aq[ks][0] = __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16));
+            aq[ks][1] = __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8));
+        }
+    };
 
     int u;
     {
@@ -276,233 +377,196 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
             const int mid = (lo + hi) >> 1;
             if (s_off[mid] <= g0) lo = mid; else hi = mid;
         }
-        u = lo;
+        u = lo;                            // s_off[u] <= g0 < s_off[u + 1]: list u is not empty
     }
+    load_q(u);
+
+    // The first segment's list may continue in earlier blocks and, when more
+    // segments follow, its arrival is taken at once but resolved after the
+    // block's last segment, so the ring keeps streaming meanwhile.
+    int pend_u = -1;
+    uint32_t pend_prev = 0u;
 
     while (true) {
         const long long seg_lo = max(g0, static_cast<long long>(s_off[u]));
         const long long seg_hi = min(g1, static_cast<long long>(s_off[u + 1]));
-        if (seg_lo < seg_hi) {
-            const int r = u / a.hkv, j = u % a.hkv;
-            // q fragments (A operand rows 0-7 = heads 0-3 twice, rows 8-15 zero)
-            uint32_t aq[8][2];
-            {
-                const uint16_t *qrow = static_cast<const uint16_t *>(a.q) +
-                                       (static_cast<size_t>(r) * a.hq + j * kGroup + hq_row) * kHeadDim + tq;
+        float m_run = -INFINITY, l_run = 0.f;
+        float D[8][4];
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    aq[ks][0] = __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16));
-                    aq[ks][1] = __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8));
-                }
-            }
-            float m_run = -INFINITY, l_run = 0.f;
-            float D[8][4];
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) D[mt][0] = D[mt][1] = D[mt][2] = D[mt][3] = 0.f;
+        for (int mt = 0; mt < 8; ++mt) D[mt][0] = D[mt][1] = D[mt][2] = D[mt][3] = 0.f;
 
-            const long long first = seg_lo + ((warp - (seg_lo - g0) % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
-            for (long long g = first; g < seg_hi; g += kConsumerWarps) {
-                const long long idx = g - g0;
-                const int slot = static_cast<int>(idx % kSlots);
-                const uint32_t round = static_cast<uint32_t>(idx / kSlots);
-                if (!mbar_wait(smem_u32(&sm.full[slot]), round & 1u) && lane == 0)
-                    raise_status(a.status, kDevTimeout);
-                const int ntok = sm.meta[slot].y;
-                if (ntok > 0) {
-                    const uint32_t kb = smem_u32(stage + slot * kSlotBytes);
-                    const uint32_t vb = kb + 2 * kHalfBox;
-                    // ---- S^T = q K^T for the 4 heads x 16 tokens ----
-                    float acc[4][4];
+        const long long first = seg_lo + ((warp - (seg_lo - g0) % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
+        for (long long g = first; g < seg_hi; g += kConsumerWarps) {
+            const long long idx = g - g0;
+            const int slot = static_cast<int>(idx % kSlots);
+            const uint32_t round = static_cast<uint32_t>(idx / kSlots);
+            if (!mbar_wait(smem_u32(&sm.full[slot]), round & 1u) && lane == 0)
+                raise_status(a.status, kDevTimeout);
+            const int ntok = sm.meta[slot].y;
+            if (ntok > 0) {
+                const uint32_t kb = smem_u32(stage + slot * kSlotBytes);
+                const uint32_t vb = kb + 2 * kHalfBox;
+                // ---- S^T = q K^T for the 4 heads x 16 tokens ----
+                float acc[4][4];
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
-                    {
-                        const int t = (lane & 7) + ((lane >> 4) << 3);
-                        const int sw = t & 7;
+                for (int x = 0; x < 4; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
+                {
+                    const int t = (lane & 7) + ((lane >> 4) << 3);
+                    const int sw = t & 7;
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const int ch = 2 * ks + ((lane >> 3) & 1);
-                            const uint32_t addr = kb + (ch >> 3) * kHalfBox + t * 128 + (((ch & 7) ^ sw) << 4);
-                            uint32_t b0, b1, b2, b3;
-                            ldsm_x4(addr, b0, b1, b2, b3);
-                            const int par = (ks & 1) * 2;
-                            mma_bf16_16816(acc[par], aq[ks][0], 0u, aq[ks][1], 0u, b0, b1);
-                            mma_bf16_16816(acc[par + 1], aq[ks][0], 0u, aq[ks][1], 0u, b2, b3);
-                        }
-                    }
-                    float s[4] = {(acc[0][0] + acc[2][0]) * c, (acc[0][1] + acc[2][1]) * c,
-                                  (acc[1][0] + acc[3][0]) * c, (acc[1][1] + acc[3][1]) * c};
-                    const bool tail = ntok < kPageSize;
-                    if (tail) {
-                        if (tq >= ntok) s[0] = -INFINITY;
-                        if (tq + 1 >= ntok) s[1] = -INFINITY;
-                        if (tq + 8 >= ntok) s[2] = -INFINITY;
-                        if (tq + 9 >= ntok) s[3] = -INFINITY;
-                    }
-                    float pm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
-                    pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
-                    const float m_new = fmaxf(m_run, pm);
-                    const float m_use = m_new == -INFINITY ? 0.f : m_new;
-                    const float alpha = exp2f(m_run - m_use);
-                    float p[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) p[x] = exp2f(s[x] - m_use);
-                    l_run = l_run * alpha + (p[0] + p[1]) + (p[2] + p[3]);
-                    m_run = m_new;
-                    // B operand: columns 0-3 bf16(P), columns 4-7 residual
-                    uint32_t bp0, bp1;
-                    {
-                        uint32_t h[4];
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const uint32_t hb = f32_to_bf16_rne(p[x]);
-                            h[x] = lo_lane ? f32_to_bf16_rne(p[x] - __uint_as_float(hb << 16)) : hb;
-                        }
-                        bp0 = h[0] | (h[1] << 16);
-                        bp1 = h[2] | (h[3] << 16);
-                    }
-                    // rescale the running O^T columns (heads hn0, hn0+1)
-                    const float al0 = __shfl_sync(0xffffffffu, alpha, 4 * hn0);
-                    const float al1 = __shfl_sync(0xffffffffu, alpha, 4 * (hn0 + 1));
-                    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            D[mt][0] *= al0;
-                            D[mt][1] *= al1;
-                            D[mt][2] *= al0;
-                            D[mt][3] *= al1;
-                        }
-                    }
-                    // ---- O^T += V^T P^T ----
-                    uint32_t msk01 = 0xFFFFFFFFu, msk23 = 0xFFFFFFFFu;
-                    if (tail) {
-                        msk01 = (tq < ntok ? 0x0000FFFFu : 0u) | (tq + 1 < ntok ? 0xFFFF0000u : 0u);
-                        msk23 = (tq + 8 < ntok ? 0x0000FFFFu : 0u) | (tq + 9 < ntok ? 0xFFFF0000u : 0u);
-                    }
-                    {
-                        const int mi = lane >> 3;
-                        const int t = (lane & 7) + ((mi >> 1) << 3);
-                        const int sw = t & 7;
-#pragma unroll
-                        for (int mt = 0; mt < 8; ++mt) {
-                            const int ch = 2 * mt + (mi & 1);
-                            const uint32_t addr = vb + (ch >> 3) * kHalfBox + t * 128 + (((ch & 7) ^ sw) << 4);
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4_trans(addr, a0, a1, a2, a3);
-                            mma_bf16_16816(D[mt], a0 & msk01, a1 & msk01, a2 & msk23, a3 & msk23, bp0, bp1);
-                        }
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int ch = 2 * ks + ((lane >> 3) & 1);
+                        const uint32_t addr = kb + (ch >> 3) * kHalfBox + t * 128 + (((ch & 7) ^ sw) << 4);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(addr, b0, b1, b2, b3);
+                        const int par = (ks & 1) * 2;
+                        mma_bf16_16816(acc[par], aq[ks][0], 0u, aq[ks][1], 0u, b0, b1);
+                        mma_bf16_16816(acc[par + 1], aq[ks][0], 0u, aq[ks][1], 0u, b2, b3);
                     }
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
-            }
-
-            // ---- warp result -> shared memory ----
-            float lsum = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
-            lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+                float s[4] = {(acc[0][0] + acc[2][0]) * c, (acc[0][1] + acc[2][1]) * c,
+                              (acc[1][0] + acc[3][0]) * c, (acc[1][1] + acc[3][1]) * c};
+                const bool tail = ntok < kPageSize;
+                if (tail) {
+                    if (tq >= ntok) s[0] = -INFINITY;
+                    if (tq + 1 >= ntok) s[1] = -INFINITY;
+                    if (tq + 8 >= ntok) s[2] = -INFINITY;
+                    if (tq + 9 >= ntok) s[3] = -INFINITY;
+                }
+                float pm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 1));
+                pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 2));
+                const float m_new = fmaxf(m_run, pm);
+                const float m_use = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = exp2f(m_run - m_use);
+                float p[4];
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
+                for (int x = 0; x < 4; ++x) p[x] = exp2f(s[x] - m_use);
+                l_run = l_run * alpha + (p[0] + p[1]) + (p[2] + p[3]);
+                m_run = m_new;
+                // B operand: columns 0-3 bf16(P), columns 4-7 residual
+                uint32_t bp0, bp1;
+                {
+                    uint32_t hb4[4];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const float v = D[mt][x] + __shfl_xor_sync(0xffffffffu, D[mt][x], 2);
-                    if ((lane & 3) < 2) {
-                        const int h = 2 * (lane & 3) + (x & 1);
-                        const int d = 16 * mt + (lane >> 2) + (x >= 2 ? 8 : 0);
-                        sm.co[warp][h][d] = v;
+                    for (int x = 0; x < 4; ++x) {
+                        const uint32_t hb = f32_to_bf16_rne(p[x]);
+                        hb4[x] = lo_lane ? f32_to_bf16_rne(p[x] - __uint_as_float(hb << 16)) : hb;
+                    }
+                    bp0 = hb4[0] | (hb4[1] << 16);
+                    bp1 = hb4[2] | (hb4[3] << 16);
+                }
+                // rescale the running O^T columns (heads hn0, hn0+1)
+                const float al0 = __shfl_sync(0xffffffffu, alpha, 4 * hn0);
+                const float al1 = __shfl_sync(0xffffffffu, alpha, 4 * (hn0 + 1));
+                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        D[mt][0] *= al0;
+                        D[mt][1] *= al1;
+                        D[mt][2] *= al0;
+                        D[mt][3] *= al1;
+                    }
+                }
+                // ---- O^T += V^T P^T ----
+                uint32_t msk01 = 0xFFFFFFFFu, msk23 = 0xFFFFFFFFu;
+                if (tail) {
+                    msk01 = (tq < ntok ? 0x0000FFFFu : 0u) | (tq + 1 < ntok ? 0xFFFF0000u : 0u);
+                    msk23 = (tq + 8 < ntok ? 0x0000FFFFu : 0u) | (tq + 9 < ntok ? 0xFFFF0000u : 0u);
+                }
+                {
+                    const int mi = lane >> 3;
+                    const int t = (lane & 7) + ((mi >> 1) << 3);
+                    const int sw = t & 7;
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const int ch = 2 * mt + (mi & 1);
+                        const uint32_t addr = vb + (ch >> 3) * kHalfBox + t * 128 + (((ch & 7) ^ sw) << 4);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4_trans(addr, a0, a1, a2, a3);
+                        mma_bf16_16816(D[mt], a0 & msk01, a1 & msk01, a2 & msk23, a3 & msk23, bp0, bp1);
                     }
                 }
             }
-            if (lane < 16 && (lane & 3) == 0) {
-                sm.cm[warp][lane >> 2] = m_run;
-                sm.cl[warp][lane >> 2] = lsum;
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-
-            // ---- block result: thread -> (head, 4 dims) ----
-            const int h = tid >> 5, d0 = (tid & 31) * 4;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.cm[w][h]);
-            const float Ms = M == -INFINITY ? 0.f : M;
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            float Lsum = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float e = exp2f(sm.cm[w][h] - Ms);
-                const float4 v = *reinterpret_cast<const float4 *>(&sm.co[w][h][d0]);
-                o.x += e * v.x; o.y += e * v.y; o.z += e * v.z; o.w += e * v.w;
-                Lsum += e * sm.cl[w][h];
-            }
-            const long long ua = s_off[u], ue = s_off[u + 1];
-            const int bfirst = block_of(ua, W, n), blast = block_of(ue - 1, W, n);
-            float *orow = a.out + (static_cast<size_t>(r) * a.hq + j * kGroup + h) * kHeadDim + d0;
-            if (bfirst == blast) {
-                const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-                *reinterpret_cast<float4 *>(orow) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
-            } else {
-                // Two-level merge.  Blocks bfirst..blast of this list form groups
-                // of kMergeSpan; the last block to finish in a group merges the
-                // group's partials into the group's first slot, and the last
-                // group to finish merges the group partials into the output.
-                // Both merges read at most kMergeSpan partials in one batch.
-                float *part = a.partials + static_cast<size_t>(b + u) * kPartFloats;
-                *reinterpret_cast<float4 *>(part + 2 * kGroup + h * kHeadDim + d0) = o;
-                if ((tid & 31) == 0) {
-                    part[h] = M;
-                    part[kGroup + h] = Lsum;
-                }
-                // the CTA barrier makes every thread's partial visible to thread 0,
-                // whose acq_rel atomic publishes it and acquires the others
-                asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                const int gfirst = bfirst + (b - bfirst) / kMergeSpan * kMergeSpan;
-                const int gn = min(kMergeSpan, blast - gfirst + 1);
-                if (gn > 1) {
-                    if (tid == 0) {
-                        const uint32_t prev = atomic_add_acq_rel_gpu(&a.gcounters[gfirst + u], 1u);
-                        sm.flag = (prev == static_cast<uint32_t>(gn - 1)) ? 1 : 0;
-                    }
-                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                    if (sm.flag) {
-                        float gm, gl;
-                        float4 go;
-                        merge_partials(a.partials, gfirst + u, 1, gn, h, d0, gm, gl, go);
-                        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                        float *gp = a.partials + static_cast<size_t>(gfirst + u) * kPartFloats;
-                        *reinterpret_cast<float4 *>(gp + 2 * kGroup + h * kHeadDim + d0) = go;
-                        if ((tid & 31) == 0) {
-                            gp[h] = gm;
-                            gp[kGroup + h] = gl;
-                        }
-                        if (tid == 0) a.gcounters[gfirst + u] = 0u;     // ready for the next launch
-                    }
-                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                } else {
-                    if (tid == 0) sm.flag = 1;                     // a group of one is its own merge
-                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                }
-                if (sm.flag) {
-                    const int ngroups = (blast - bfirst) / kMergeSpan + 1;
-                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                    if (tid == 0) {
-                        const uint32_t prev = atomic_add_acq_rel_gpu(&a.counters[u], 1u);
-                        sm.flag = (prev == static_cast<uint32_t>(ngroups - 1)) ? 1 : 0;
-                    }
-                    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-                    if (sm.flag) {
-                        float fm, fl;
-                        float4 fo;
-                        merge_partials(a.partials, bfirst + u, kMergeSpan, ngroups, h, d0, fm, fl, fo);
-                        const float inv = fl > 0.f ? 1.f / fl : 0.f;
-                        *reinterpret_cast<float4 *>(orow) = make_float4(fo.x * inv, fo.y * inv, fo.z * inv, fo.w * inv);
-                        if (tid == 0) a.counters[u] = 0u;          // ready for the next launch
-                    }
-                }
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sm.empty[slot]));
         }
-        if (static_cast<long long>(s_off[u + 1]) >= g1) break;
-        ++u;
+
+        // the next non-empty list of this block: its q loads overlap the
+        // combine below (the current q is no longer needed)
+        const bool more = seg_hi < g1;
+        int un = u + 1;
+        if (more) {
+            while (s_off[un + 1] == s_off[un]) ++un;
+            load_q(un);
+        }
+
+        // ---- warp result -> shared memory ----
+        float lsum = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+        lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const float v = D[mt][x] + __shfl_xor_sync(0xffffffffu, D[mt][x], 2);
+                if ((lane & 3) < 2) {
+                    const int hh = 2 * (lane & 3) + (x & 1);
+                    const int d = 16 * mt + (lane >> 2) + (x >= 2 ? 8 : 0);
+                    sm.co[warp][hh][d] = v;
+                }
+            }
+        }
+        if (lane < 16 && (lane & 3) == 0) {
+            sm.cm[warp][lane >> 2] = m_run;
+            sm.cl[warp][lane >> 2] = lsum;
+        }
+        consumer_bar();
+
+        // ---- block result: thread -> (head, 4 dims) ----
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm.cm[w][h]);
+        const float Ms = M == -INFINITY ? 0.f : M;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        float Lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float e = exp2f(sm.cm[w][h] - Ms);
+            const float4 v = *reinterpret_cast<const float4 *>(&sm.co[w][h][d0]);
+            o.x += e * v.x; o.y += e * v.y; o.z += e * v.z; o.w += e * v.w;
+            Lsum += e * sm.cl[w][h];
+        }
+        const ListSplit ls = list_split(s_off, u, b, W, n);
+        if (ls.bfirst == ls.blast) {
+            const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+            *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
+                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+        } else {
+            // this block's partial of list u -> slot b + u, then its arrival
+            float *part = a.partials + static_cast<size_t>(b + u) * kPartFloats;
+            *reinterpret_cast<float4 *>(part + 2 * kGroup + h * kHeadDim + d0) = o;
+            if ((tid & 31) == 0) {
+                part[h] = M;
+                part[kGroup + h] = Lsum;
+            }
+            // the CTA barrier makes every thread's partial visible to thread 0,
+            // whose acq_rel atomic publishes it and acquires the others
+            consumer_bar();
+            uint32_t prev = 0u;
+            if (ls.gn > 1 && tid == 0) prev = atomic_add_acq_rel_gpu(&a.gcounters[ls.gfirst + u], 1u);
+            if (more) {                    // first segment: resolved after the last one
+                pend_u = u;
+                pend_prev = prev;
+            } else {
+                resolve_list(a, sm.flag, u, ls, prev, h, d0);
+            }
+        }
+        consumer_bar();                    // sm.co / cm / cl are reused by the next segment
+        if (!more) break;
+        u = un;
     }
+    if (pend_u >= 0)
+        resolve_list(a, sm.flag, pend_u, list_split(s_off, pend_u, b, W, n), pend_prev, h, d0);
 }
 
 int attend_blocks_per_sm() { return kBlocksPerSm; }

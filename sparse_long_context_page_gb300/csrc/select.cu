@@ -225,11 +225,14 @@ __device__ unsigned long long sel_excl_scan(unsigned long long v, unsigned long 
 
 constexpr int kCand = 2048;                 // crossing-bin pages refined by one warp
 constexpr int kPairMax = 256;               // crossing-bin pages resolved pairwise
+static_assert(kPairMax * 4 <= kSelThreads, "pairwise path: at least 4 threads per candidate");
+static_assert(kMaxPagesPerSeq / kScoreChunk <= 256, "normalisers: one thread per chunk and head");
 
 struct SelectShared {
     uint32_t h1[kL1Bins];
     uint32_t h2[kL2Bins];
     uint32_t cand[kCand];                   // mass bits of the crossing bin's pages
+    uint32_t cand_fx[kPairMax];             // their fixed-point masses (pairwise path only)
     uint16_t cand_idx[kCand];               // their page indices (pairwise path only)
     int ncand;
     unsigned long long scan[32];
@@ -323,69 +326,56 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     }
     if (!mbar_wait(bar, 0) && tid == 0) raise_status(status, kDevTimeout);
 
-    // 2. normalisers of the group's heads: (max, sum) pairs merged online,
-    //    thread -> head tid/256, chunks tid%256 + 256k
+    // 2. normalisers of the group's heads.  Thread -> (head tid/256, chunk
+    //    tid%256): M = max of the chunk maxima, e_c = 2^(M_c - M) once per
+    //    chunk, Z = sum_c e_c Z_c; the chunk factor is e_c / (G Z).
     {
-        const int hg = tid >> 8, ci0 = tid & 255;
-        const float *cs = s_c + hg * ldc;
-        float mx = -INFINITY, z = 0.f;
-        for (int ci = ci0; ci < nch; ci += 256) {
-            const float cm = cs[2 * ci], cz = cs[2 * ci + 1];
-            if (cm == -INFINITY) continue;
-            const float nm = fmaxf(mx, cm);
-            z = z * exp2f(mx - nm) + cz * exp2f(cm - nm);
-            mx = nm;
+        const int hg = tid >> 8, ci = tid & 255;
+        float cm = -INFINITY, cz = 0.f;
+        if (ci < nch) {
+            cm = s_c[hg * ldc + 2 * ci];
+            cz = s_c[hg * ldc + 2 * ci + 1];
         }
+        float mx = cm;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float om = __shfl_xor_sync(0xffffffffu, mx, o);
-            const float oz = __shfl_xor_sync(0xffffffffu, z, o);
-            const float nm = fmaxf(mx, om);
-            z = (mx == -INFINITY ? 0.f : z * exp2f(mx - nm)) + (om == -INFINITY ? 0.f : oz * exp2f(om - nm));
-            mx = nm;
-        }
-        if (lane == 0) {
-            sh.red[warp] = mx;
-            sh.red2[warp] = z;
-        }
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) sh.red[warp] = mx;
         __syncthreads();
-        if ((tid & 255) == 0) {
-            float M = -INFINITY;
+        float M = -INFINITY;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) M = fmaxf(M, sh.red[hg * 8 + w]);
-            float Z = 0.f;
-            if (M != -INFINITY)
+        for (int w = 0; w < 8; ++w) M = fmaxf(M, sh.red[hg * 8 + w]);
+        const float e = (cm == -INFINITY) ? 0.f : exp2f(cm - M);
+        float z = cz * e;
 #pragma unroll
-                for (int w = 0; w < 8; ++w)
-                    if (sh.red[hg * 8 + w] != -INFINITY) Z += sh.red2[hg * 8 + w] * exp2f(sh.red[hg * 8 + w] - M);
-            sh.mmax[hg] = M;
-            sh.zinv[hg] = Z > 0.f ? 1.f / (kGroup * Z) : 0.f;
-        }
-    }
-    __syncthreads();
-    // per-chunk factors 2^(M_c - M) / (G Z) for the four heads
-    for (int ci = tid; ci < nch; ci += kSelThreads) {
-        float f[kGroup];
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (lane == 0) sh.red2[warp] = z;
+        __syncthreads();
+        float Z = 0.f;
 #pragma unroll
-        for (int g = 0; g < kGroup; ++g) {
-            const float mc = s_c[g * ldc + 2 * ci];
-            f[g] = (mc == -INFINITY || sh.mmax[g] == -INFINITY) ? 0.f : exp2f(mc - sh.mmax[g]) * sh.zinv[g];
-        }
-        s_f[ci] = make_float4(f[0], f[1], f[2], f[3]);
+        for (int w = 0; w < 8; ++w) Z += sh.red2[hg * 8 + w];
+        const float zinv = Z > 0.f ? 1.f / (kGroup * Z) : 0.f;
+        if (ci < nch) reinterpret_cast<float *>(s_f)[4 * ci + hg] = e * zinv;
     }
     __syncthreads();
 
     // 3. masses (natural page order, no exponentials) and the level-1 histogram
+    {
+        uint32_t xs[kSelStripes];
 #pragma unroll
-    for (int k = 0; k < kSelStripes; ++k) {
-        const int p = k * kSelThreads + tid;
-        if (p >= F) break;
-        const float4 f = s_f[p / kScoreChunk];
-        float m = s_w[p] * f.x + s_w[wld + p] * f.y + s_w[2 * wld + p] * f.z + s_w[3 * wld + p] * f.w;
-        m = fminf(fmaxf(m, 0.f), 1.5f);            // NaN -> 0
-        const uint32_t x = __float_as_uint(m);
-        s_bits[p] = x;
-        atomicAdd(&sh.h1[l1_bin(x)], to_fx(x));
+        for (int k = 0; k < kSelStripes; ++k) {
+            const int p = k * kSelThreads + tid;
+            xs[k] = 0u;
+            if (p < F) {
+                const float4 f = s_f[p / kScoreChunk];
+                float m = s_w[p] * f.x + s_w[wld + p] * f.y + s_w[2 * wld + p] * f.z + s_w[3 * wld + p] * f.w;
+                m = fminf(fmaxf(m, 0.f), 1.5f);            // NaN -> 0
+                xs[k] = __float_as_uint(m);
+                s_bits[p] = xs[k];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kSelStripes; ++k)
+            if (k * kSelThreads + tid < F) atomicAdd(&sh.h1[l1_bin(xs[k])], to_fx(xs[k]));
     }
     __syncthreads();
 
@@ -424,24 +414,34 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     if (tid == 0) sh.ncand = 0;
     __syncthreads();
     if (sh.found) {
+        // ballots first, one slot reservation per warp, then the writes
         const uint32_t lo = sh.lo, hi = sh.hi;
+        uint32_t xk[kSelStripes];
+        unsigned mk[kSelStripes];
+        int cntw = 0;
 #pragma unroll
         for (int k = 0; k < kSelStripes; ++k) {
-            const int p0 = k * kSelThreads + warp * 32;
-            if (p0 >= F) break;                              // warp-uniform
-            const int p = p0 + lane;
-            const uint32_t x = p < F ? s_bits[p] : 0u;
-            const bool in = p < F && x >= lo && x < hi;
-            const unsigned m = __ballot_sync(0xffffffffu, in);
-            if (m) {
-                int base = 0;
-                if (lane == 0) base = atomicAdd(&sh.ncand, __popc(m));
-                base = __shfl_sync(0xffffffffu, base, 0);
-                const int slot = base + __popc(m & ((1u << lane) - 1u));
-                if (in && slot < kCand) {
-                    sh.cand[slot] = x;
-                    sh.cand_idx[slot] = static_cast<uint16_t>(p);
+            const int p = k * kSelThreads + tid;
+            xk[k] = p < F ? s_bits[p] : 0u;
+            mk[k] = __ballot_sync(0xffffffffu, p < F && xk[k] >= lo && xk[k] < hi);
+            cntw += __popc(mk[k]);
+        }
+        if (cntw) {                                          // warp-uniform
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&sh.ncand, cntw);
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+            for (int k = 0; k < kSelStripes; ++k) {
+                if ((mk[k] >> lane) & 1u) {
+                    const int slot = base + __popc(mk[k] & lt);
+                    if (slot < kCand) {
+                        sh.cand[slot] = xk[k];
+                        sh.cand_idx[slot] = static_cast<uint16_t>(k * kSelThreads + tid);
+                        if (slot < kPairMax) sh.cand_fx[slot] = to_fx(xk[k]);
+                    }
                 }
+                base += __popc(mk[k]);
             }
         }
     }
@@ -449,23 +449,34 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     const bool use_pair = sh.found && sh.ncand <= kPairMax;
     const bool use_cand = sh.found && !use_pair && sh.ncand <= kCand;
     if (use_pair) {
-        // candidate t: masses ranked before it (larger, or equal with a lower
-        // page index); the candidate whose running sum crosses gamma is the cut
+        // candidate c: masses ranked before it (larger, or equal with a lower
+        // page index); the candidate whose running sum crosses gamma is the
+        // cut.  2^lg threads (lanes of one warp) share a candidate's sums.
         const int nc = sh.ncand;
         const unsigned long long above0 = sh.above;
         __syncthreads();                                 // every thread has read `above`
-        if (tid < nc) {
-            const uint32_t x = sh.cand[tid];
-            const uint32_t xi = sh.cand_idx[tid];
-            unsigned long long gt_sum = 0ull, tie_before = 0ull;
-            for (int c = 0; c < nc; ++c) {
+        const int lg = nc <= 32 ? 5 : nc <= 64 ? 4 : nc <= 128 ? 3 : 2;
+        const int ci = tid >> lg, part = tid & ((1 << lg) - 1);
+        uint32_t gt_sum = 0u, tie_before = 0u;          // <= the total mass: fits 32 bits
+        uint32_t x = 0u, xi = 0u;
+        if (ci < nc) {
+            x = sh.cand[ci];
+            xi = sh.cand_idx[ci];
+#pragma unroll 4
+            for (int c = part; c < nc; c += 1 << lg) {
                 const uint32_t y = sh.cand[c];
-                const uint32_t fy = to_fx(y);
-                if (y > x) gt_sum += fy;
-                else if (y == x && sh.cand_idx[c] < xi) tie_before += fy;
+                const uint32_t fy = sh.cand_fx[c];
+                gt_sum += y > x ? fy : 0u;
+                tie_before += (y == x && sh.cand_idx[c] < xi) ? fy : 0u;
             }
+        }
+        for (int o = 1; o < (1 << lg); o <<= 1) {
+            gt_sum += __shfl_xor_sync(0xffffffffu, gt_sum, o);
+            tie_before += __shfl_xor_sync(0xffffffffu, tie_before, o);
+        }
+        if (ci < nc && part == 0) {
             const unsigned long long before = above0 + gt_sum + tie_before;
-            if (before < gamma_fx && before + to_fx(x) >= gamma_fx) {   // exactly one candidate
+            if (before < gamma_fx && before + sh.cand_fx[ci] >= gamma_fx) {   // exactly one candidate
                 sh.lo = x;
                 sh.hi = x + 1u;
                 sh.above = above0 + gt_sum;
