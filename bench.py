@@ -21,6 +21,7 @@ exchange step); the max over ranks is reported.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import math
 import os
@@ -84,7 +85,9 @@ def max_over_ranks(x: float, world: int) -> float:
 # --------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 20 ms; stop() keeps those stamped inside the
+    timed window (host wall clock, bracketing the timed region)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -93,33 +96,40 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, window=None):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.05)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        sm, smax, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                smax.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]),
+                             {nm for nm, v in zip(names, parts[5:9]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for nm, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": float(max(smax)) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        where = "inside the timed region"
+        sel = rows
+        if window is not None:
+            sel = [r for r in rows if window[0] <= r[0] <= window[1]]
+            if not sel:                      # region shorter than the sampling period
+                sel = sorted(rows, key=lambda r: min(abs(r[0] - window[0]), abs(r[0] - window[1])))[:2]
+                where = "nearest samples to a timed region shorter than the sampling period"
+        reasons = set().union(*[r[3] for r in sel]) if sel else set()
+        return {"sm_mhz": float(np.median([r[1] for r in sel])) if sel else None,
+                "sm_max_mhz": float(max(r[2] for r in sel)) if sel else None,
+                "samples": len(sel), "where": where, "reasons": sorted(reasons)}
 
 
 # --------------------------------------------------------------------------- bytes
@@ -173,6 +183,16 @@ def time_oracle(w, layers, gamma, threads=0):
 
 # --------------------------------------------------------------------------- our arm
 
+def workload_config(args, w, head):
+    sp = w.spec
+    return {"workload": f"{args.workload}: {sp.batch} request(s) x {int(w.seq_lens.max())} "
+                        f"tokens, {sp.layers} layers, {sp.q_heads} q / {sp.kv_heads} kv heads, "
+                        f"d=128, 16-token pages",
+            "gamma": round(head, 4), "seed": args.seed,
+            "l2": "inputs larger than L2 (each step reads >5 GB of K/V)",
+            "graph": f"whole {sp.layers}-layer step in one CUDA graph, replayed"}
+
+
 def capture_step(st, gamma):
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -192,13 +212,15 @@ def time_graph(g, steps, warmup, world):
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
     e0.record()
     for _ in range(steps):
         g.replay()
     e1.record()
     torch.cuda.synchronize()
+    t1 = time.time()
     barrier(world)
-    return e0.elapsed_time(e1) / steps                   # ms per step
+    return e0.elapsed_time(e1) / steps, (t0, t1)         # ms per step, host window
 
 
 def time_parts(st, gamma, steps, warmup):
@@ -265,8 +287,8 @@ def run_ours(args):
     for gm in gammas:
         g = capture_step(st, gm)
         clocks = ClockSampler(local) if gm == head else None
-        ms = time_graph(g, args.steps if gm == head else max(3, args.steps // 2), args.warmup, world)
-        clk = clocks.stop() if clocks else None
+        ms, window = time_graph(g, args.steps if gm == head else max(3, args.steps // 2), args.warmup, world)
+        clk = clocks.stop(window) if clocks else None
         ms = max_over_ranks(ms, world)
         lengths = st.lengths.cpu().numpy()
         per_layer, total, frac, parts = step_bytes(w, lengths, gm)
@@ -336,12 +358,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic: seeded q/K/V, keys of 1-5% of pages per (layer, KV head) planted as "
                 "c*qhat+N(0,1) with c~U[0,4] (stands in for RULER at 128k)",
-        "config": {"workload": f"{args.workload}: {sp.batch} request(s) x {int(w.seq_lens.max())} "
-                               f"tokens, {sp.layers} layers, {sp.q_heads} q / {sp.kv_heads} kv heads, "
-                               f"d=128, 16-token pages",
-                   "gamma": round(head, 4), "seed": args.seed,
-                   "l2": "inputs larger than L2 (each step reads >5 GB of K/V)",
-                   "graph": "whole 32-layer step in one CUDA graph, replayed"},
+        "config": workload_config(args, w, head),
         "hbm_gbs": round(hd["bytes"] / hd["ms"] / 1e6, 1),
         "hbm_frac_of_measured": round(hd["bytes"] / hd["ms"] / 1e6 / peak, 4),
         "hbm_frac_of_8tbs_nominal": round(hd["bytes"] / hd["ms"] / 1e6 / 8000.0, 4),
@@ -385,23 +402,27 @@ def run_reference(args):
     w = W.make_workload(args.workload, seed=args.seed, device=dev)
     sp = w.spec
     head = float(np.float32(args.gamma))
+    from oracle import oracle as O
+    n_cached = min(sp.layers, 4)                 # host copies of 4 layers, cycled
+    samples = [oracle_sample(w, [l], head) for l in range(n_cached)]
     times = []
     used = 1
     for i in range(args.warmup + args.steps):
-        l = i % sp.layers
-        secs, used = time_oracle(w, [l], head)
+        q, summ, k, v = samples[i % n_cached]
+        t0 = time.perf_counter()
+        _, _, used = O.decode_step(q, summ, k, v, w.page_table, w.seq_lens, head, w.sm_scale)
         if i >= args.warmup:
-            times.append(secs * sp.layers)
+            times.append((time.perf_counter() - t0) * sp.layers)
     v = float(np.mean(times)) * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us/step",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same generator and seed)",
-        "config": {"workload": args.workload, "gamma": round(head, 4), "seed": args.seed},
+        "config": workload_config(args, w, head),
         "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": used, "kind": "oracle",
-                         "sample": f"one layer (all KV heads, full context) per step, "
-                                   f"x{sp.layers} for a 32-layer step"},
+                         "sample": f"one layer (all KV heads, full context) per step, layers "
+                                   f"0..{n_cached - 1} cycled, x{sp.layers} for a {sp.layers}-layer step"},
         "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -411,7 +432,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b_128k")
