@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import datetime
+import hashlib
 import json
 import math
 import os
@@ -37,6 +38,21 @@ sys.path.insert(0, ROOT)
 
 METRIC = "µs/decode-attn step & achieved HBM GB/s at 128k ctx, γ=0.99 vs γ=1 dense"
 FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) that k_attend moves per list entry, i.e. per kept
+# (page, KV head) with its 4 KB of K and 4 KB of V, from a one-pass ncu capture
+# of a dense launch (65,536 entries: dram__bytes_read.sum + dram__bytes_write.sum
+# divided by the entries).  The digest names the kernel sources the capture was
+# taken on; once they change the figure is withheld (traffic = null).
+ATTEND_TRAFFIC = {"sources_sha256": None, "dram_bytes_per_entry": None}
+
+
+def attend_sources_digest() -> str:
+    h = hashlib.sha256()
+    for f in ("attend.cu", "moira_device.cuh"):
+        with open(os.path.join(ROOT, "sparse_long_context_page_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def log(*a):
@@ -306,6 +322,11 @@ def run_ours(args):
     summ_layer = results[head]["parts"]["summaries"] / sp.layers
     att_bytes = per_layer - summ_layer                    # K/V of kept tokens + q + out
     att_gbs = float(att_bytes.mean() / (att_ms * 1e6))
+    entries = float(lengths.reshape(sp.layers, -1).sum(axis=1).mean())     # list entries per launch
+    digest = attend_sources_digest()
+    traffic = None
+    if ATTEND_TRAFFIC["dram_bytes_per_entry"] and ATTEND_TRAFFIC["sources_sha256"] == digest:
+        traffic = int(round(ATTEND_TRAFFIC["dram_bytes_per_entry"] * entries))
 
     # end to end: host q in, host out back, through moira_decode_step_host
     q_host = w.q.cpu().pin_memory()
@@ -375,7 +396,11 @@ def run_ours(args):
                          "how": "in-graph, 32 layers of one half per graph, CUDA events"},
         "roofline": {"kernel": "k_attend", "bound": "hbm", "achieved": round(att_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(att_gbs / peak, 4),
-                     "peak_source": peak_src, "traffic": None,
+                     "peak_source": peak_src, "traffic": traffic,
+                     "traffic_how": ("ncu DRAM bytes per list entry of a dense launch x entries per launch"
+                                     if traffic is not None else
+                                     "null: no ncu capture of the current k_attend sources"),
+                     "entries_per_launch": round(entries, 1),
                      "bytes_per_launch": int(att_bytes.mean())},
         "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "us/step",
                 "h2d_bytes_per_step": int(q_host.numel() * 2),

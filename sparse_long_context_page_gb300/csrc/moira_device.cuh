@@ -146,6 +146,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
     }
 }
 
+// ---- shared-memory histograms ------------------------------------------------------
+// hist[bin] += v for the active lanes.  When all active lanes of the warp hit
+// the same bin (a flat mass distribution sends whole warps to one bin) their
+// sum is added once; otherwise every lane adds its own.  Every lane of the
+// warp must call it.
+__device__ __forceinline__ void hist_add_warp(uint32_t *hist, uint32_t bin, uint32_t v, bool active)
+{
+    const unsigned act = __ballot_sync(0xffffffffu, active);
+    if (!active) return;
+    int same;
+    __match_all_sync(act, bin, &same);
+    if (same) {
+        const uint32_t sum = __reduce_add_sync(act, v);
+        if (static_cast<int>(__ffs(act)) - 1 == static_cast<int>(threadIdx.x & 31)) atomicAdd(&hist[bin], sum);
+    } else {
+        atomicAdd(&hist[bin], v);
+    }
+}
+
 // ---- programmatic dependent launch -------------------------------------------------
 // A kernel launched with programmatic stream serialisation may start while its
 // predecessor in the stream is still running.  pdl_wait() blocks until the

@@ -375,7 +375,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         }
 #pragma unroll
         for (int k = 0; k < kSelStripes; ++k)
-            if (k * kSelThreads + tid < F) atomicAdd(&sh.h1[l1_bin(xs[k])], to_fx(xs[k]));
+            if (k * kSelThreads < F)                      // warp-uniform: the stripe has pages
+                hist_add_warp(sh.h1, static_cast<uint32_t>(l1_bin(xs[k])), to_fx(xs[k]),
+                              k * kSelThreads + tid < F);
     }
     __syncthreads();
 
@@ -563,9 +565,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
 #pragma unroll
             for (int k = 0; k < kSelStripes; ++k) {
                 const int p = k * kSelThreads + tid;
-                if (p >= F) break;
-                const uint32_t x = s_bits[p];
-                if (x >= lo && x < hi) atomicAdd(&sh.h2[(x - lo) >> shift], to_fx(x));
+                if (k * kSelThreads >= F) break;              // warp-uniform
+                const uint32_t x = p < F ? s_bits[p] : 0u;
+                hist_add_warp(sh.h2, (x - lo) >> shift, to_fx(x), p < F && x >= lo && x < hi);
             }
             __syncthreads();
             if (warp == 0) {
