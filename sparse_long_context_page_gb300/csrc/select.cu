@@ -5,8 +5,9 @@
 //
 // Two kernels per layer:
 //  k_score  : all SMs stream the page summaries once (bulk copies into shared
-//             memory) and compute the page logits on the tensor cores, the G
-//             query rows of a KV head sharing every summary.  Per chunk of 32
+//             memory; blocks of 32 pages x 4 KV heads) and compute the page
+//             logits on the tensor cores, the G query rows of a KV head
+//             sharing every summary.  Per chunk of 32
 //             pages and query head it stores the chunk max M_c and sum
 //             Z_c = sum_p 2^(s_p - M_c), and per page the chunk-relative
 //             weight e_p = 2^(s_p - M_c) (log2-domain logits).
@@ -31,56 +32,59 @@ namespace moira {
 // ---------------------------------------------------------------------------
 // k_score
 // ---------------------------------------------------------------------------
-constexpr int kScoreThreads = 256;        // 8 warps
-constexpr int kScoreMaxItems = 2;         // (KV head, half) work items per warp for Hkv <= 8
+constexpr int kScoreThreads = 256;        // 8 warps: one (KV head, 16-page half) item each
+constexpr int kScoreHeads = 4;            // KV heads per block; blockIdx.z picks the slice
 
 // One block scores kScoreChunk (32) consecutive full pages of one request for
-// every KV head.  The page-table slice and the queries are read first; each
-// listed page's summaries (Hkv x 256 B, contiguous per physical page) then
-// arrive by 1-D bulk copies on one mbarrier, at a padded shared-memory stride
-// of Hkv*256+16 bytes so that 8 consecutive pages fall in different banks.
-// Logits come from the tensor cores: for KV head j and 16 pages,
+// kScoreHeads KV heads (Hkv = 8 takes two blocks per chunk, so about four
+// blocks share an SM and one block's loads overlap another's arithmetic).
+// The page-table slice and the queries are read first; each listed page's
+// summaries for the block's heads (contiguous, 256 B per head) then arrive by
+// 1-D bulk copies on one mbarrier, at a padded shared-memory stride so that 8
+// consecutive pages fall in different banks.  Logits come from the tensor
+// cores: for KV head j and 16 pages,
 //   S^T[h][p] = sum_d q_{4j+h}[d] * kbar_p[d]   (mma.m16n8k16, fp32 accumulate)
 // with A = the group's 4 query rows (repeated in rows 4-7) and B = the
 // summaries via ldmatrix, i.e. 8 k-steps x 2 MMAs per (head, 16 pages).
-__global__ void __launch_bounds__(kScoreThreads, 2) k_score(
+__global__ void __launch_bounds__(kScoreThreads, 4) k_score(
     const uint16_t *__restrict__ q, const uint16_t *__restrict__ summ,
     const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
     int max_pages, int ld, long long num_pages, float scale_log2, float *__restrict__ weights,
     float *__restrict__ chunks, int ldc, uint32_t *status)
 {
     extern __shared__ __align__(128) uint8_t s_summ[];     // [32 pages][stride]
-    __shared__ __align__(16) float s_s[32 * kScoreChunk];  // [Hq <= 32][32 pages] logits
+    __shared__ __align__(16) float s_s[kScoreHeads * kGroup * kScoreChunk];  // [local q head][page]
     __shared__ int s_phys[kScoreChunk];
     __shared__ __align__(8) unsigned long long s_bar;
     pdl_trigger();
     pdl_wait();                               // q and the score buffers follow earlier kernels
     const int r = blockIdx.y;
     const int chunk = blockIdx.x;
+    const int nh = min(hkv, kScoreHeads);     // KV heads of this block: jb .. jb + nh - 1
+    const int jb = blockIdx.z * nh;
     const int p0 = chunk * kScoreChunk;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t page_bytes = static_cast<uint32_t>(hkv) * kHeadDim * 2;
+    const uint32_t page_bytes = static_cast<uint32_t>(nh) * kHeadDim * 2;
     const uint32_t stride = page_bytes + 16;
     const uint32_t bar = smem_u32(&s_bar);
     const int hrow = (lane >> 2) & 3;
-    const int n_work = hkv * 2;               // (KV head, 16-page half)
+    const bool has_item = warp < nh * 2;      // (local KV head, 16-page half)
+    const int jl = warp >> 1, half = warp & 1;
 
     // loads that do not need the sequence length first: page ids and the
-    // query fragments of this warp's work items
+    // query fragments of this warp's item
     int L = seq_lens[r];
     const int pid_pre = (threadIdx.x < kScoreChunk && p0 + static_cast<int>(threadIdx.x) < max_pages)
                             ? __ldg(page_table + static_cast<size_t>(r) * max_pages + p0 + threadIdx.x)
                             : -1;
-    uint32_t aq[kScoreMaxItems][8][2];
-#pragma unroll
-    for (int it = 0; it < kScoreMaxItems; ++it) {
-        const int wi = warp + it * (kScoreThreads / 32);
-        const int j = wi < n_work ? (wi >> 1) : 0;
+    uint32_t aq[8][2];
+    {
+        const int j = jb + (has_item ? jl : 0);
         const uint16_t *qrow = q + (static_cast<size_t>(r) * hq + j * kGroup + hrow) * kHeadDim + 2 * (lane & 3);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            aq[it][ks][0] = wi < n_work ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)) : 0u;
-            aq[it][ks][1] = wi < n_work ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)) : 0u;
+            aq[ks][0] = has_item ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)) : 0u;
+            aq[ks][1] = has_item ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)) : 0u;
         }
     }
     L = L < 0 ? 0 : (L > max_pages * kPageSize ? max_pages * kPageSize : L);
@@ -101,49 +105,46 @@ __global__ void __launch_bounds__(kScoreThreads, 2) k_score(
         __syncwarp();
         if (ok)
             bulk_load(smem_u32(s_summ + lane * stride),
-                      summ + static_cast<size_t>(phys) * hkv * kHeadDim, page_bytes, bar);
-        if (lane < np && !ok) raise_status(status, kDevBadPage);
+                      summ + (static_cast<size_t>(phys) * hkv + jb) * kHeadDim, page_bytes, bar);
+        if (lane < np && !ok && blockIdx.z == 0) raise_status(status, kDevBadPage);
     }
     if (!mbar_wait(bar, 0) && threadIdx.x == 0) raise_status(status, kDevTimeout);
 
-#pragma unroll
-    for (int it = 0; it < kScoreMaxItems; ++it) {
-        const int wi = warp + it * (kScoreThreads / 32);
-        if (wi >= n_work) break;                              // warp-uniform
-        const int j = wi >> 1, half = wi & 1;
+    if (has_item) {                                          // warp-uniform
         float acc[2][4];
 #pragma unroll
         for (int x = 0; x < 2; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
         // ldmatrix rows: matrices (pages 0-7, dims +0), (pages 0-7, +8), (pages 8-15, +0), (8-15, +8)
         const int prow = half * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const uint32_t rbase = smem_u32(s_summ) + prow * stride + j * kHeadDim * 2 + (((lane >> 3) & 1) << 4);
+        const uint32_t rbase = smem_u32(s_summ) + prow * stride + jl * kHeadDim * 2 + (((lane >> 3) & 1) << 4);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4(rbase + ks * 32, b0, b1, b2, b3);
-            mma_bf16_16816(acc[0], aq[it][ks][0], 0u, aq[it][ks][1], 0u, b0, b1);
-            mma_bf16_16816(acc[1], aq[it][ks][0], 0u, aq[it][ks][1], 0u, b2, b3);
+            mma_bf16_16816(acc[0], aq[ks][0], 0u, aq[ks][1], 0u, b0, b1);
+            mma_bf16_16816(acc[1], aq[ks][0], 0u, aq[ks][1], 0u, b2, b3);
         }
         if (lane < 16) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int pl = half * 16 + nt * 8 + 2 * (lane & 3);
-                const int h = j * kGroup + hrow;
+                const int hl = jl * kGroup + hrow;
                 float s0 = acc[nt][0] * scale_log2, s1 = acc[nt][1] * scale_log2;
                 if (pl >= np || s_phys[pl] < 0 || s_phys[pl] >= num_pages) s0 = -INFINITY;
                 if (pl + 1 >= np || s_phys[pl + 1] < 0 || s_phys[pl + 1] >= num_pages) s1 = -INFINITY;
-                *reinterpret_cast<float2 *>(&s_s[h * kScoreChunk + pl]) = make_float2(s0, s1);
+                *reinterpret_cast<float2 *>(&s_s[hl * kScoreChunk + pl]) = make_float2(s0, s1);
             }
         }
     }
     __syncthreads();
-    // per query head: chunk max, chunk sum and the chunk-relative weights;
-    // 8 lanes per head (4 pages each), 4 heads per warp instruction
-    for (int h0 = warp * 4; h0 < hq; h0 += 4 * (kScoreThreads / 32)) {
-        const int h = h0 + (lane >> 3);
+    // per query head of the block: chunk max, chunk sum and the chunk-relative
+    // weights; 8 lanes per head (4 pages each), 4 heads per warp instruction
+    const int hql = nh * kGroup;
+    for (int h0 = warp * 4; h0 < hql; h0 += 4 * (kScoreThreads / 32)) {
+        const int hl = h0 + (lane >> 3);
         const int sub = lane & 7;
         float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (h < hq) v = *reinterpret_cast<const float4 *>(&s_s[h * kScoreChunk + sub * 4]);
+        if (hl < hql) v = *reinterpret_cast<const float4 *>(&s_s[hl * kScoreChunk + sub * 4]);
         float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -154,7 +155,8 @@ __global__ void __launch_bounds__(kScoreThreads, 2) k_score(
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        if (h < hq) {
+        if (hl < hql) {
+            const int h = jb * kGroup + hl;
             float *dst = weights + (static_cast<size_t>(r) * hq + h) * ld + p0 + sub * 4;
             *reinterpret_cast<float4 *>(dst) = e;          // pages past F are never read
             if (sub == 0) {
@@ -670,8 +672,9 @@ cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_ta
                          uint32_t *status, cudaStream_t stream)
 {
     const int n_chunks = (max_pages + kScoreChunk - 1) / kScoreChunk;
-    dim3 grid(n_chunks, batch);
-    const size_t smem = static_cast<size_t>(kScoreChunk) * (hkv * kHeadDim * 2 + 16);
+    const int nh = hkv < kScoreHeads ? hkv : kScoreHeads;
+    dim3 grid(n_chunks, batch, hkv / nh);
+    const size_t smem = static_cast<size_t>(kScoreChunk) * (nh * kHeadDim * 2 + 16);
     cudaError_t e = cudaFuncSetAttribute(k_score, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
