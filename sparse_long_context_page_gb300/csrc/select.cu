@@ -56,8 +56,8 @@ __global__ void __launch_bounds__(kScoreThreads, 4) k_score(
     __shared__ __align__(16) float s_s[kScoreHeads * kGroup * kScoreChunk];  // [local q head][page]
     __shared__ int s_phys[kScoreChunk];
     __shared__ __align__(8) unsigned long long s_bar;
-    pdl_trigger();
     pdl_wait();                               // q and the score buffers follow earlier kernels
+    pdl_trigger();                            // after the wait: see k_select
     const int r = blockIdx.y;
     const int chunk = blockIdx.x;
     const int nh = min(hkv, kScoreHeads);     // KV heads of this block: jb .. jb + nh - 1
@@ -274,8 +274,12 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_f + ldc / 2);   // [wld] mass bits
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_trigger();
-    pdl_wait();                               // weights and chunk stats come from k_score
+    // Before the wait: reads of the caller's inputs (page table, lengths) and
+    // shared-memory set-up.  With gamma < 1 this block can only have started
+    // once k_score passed its own wait (k_score signals its dependents after
+    // it), so the kernels that wrote those inputs have finished.  A dense
+    // launch has no k_score before it and waits first.
+    if (dense) pdl_wait();
     const int u = blockIdx.x;
     const int r = u / hkv, j = u % hkv;
     const int32_t *row = page_table + static_cast<size_t>(r) * max_pages;
@@ -296,6 +300,18 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         L = L < 0 ? 0 : max_pages * kPageSize;
     }
     const int F = L / kPageSize, T = (L % kPageSize) != 0;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    for (int b = tid; b < kL1Bins; b += kSelThreads) sh.h1[b] = 0u;
+    if (tid == 0) {
+        sh.found = 0;
+        sh.above = 0ull;
+    }
+    pdl_trigger();
+    pdl_wait();                               // weights and chunk stats come from k_score;
+                                              // lists may still be read by the last attention
     if (dense || F == 0) {                    // every page, no estimate
         for (int p = tid; p < F + T; p += kSelThreads) out[p] = row[p];
         if (tid == 0) lengths[u] = F + T;
@@ -305,11 +321,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     const int nstripes = (F + kSelThreads - 1) / kSelThreads;
 
     // 1. the group's weights and chunk statistics by bulk copies
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
+    __syncthreads();                          // barrier initialised, histogram cleared
     if (warp == 0) {
         const uint32_t wbytes = static_cast<uint32_t>((F + 3) & ~3) * 4;
         const uint32_t cbytes = static_cast<uint32_t>((2 * nch + 3) & ~3) * 4;
@@ -320,11 +332,6 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
             bulk_load(smem_u32(s_w + lane * wld), weights + hrow_i * ld, wbytes, bar);
             bulk_load(smem_u32(s_c + lane * ldc), chunks + hrow_i * ldc, cbytes, bar);
         }
-    }
-    for (int b = tid; b < kL1Bins; b += kSelThreads) sh.h1[b] = 0u;
-    if (tid == 0) {
-        sh.found = 0;
-        sh.above = 0ull;
     }
     if (!mbar_wait(bar, 0) && tid == 0) raise_status(status, kDevTimeout);
 
