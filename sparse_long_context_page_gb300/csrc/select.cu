@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kScoreThreads, 4) k_score(
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelStripes = kMaxPagesPerSeq / kSelThreads;   // stripes of 1024 pages
+static_assert(kSelStripes % 4 == 0, "masses: 4 pages per thread per pass");
 // Level-1 bins: the fp32 bit pattern >> 16 (exponent + 7 fraction bits, 128
 // bins per octave) for masses in [2^-32, 2); bin 0 gathers everything below.
 constexpr uint32_t kKeyLo = 95u << 7;
@@ -367,26 +368,32 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     }
     __syncthreads();
 
-    // 3. masses (natural page order, no exponentials) and the level-1 histogram
-    {
-        uint32_t xs[kSelStripes];
+    // 3. masses (natural page order, no exponentials) and the level-1
+    //    histogram; thread t takes 4 consecutive pages per pass (one chunk
+    //    factor, 16-byte shared-memory loads and stores)
 #pragma unroll
-        for (int k = 0; k < kSelStripes; ++k) {
-            const int p = k * kSelThreads + tid;
-            xs[k] = 0u;
-            if (p < F) {
-                const float4 f = s_f[p / kScoreChunk];
-                float m = s_w[p] * f.x + s_w[wld + p] * f.y + s_w[2 * wld + p] * f.z + s_w[3 * wld + p] * f.w;
-                m = fminf(fmaxf(m, 0.f), 1.5f);            // NaN -> 0
-                xs[k] = __float_as_uint(m);
-                s_bits[p] = xs[k];
-            }
+    for (int k = 0; k < kSelStripes / 4; ++k) {
+        const int p = (k * kSelThreads + tid) * 4;
+        uint32_t xs[4] = {0u, 0u, 0u, 0u};
+        if (p < F) {                        // weights are loaded up to F rounded up to 4
+            const float4 f = s_f[p / kScoreChunk];
+            const float4 w0 = *reinterpret_cast<const float4 *>(s_w + p);
+            const float4 w1 = *reinterpret_cast<const float4 *>(s_w + wld + p);
+            const float4 w2 = *reinterpret_cast<const float4 *>(s_w + 2 * wld + p);
+            const float4 w3 = *reinterpret_cast<const float4 *>(s_w + 3 * wld + p);
+            const float m[4] = {w0.x * f.x + w1.x * f.y + w2.x * f.z + w3.x * f.w,
+                                w0.y * f.x + w1.y * f.y + w2.y * f.z + w3.y * f.w,
+                                w0.z * f.x + w1.z * f.y + w2.z * f.z + w3.z * f.w,
+                                w0.w * f.x + w1.w * f.y + w2.w * f.z + w3.w * f.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xs[i] = __float_as_uint(fminf(fmaxf(m[i], 0.f), 1.5f));   // NaN -> 0
+            *reinterpret_cast<uint4 *>(s_bits + p) = make_uint4(xs[0], xs[1], xs[2], xs[3]);
         }
+        if ((k * kSelThreads + warp * 32) * 4 < F) {        // warp-uniform: the warp has pages
 #pragma unroll
-        for (int k = 0; k < kSelStripes; ++k)
-            if (k * kSelThreads < F)                      // warp-uniform: the stripe has pages
-                hist_add_warp(sh.h1, static_cast<uint32_t>(l1_bin(xs[k])), to_fx(xs[k]),
-                              k * kSelThreads + tid < F);
+            for (int i = 0; i < 4; ++i)
+                hist_add_warp(sh.h1, static_cast<uint32_t>(l1_bin(xs[i])), to_fx(xs[i]), p + i < F);
+        }
     }
     __syncthreads();
 
