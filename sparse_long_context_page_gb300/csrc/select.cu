@@ -240,7 +240,8 @@ struct SelectShared {
     int ncand;
     unsigned long long scan[32];
     unsigned long long above;
-    unsigned long long cnt[kSelStripes * kSelWarps];    // (stripe, warp): gt | eq << 32
+    uint32_t cnt[kSelStripes * kSelWarps];              // (stripe, warp): gt | eq << 16
+    uint32_t cnt_total;
     uint32_t lo, hi;
     int found;
     float red[kSelWarps];
@@ -633,7 +634,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     }
 
     // 7. ordered compaction by stripes of 1024 pages: per (stripe, warp) counts
-    //    of pages above and at the cut, one block scan, then warp ballots
+    //    of pages above and at the cut (16 bits each: at most 8192), one warp
+    //    scans them in page order, then warp ballots place the kept pages
     const unsigned lt_mask = (1u << lane) - 1u;
     unsigned gt_m[kSelStripes], eq_m[kSelStripes];
 #pragma unroll
@@ -644,24 +646,40 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
             const uint32_t x = p < F ? s_bits[p] : 0u;
             gt_m[k] = __ballot_sync(0xffffffffu, p < F && x > cut);
             eq_m[k] = __ballot_sync(0xffffffffu, p < F && x == cut);
-            if (lane == 0)
-                sh.cnt[k * kSelWarps + warp] =
-                    __popc(gt_m[k]) | (static_cast<unsigned long long>(__popc(eq_m[k])) << 32);
+            if (lane == 0) sh.cnt[k * kSelWarps + warp] = __popc(gt_m[k]) | (__popc(eq_m[k]) << 16);
         }
     }
     __syncthreads();
-    unsigned long long mine = 0ull, total;
-    if (tid < nstripes * kSelWarps) mine = sh.cnt[tid];
-    const unsigned long long pre = sel_excl_scan(mine, sh.scan, &total);
-    if (tid < nstripes * kSelWarps) sh.cnt[tid] = pre;
+    if (warp == 0) {                          // lane l: entries 8l .. 8l+7
+        uint32_t v[8], run = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            const uint32_t c = e < nstripes * kSelWarps ? sh.cnt[e] : 0u;
+            v[i] = run;
+            run += c;
+        }
+        uint32_t x = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        const uint32_t base = x - run;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (lane * 8 + i < nstripes * kSelWarps) sh.cnt[lane * 8 + i] = base + v[i];
+        if (lane == 31) sh.cnt_total = x;
+    }
     __syncthreads();
+    static_assert(kSelStripes * kSelWarps <= 256, "one warp scans the compaction counts");
     bool badp = false;
 #pragma unroll
     for (int k = 0; k < kSelStripes; ++k) {
         if (k < nstripes && (gt_m[k] | eq_m[k]) != 0u) {     // warp-uniform
-            const unsigned long long base = sh.cnt[k * kSelWarps + warp];
-            const unsigned long long gt_before = (base & 0xFFFFFFFFull) + __popc(gt_m[k] & lt_mask);
-            const unsigned long long eq_before = (base >> 32) + __popc(eq_m[k] & lt_mask);
+            const uint32_t base = sh.cnt[k * kSelWarps + warp];
+            const unsigned long long gt_before = (base & 0xFFFFu) + __popc(gt_m[k] & lt_mask);
+            const unsigned long long eq_before = (base >> 16) + __popc(eq_m[k] & lt_mask);
             const bool is_gt = (gt_m[k] >> lane) & 1u, is_eq = (eq_m[k] >> lane) & 1u;
             if (is_gt || (is_eq && eq_before < need_tied)) {
                 const int pos = static_cast<int>(gt_before + (eq_before < need_tied ? eq_before : need_tied));
@@ -672,7 +690,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     }
     if (badp) raise_status(status, kDevBadPage);
     if (tid == 0) {
-        const unsigned long long gt_all = total & 0xFFFFFFFFull, eq_all = total >> 32;
+        const unsigned long long gt_all = sh.cnt_total & 0xFFFFu, eq_all = sh.cnt_total >> 16;
         const int kept = static_cast<int>(gt_all + (eq_all < need_tied ? eq_all : need_tied));
         if (T) out[kept] = tail_pre;
         lengths[u] = kept + T;
