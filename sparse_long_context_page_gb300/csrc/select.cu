@@ -391,9 +391,13 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
             *reinterpret_cast<uint4 *>(s_bits + p) = make_uint4(xs[0], xs[1], xs[2], xs[3]);
         }
         if ((k * kSelThreads + warp * 32) * 4 < F) {        // warp-uniform: the warp has pages
+            // masses below 2^-32 are 0 in fixed point and add nothing (most
+            // pages of a peaked group)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                hist_add_warp(sh.h1, static_cast<uint32_t>(l1_bin(xs[i])), to_fx(xs[i]), p + i < F);
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t fx = to_fx(xs[i]);
+                hist_add_warp(sh.h1, static_cast<uint32_t>(l1_bin(xs[i])), fx, p + i < F && fx != 0u);
+            }
         }
     }
     __syncthreads();
@@ -622,15 +626,16 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     }
 
     // 6. cut value and how many pages tied at it are needed
-    uint32_t cut;
-    unsigned long long need_tied;
+    // (32-bit: gamma - above <= 2^31 and the cut's fixed-point mass < 2^32)
+    uint32_t cut, need_tied;
     if (sh.found) {
         cut = sh.lo;
-        const unsigned long long cfx = to_fx(cut);
-        need_tied = (gamma_fx - sh.above + cfx - 1ull) / cfx;   // cfx > 0: it carried the crossing
+        const uint32_t cfx = to_fx(cut);                          // > 0: it carried the crossing
+        const uint32_t d = static_cast<uint32_t>(gamma_fx - sh.above);
+        need_tied = d / cfx + (d % cfx != 0u ? 1u : 0u);
     } else {                                                      // total < gamma: keep all
         cut = 0u;
-        need_tied = 0xFFFFFFFFull;
+        need_tied = 0xFFFFFFFFu;
     }
 
     // 7. ordered compaction by stripes of 1024 pages: per (stripe, warp) counts
@@ -678,8 +683,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     for (int k = 0; k < kSelStripes; ++k) {
         if (k < nstripes && (gt_m[k] | eq_m[k]) != 0u) {     // warp-uniform
             const uint32_t base = sh.cnt[k * kSelWarps + warp];
-            const unsigned long long gt_before = (base & 0xFFFFu) + __popc(gt_m[k] & lt_mask);
-            const unsigned long long eq_before = (base >> 16) + __popc(eq_m[k] & lt_mask);
+            const uint32_t gt_before = (base & 0xFFFFu) + __popc(gt_m[k] & lt_mask);
+            const uint32_t eq_before = (base >> 16) + __popc(eq_m[k] & lt_mask);
             const bool is_gt = (gt_m[k] >> lane) & 1u, is_eq = (eq_m[k] >> lane) & 1u;
             if (is_gt || (is_eq && eq_before < need_tied)) {
                 const int pos = static_cast<int>(gt_before + (eq_before < need_tied ? eq_before : need_tied));
@@ -690,7 +695,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     }
     if (badp) raise_status(status, kDevBadPage);
     if (tid == 0) {
-        const unsigned long long gt_all = sh.cnt_total & 0xFFFFu, eq_all = sh.cnt_total >> 16;
+        const uint32_t gt_all = sh.cnt_total & 0xFFFFu, eq_all = sh.cnt_total >> 16;
         const int kept = static_cast<int>(gt_all + (eq_all < need_tied ? eq_all : need_tied));
         if (T) out[kept] = tail_pre;
         lengths[u] = kept + T;
