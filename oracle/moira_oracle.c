@@ -17,7 +17,9 @@
  *            Chinese translation), section 2 (related work): metadata
  *            estimators summarise a block by its mean vector (Quest/SparQ);
  *            section 1 and figure 1: top-p selection needs a global softmax to
- *            form the cumulative probability.
+ *            form the cumulative probability, top-k keeps a fixed budget, and
+ *            top-delta keeps the blocks within a relative threshold of the
+ *            local maximum.
  *
  * The estimator is not fixed by the pages; this oracle and the CUDA library
  * both use the same stated choice: a page's summary is the mean of its keys,
@@ -170,6 +172,45 @@ int32_t oracle_cover(const double *mass, int32_t F, double gamma,
     return k;
 }
 
+/* [FFD] section 1, figure 1 (a): a fixed budget keeps the k pages of largest
+ * estimated mass, equal masses by lower logical index (the coverage rule's
+ * order).  k >= F keeps every page; k <= 0 keeps none.
+ *   keep : [F] out, 1 for kept pages
+ * Returns the number of kept pages. */
+int32_t oracle_topk(const double *mass, int32_t F, int32_t k, uint8_t *keep)
+{
+    mass_idx *v = (mass_idx *)malloc(sizeof(mass_idx) * (size_t)(F > 0 ? F : 1));
+    for (int32_t p = 0; p < F; ++p) { v[p].m = mass[p]; v[p].p = p; }
+    qsort(v, (size_t)F, sizeof(mass_idx), by_mass_desc_then_index);
+    int32_t n = k < 0 ? 0 : (k > F ? F : k);
+    for (int32_t p = 0; p < F; ++p) keep[p] = 0;
+    for (int32_t i = 0; i < n; ++i) keep[v[i].p] = 1;
+    free(v);
+    return n;
+}
+
+/* [FFD] section 1, figure 1 (c) and its list of contributions: top-delta keeps
+ * the blocks whose estimated contribution is within a relative threshold delta
+ * of the local maximum.  The formula itself is cut from the page; the reading
+ * taken: keep page p when mass_p >= delta * max_q mass_q (the same estimated
+ * masses as the coverage rule, the maximum over the unit's full pages).
+ * delta <= 0 keeps every page.
+ *   keep : [F] out, 1 for kept pages
+ * Returns the number of kept pages. */
+int32_t oracle_topdelta(const double *mass, int32_t F, double delta, uint8_t *keep)
+{
+    double mx = 0.0;
+    for (int32_t p = 0; p < F; ++p)
+        if (mass[p] > mx) mx = mass[p];
+    const double thr = delta * mx;
+    int32_t n = 0;
+    for (int32_t p = 0; p < F; ++p) {
+        keep[p] = mass[p] >= thr;
+        n += keep[p];
+    }
+    return n;
+}
+
 /* One unit's selection: estimator + coverage + the partial tail page.
  *   summ_pool : [*][Hkv][d] bf16 summaries by physical page; page_row maps
  *               logical page p to its physical page
@@ -204,6 +245,43 @@ int32_t oracle_select_unit(const uint16_t *q_group, const uint16_t *summ_pool,
         if (keep[p]) list_out[n++] = p;
     if (T) list_out[n++] = F;
     if (mass_out) memcpy(mass_out, mass, sizeof(double) * (size_t)F);
+    free(summ);
+    free(mass);
+    free(keep);
+    return n;
+}
+
+/* oracle_select_unit with the rule chosen by `rule`: 0 = coverage (param =
+ * gamma), 1 = top-k (param = k, a whole number), 2 = top-delta (param =
+ * delta).  The estimator, the tail page and the list order are the same for
+ * every rule.  Returns the list length. */
+int32_t oracle_select_unit_rule(const uint16_t *q_group, const uint16_t *summ_pool,
+                                int32_t Hkv, int32_t j, const int32_t *page_row,
+                                int32_t seq_len, int32_t S, int32_t G, int32_t d,
+                                int32_t rule, double param, double sm_scale,
+                                int32_t *list_out)
+{
+    if (rule == 0)
+        return oracle_select_unit(q_group, summ_pool, Hkv, j, page_row, seq_len, S, G, d,
+                                  param, sm_scale, list_out, NULL, NULL, NULL);
+    int32_t F = seq_len / S, T = (seq_len % S) != 0;
+    int32_t n = 0;
+    if (F == 0) {
+        for (int32_t p = 0; p < T; ++p) list_out[n++] = p;
+        return n;
+    }
+    uint16_t *summ = (uint16_t *)calloc((size_t)F * d, sizeof(uint16_t));
+    for (int32_t p = 0; p < F; ++p)
+        memcpy(summ + (size_t)p * d,
+               summ_pool + ((size_t)page_row[p] * Hkv + j) * d, sizeof(uint16_t) * d);
+    double *mass = (double *)malloc(sizeof(double) * (size_t)F);
+    uint8_t *keep = (uint8_t *)malloc((size_t)F);
+    oracle_page_mass(q_group, summ, G, F, d, sm_scale, NULL, mass);
+    if (rule == 1) oracle_topk(mass, F, (int32_t)param, keep);
+    else oracle_topdelta(mass, F, param, keep);
+    for (int32_t p = 0; p < F; ++p)
+        if (keep[p]) list_out[n++] = p;
+    if (T) list_out[n++] = F;
     free(summ);
     free(mass);
     free(keep);

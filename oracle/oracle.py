@@ -54,6 +54,15 @@ def _load():
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_double, ctypes.c_double, _i32p, _f64p, _i32p, _f64p]
     lib.oracle_select_unit.restype = ctypes.c_int32
+    lib.oracle_topk.argtypes = [_f64p, ctypes.c_int32, ctypes.c_int32, _u8p]
+    lib.oracle_topk.restype = ctypes.c_int32
+    lib.oracle_topdelta.argtypes = [_f64p, ctypes.c_int32, ctypes.c_double, _u8p]
+    lib.oracle_topdelta.restype = ctypes.c_int32
+    lib.oracle_select_unit_rule.argtypes = [_u16p, _u16p, ctypes.c_int32, ctypes.c_int32, _i32p,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                            ctypes.c_double, _i32p]
+    lib.oracle_select_unit_rule.restype = ctypes.c_int32
     lib.oracle_attend_unit.argtypes = [_u16p, _u16p, _u16p, ctypes.c_int32, ctypes.c_int32, _i32p,
                                        _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_double, _f64p]
@@ -137,6 +146,43 @@ def select_unit(q_group, summ_pool, j, page_row, seq_len, gamma, sm_scale, page_
                                float(sm_scale), lst.ctypes.data_as(_i32p), mass.ctypes.data_as(_f64p),
                                order.ctypes.data_as(_i32p), cum.ctypes.data_as(_f64p))
     return lst[:n].copy(), mass, order, cum
+
+
+RULE_COVERAGE, RULE_TOPK, RULE_TOPDELTA = 0, 1, 2
+
+
+def topk(mass: np.ndarray, k: int) -> np.ndarray:
+    """Fixed budget: keep mask of the k largest masses (ties: lower index)."""
+    lib = _load()
+    m = np.ascontiguousarray(mass, np.float64)
+    keep = np.zeros(m.shape[0], np.uint8)
+    lib.oracle_topk(m.ctypes.data_as(_f64p), m.shape[0], int(k), keep.ctypes.data_as(_u8p))
+    return keep.astype(bool)
+
+
+def topdelta(mass: np.ndarray, delta: float) -> np.ndarray:
+    """Relative threshold: keep mask of masses >= delta * max mass."""
+    lib = _load()
+    m = np.ascontiguousarray(mass, np.float64)
+    keep = np.zeros(m.shape[0], np.uint8)
+    lib.oracle_topdelta(m.ctypes.data_as(_f64p), m.shape[0], float(delta), keep.ctypes.data_as(_u8p))
+    return keep.astype(bool)
+
+
+def select_unit_rule(q_group, summ_pool, j, page_row, seq_len, rule, param, sm_scale, page_size=16):
+    """Selection for one unit under `rule` (RULE_COVERAGE / RULE_TOPK /
+    RULE_TOPDELTA with param gamma / k / delta) -> kept LOGICAL pages."""
+    lib = _load()
+    G, d = q_group.shape
+    Hkv = summ_pool.shape[-2]
+    F = seq_len // page_size
+    qa, qp = _c(q_group, np.uint16, _u16p)
+    sa, sp = _c(summ_pool, np.uint16, _u16p)
+    ra, rp = _c(page_row, np.int32, _i32p)
+    lst = np.empty(F + 1, np.int32)
+    n = lib.oracle_select_unit_rule(qp, sp, Hkv, j, rp, seq_len, page_size, G, d, int(rule),
+                                    float(param), float(sm_scale), lst.ctypes.data_as(_i32p))
+    return lst[:n].copy()
 
 
 def attend_unit(q_group, k_pool, v_pool, j, page_row, lst, seq_len, sm_scale):

@@ -270,6 +270,91 @@ def test_select_unit_uniform_and_dominant_and_permutation():
         assert np.array_equal(a, b)
 
 
+# ---------------------------------------------------------------- alternative rules
+
+def _dominance_set(m, k):
+    """Brute force: the k-subsets S where every kept page outranks every
+    dropped one (larger mass, or equal mass and lower index)."""
+    F = len(m)
+    out = []
+    for S in itertools.combinations(range(F), k):
+        rest = [q for q in range(F) if q not in S]
+        if all(m[p] > m[q] or (m[p] == m[q] and p < q) for p in S for q in rest):
+            out.append(set(S))
+    return out
+
+
+def test_topk_brute_force_unique_and_heaviest():
+    rng = np.random.default_rng(21)
+    for trial in range(60):
+        F = int(rng.integers(1, 10))
+        m = rng.integers(0, 4, F).astype(np.float64)        # many ties
+        m = m / m.sum() if m.sum() > 0 else np.full(F, 1.0 / F)
+        for k in range(0, F + 2):
+            keep = oracle.topk(m, k)
+            kk = min(k, F)
+            sets = _dominance_set(m, kk)
+            assert len(sets) == 1                            # the order is total
+            assert set(np.flatnonzero(keep)) == sets[0]
+            best = max(sum(m[list(S)]) for S in itertools.combinations(range(F), kk))
+            assert math.isclose(m[keep].sum(), best, abs_tol=1e-15)
+
+
+def test_topk_uniform_nesting_and_limits():
+    F = 37
+    m = np.full(F, 1.0 / F)
+    assert np.array_equal(np.flatnonzero(oracle.topk(m, 5)), np.arange(5))   # ties: lowest indices
+    assert oracle.topk(m, 0).sum() == 0 and oracle.topk(m, F + 9).all()
+    rng = np.random.default_rng(22)
+    m = rng.dirichlet(np.full(F, 0.3))
+    prev = np.zeros(F, bool)
+    for k in range(F + 1):
+        cur = oracle.topk(m, k)
+        assert cur.sum() == k and np.all(cur >= prev)        # nested in k
+        prev = cur
+
+
+def test_topdelta_threshold_definition_and_relation_to_topk():
+    rng = np.random.default_rng(23)
+    for trial in range(40):
+        F = int(rng.integers(1, 60))
+        m = rng.dirichlet(np.full(F, 0.5))
+        mx = m.max()
+        for delta in (1.0, 0.9, 0.5, 0.1, 1e-3, 0.0, -1.0):
+            keep = oracle.topdelta(m, delta)
+            # restated from the definition, not from the oracle
+            assert np.array_equal(keep, m >= delta * mx)
+            # without ties a threshold set is a prefix of the rule order
+            assert np.array_equal(keep, oracle.topk(m, int(keep.sum())))
+        assert oracle.topdelta(m, 1.0).sum() == int((m == mx).sum())
+        assert oracle.topdelta(m, 0.0).all()
+    m = np.array([0.25, 0.25, 0.5, 0.0])
+    assert list(oracle.topdelta(m, 0.5)) == [True, True, True, False]     # >= at the threshold
+    assert list(oracle.topdelta(m, 0.51)) == [False, False, True, False]
+
+
+def test_select_unit_rule_matches_mass_level_rules():
+    rng = np.random.default_rng(24)
+    n = 61
+    L = 16 * 60 + 7                                          # 60 full pages + tail
+    kp = _pool(rng, n)
+    summ = oracle.summaries(kp.reshape(-1, 16, D)).reshape(n, 2, D)
+    row = rng.permutation(n).astype(np.int32)
+    q = bf16_bits(rng.standard_normal((4, D)))
+    base, mass, *_ = oracle.select_unit(q, summ, 1, row, L, 0.9, SM)
+    a = oracle.select_unit_rule(q, summ, 1, row, L, oracle.RULE_COVERAGE, 0.9, SM)
+    assert np.array_equal(a, base)
+    for k in (0, 1, 7, 60, 99):
+        lst = oracle.select_unit_rule(q, summ, 1, row, L, oracle.RULE_TOPK, k, SM)
+        want = list(np.flatnonzero(oracle.topk(mass, k))) + [60]
+        assert list(lst) == want
+    for delta in (0.9, 0.1, 1e-4):
+        lst = oracle.select_unit_rule(q, summ, 1, row, L, oracle.RULE_TOPDELTA, delta, SM)
+        want = list(np.flatnonzero(mass >= delta * mass.max())) + [60]
+        assert list(lst) == want
+    assert list(oracle.select_unit_rule(q, summ, 1, row, 9, oracle.RULE_TOPK, 3, SM)) == [0]   # tail only
+
+
 # ---------------------------------------------------------------- attention
 
 def _sdpa(q, k, v, scale):
