@@ -136,6 +136,30 @@ moira_status moira_select(const moira_shape *shape, const void *q, const void *s
                           int32_t *lengths, void *workspace, size_t ws_bytes,
                           moira_stream_t stream);
 
+/* Page rules for moira_select_rule. */
+typedef enum {
+    MOIRA_RULE_COVERAGE = 0,  /* smallest set reaching mass gamma ("MOIRA" abstract); param = gamma */
+    MOIRA_RULE_TOPK = 1,      /* fixed budget ("Faster Flash Decoding" section 1, figure 1 (a)):
+                                 the k heaviest full pages, equal masses lower index first;
+                                 param = k, a whole number in [0, 2^24] */
+    MOIRA_RULE_TOPDELTA = 2   /* relative threshold to the maximum ("Faster Flash Decoding"
+                                 section 1, figure 1 (c); its formula is cut from the page, read
+                                 as): every full page with mass >= delta * the unit's largest
+                                 mass; param = delta in (0, 1] */
+} moira_rule;
+
+/* moira_select with the page rule chosen by `rule` (see moira_rule).  The
+ * estimator, the partial tail page (always kept, last), the list order, the
+ * buffers, the workspace and the errors are those of moira_select;
+ * MOIRA_RULE_COVERAGE with param = gamma is exactly moira_select.  A `param`
+ * outside the rule's range returns MOIRA_EINVAL and launches nothing.  The
+ * rules let a caller compare selections that read the same number of bytes. */
+moira_status moira_select_rule(const moira_shape *shape, const void *q, const void *summ,
+                               const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                               int32_t max_pages, int32_t rule, float param, float sm_scale,
+                               int32_t *lists, int32_t *lengths, void *workspace, size_t ws_bytes,
+                               moira_stream_t stream);
+
 /* Self-planning ragged attention ("MOIRA" abstract: "lets each thread block
  * derive its own share of the work from the list lengths, so the whole
  * decode step stays inside the CUDA graph").  A fixed grid (a multiple of

@@ -31,7 +31,10 @@ MAX_PAGES_PER_SEQ, MAX_UNITS = 8192, 4096
 EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summaries",
            "moira_select", "moira_attend", "moira_decode_step", "moira_decode_step_host",
            "moira_read_device_status", "moira_attend_grid_blocks", "moira_status_string",
-           "moira_select_noalloc")
+           "moira_select_noalloc", "moira_select_rule")
+
+# page rules of moira_select_rule (moira_rule in include/moira.h)
+RULE_COVERAGE, RULE_TOPK, RULE_TOPDELTA = 0, 1, 2
 
 
 class MoiraError(RuntimeError):
@@ -76,6 +79,9 @@ def load_library(build_if_missing: bool = True):
     lib.moira_select.argtypes = [sp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, ctypes.c_float,
                                  _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.moira_select.restype = ctypes.c_int
+    lib.moira_select_rule.argtypes = [sp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
+                                      ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.moira_select_rule.restype = ctypes.c_int
     lib.moira_attend.argtypes = [sp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _vp,
                                  _vp, ctypes.c_size_t, _vp]
     lib.moira_attend.restype = ctypes.c_int
@@ -171,6 +177,23 @@ def select(shape: Shape, q, summ, page_table, seq_lens, gamma: float, sm_scale: 
                             float(gamma), float(sm_scale), _dev(lists, "lists", torch.int32),
                             _dev(lengths, "lengths", torch.int32), _dev(ws, "workspace", torch.uint8),
                             ws.numel(), _stream(stream)), "moira_select")
+
+
+def select_rule(shape: Shape, q, summ, page_table, seq_lens, rule: int, param: float,
+                sm_scale: float, lists, lengths, ws, stream=None):
+    """Per-(request, KV head) lists for one layer under a page rule:
+    RULE_COVERAGE (param = gamma), RULE_TOPK (param = k) or RULE_TOPDELTA
+    (param = delta); see include/moira.h."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    _check(lib.moira_select_rule(ctypes.byref(shape), _dev(q, "q", torch.bfloat16),
+                                 _dev(summ, "summ", torch.bfloat16),
+                                 _dev(page_table, "page_table", torch.int32, 2),
+                                 _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                                 int(rule), float(param), float(sm_scale),
+                                 _dev(lists, "lists", torch.int32), _dev(lengths, "lengths", torch.int32),
+                                 _dev(ws, "workspace", torch.uint8), ws.numel(), _stream(stream)),
+           "moira_select_rule")
 
 
 def attend(shape: Shape, q, k_pool, v_pool, lists, lengths, seq_lens, max_pages: int,

@@ -113,18 +113,28 @@ moira_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOIRA_OK : M
 
 moira_status select_impl(const moira_shape *shape, const void *q, const void *summ,
                          const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
-                         int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
-                         int32_t *lengths, void *ws, size_t ws_bytes, cudaStream_t stream)
+                         int32_t max_pages, int32_t rule, float param, float sm_scale,
+                         int32_t *lists, int32_t *lengths, void *ws, size_t ws_bytes,
+                         cudaStream_t stream)
 {
+    static_assert(MOIRA_RULE_COVERAGE == kRuleCoverage && MOIRA_RULE_TOPK == kRuleTopK &&
+                      MOIRA_RULE_TOPDELTA == kRuleTopDelta,
+                  "public rule values match the kernels'");
+    const float gamma = rule == MOIRA_RULE_COVERAGE ? param : 0.5f;
     const WsLayout L = layout_for(shape, batch, max_pages);
     uint8_t *w = static_cast<uint8_t *>(ws);
     uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
     float *scores = reinterpret_cast<float *>(w + L.scores);
     float *chunks = reinterpret_cast<float *>(w + L.chunks);
-    const bool dense = gamma >= 1.0f;
-    // gamma on the 2^-31 fixed-point grid of the mass histograms, rounded up
-    const unsigned long long gfx =
-        dense ? 0ull : static_cast<unsigned long long>(std::ceil(static_cast<double>(gamma) * 0x1p31));
+    const bool dense = rule == MOIRA_RULE_COVERAGE && gamma >= 1.0f;
+    // coverage: gamma on the 2^-31 fixed-point grid of the mass histograms,
+    // rounded up; top-k: the page count
+    unsigned long long gfx = 0ull;
+    if (rule == MOIRA_RULE_COVERAGE && !dense)
+        gfx = static_cast<unsigned long long>(std::ceil(static_cast<double>(gamma) * 0x1p31));
+    else if (rule == MOIRA_RULE_TOPK)
+        gfx = static_cast<unsigned long long>(param);
+    const float delta = rule == MOIRA_RULE_TOPDELTA ? param : 0.f;
     if (!dense) {
         const float scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
         cudaError_t e = launch_score(q, summ, page_table, seq_lens, batch, shape->num_q_heads,
@@ -134,8 +144,8 @@ moira_status select_impl(const moira_shape *shape, const void *q, const void *su
     }
     return cuda_status(launch_select(scores, chunks, page_table, seq_lens, batch,
                                      shape->num_q_heads, shape->num_kv_heads, max_pages,
-                                     shape->num_phys_pages, gfx, dense, lists, lengths, status,
-                                     stream));
+                                     shape->num_phys_pages, rule, gfx, delta, dense, lists,
+                                     lengths, status, stream));
 }
 
 moira_status attend_impl(const moira_shape *shape, const void *q, const void *k_pool,
@@ -212,8 +222,40 @@ moira_status moira_select(const moira_shape *shape, const void *q, const void *s
     if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
     if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
     if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
-    return select_impl(shape, q, summ, page_table, seq_lens, batch, max_pages, gamma, sm_scale,
-                       lists, lengths, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return select_impl(shape, q, summ, page_table, seq_lens, batch, max_pages,
+                       MOIRA_RULE_COVERAGE, gamma, sm_scale, lists, lengths, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+moira_status moira_select_rule(const moira_shape *shape, const void *q, const void *summ,
+                               const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                               int32_t max_pages, int32_t rule, float param, float sm_scale,
+                               int32_t *lists, int32_t *lengths, void *workspace, size_t ws_bytes,
+                               moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (!finite_pos(sm_scale)) return MOIRA_EINVAL;
+    switch (rule) {
+    case MOIRA_RULE_COVERAGE:
+        if (!(param > 0.f && param <= 1.f)) return MOIRA_EINVAL;
+        break;
+    case MOIRA_RULE_TOPK:
+        if (!(param >= 0.f && param <= 16777216.f) || param != std::floor(param)) return MOIRA_EINVAL;
+        break;
+    case MOIRA_RULE_TOPDELTA:
+        if (!(param > 0.f && param <= 1.f)) return MOIRA_EINVAL;
+        break;
+    default:
+        return MOIRA_EINVAL;
+    }
+    if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
+    if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
+    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
+    return select_impl(shape, q, summ, page_table, seq_lens, batch, max_pages, rule, param,
+                       sm_scale, lists, lengths, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 moira_status moira_attend(const moira_shape *shape, const void *q, const void *k_pool,
@@ -266,8 +308,8 @@ moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, con
     const uint16_t *sp = static_cast<const uint16_t *>(summ_all);
     for (int l = 0; l < num_layers; ++l) {
         st = select_impl(shape, q + l * q_layer, sp + l * sm_layer, page_table, seq_lens, batch,
-                         max_pages, gamma, sm_scale, lists, lengths_all + l * len_layer, workspace,
-                         ws_bytes, s);
+                         max_pages, MOIRA_RULE_COVERAGE, gamma, sm_scale, lists,
+                         lengths_all + l * len_layer, workspace, ws_bytes, s);
         if (st != MOIRA_OK) return st;
         st = attend_impl(shape, q + l * q_layer, kp + l * kv_layer, vp + l * kv_layer, lists,
                          lengths_all + l * len_layer, seq_lens, batch, max_pages, sm_scale,

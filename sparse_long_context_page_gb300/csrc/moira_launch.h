@@ -15,10 +15,16 @@ cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_ta
                          long long num_pages, float scale_log2, float *scores, float *chunks,
                          uint32_t *status, cudaStream_t stream);
 
+// Page rules of the selection (the values of the public moira_rule).
+constexpr int kRuleCoverage = 0;          // target = ceil(gamma * 2^31)
+constexpr int kRuleTopK = 1;              // target = k pages
+constexpr int kRuleTopDelta = 2;          // delta: keep mass >= delta * max mass
+
 cudaError_t launch_select(const float *scores, const float *chunks, const int32_t *page_table,
                           const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
-                          long long num_pages, unsigned long long gamma_fx, bool dense,
-                          int32_t *lists, int32_t *lengths, uint32_t *status, cudaStream_t stream);
+                          long long num_pages, int rule, unsigned long long target, float delta,
+                          bool dense, int32_t *lists, int32_t *lengths, uint32_t *status,
+                          cudaStream_t stream);
 
 struct AttendArgs {
     const void *q;

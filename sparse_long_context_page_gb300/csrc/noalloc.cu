@@ -105,7 +105,8 @@ extern "C" moira_status moira_select_noalloc(const moira_shape *shape, const voi
             return MOIRA_ECUDA;
     }
     if (launch_select(scores, chunks, page_table, seq_lens, batch, hq, shape->num_kv_heads,
-                      max_pages, shape->num_phys_pages, gfx, dense, lists, lengths, status, s) !=
+                      max_pages, shape->num_phys_pages, kRuleCoverage, gfx, 0.f, dense, lists,
+                      lengths, status, s) !=
         cudaSuccess)
         return MOIRA_ECUDA;
     return MOIRA_OK;

@@ -197,6 +197,13 @@ __device__ __forceinline__ uint32_t to_fx(uint32_t x)
     return __float2uint_rn(__uint_as_float(x) * 0x1p31f);
 }
 
+// What a page adds to the histograms: its fixed-point mass for the coverage
+// rule, 1 for top-k (the descent then counts pages instead of mass).
+__device__ __forceinline__ uint32_t rule_weight(int rule, uint32_t x)
+{
+    return rule == kRuleTopK ? 1u : to_fx(x);
+}
+
 // Exclusive scan over the block in thread order; *total gets the sum.
 __device__ unsigned long long sel_excl_scan(unsigned long long v, unsigned long long *s_warp,
                                             unsigned long long *total)
@@ -249,6 +256,7 @@ struct SelectShared {
     float mmax[kGroup];
     float zinv[kGroup];
     unsigned long long bar;
+    uint32_t xmax;                          // largest mass pattern (top-delta)
 };
 
 // Dynamic shared memory of k_select: the group's weights, its chunk
@@ -264,7 +272,8 @@ __host__ __device__ inline size_t select_smem_bytes(int max_pages, int ldc)
 __global__ void __launch_bounds__(kSelThreads) k_select(
     const float *__restrict__ weights, const float *__restrict__ chunks,
     const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
-    int max_pages, int ld, int ldc, long long num_pages, unsigned long long gamma_fx, int dense,
+    int max_pages, int ld, int ldc, long long num_pages, int rule, unsigned long long target,
+    float delta, int dense,
     int32_t *__restrict__ lists, int32_t *__restrict__ lengths, uint32_t *status)
 {
     extern __shared__ __align__(16) float s_dyn[];
@@ -310,11 +319,20 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     if (tid == 0) {
         sh.found = 0;
         sh.above = 0ull;
+        sh.xmax = 0u;
     }
     pdl_trigger();
     pdl_wait();                               // weights and chunk stats come from k_score;
                                               // lists may still be read by the last attention
-    if (dense || F == 0) {                    // every page, no estimate
+    if (rule == kRuleTopK && target == 0ull && F > 0 && !dense) {   // no full page, only the tail
+        if (tid == 0) {
+            if (T) out[0] = row[F];
+            lengths[u] = T;
+        }
+        return;
+    }
+    if (dense || F == 0 || (rule == kRuleTopK && target >= static_cast<unsigned long long>(F))) {
+        // every page, no estimate
         for (int p = tid; p < F + T; p += kSelThreads) out[p] = row[p];
         if (tid == 0) lengths[u] = F + T;
         return;
@@ -391,247 +409,261 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
             *reinterpret_cast<uint4 *>(s_bits + p) = make_uint4(xs[0], xs[1], xs[2], xs[3]);
         }
         if ((k * kSelThreads + warp * 32) * 4 < F) {        // warp-uniform: the warp has pages
-            // masses below 2^-32 are 0 in fixed point and add nothing (most
-            // pages of a peaked group)
+            if (rule == kRuleTopDelta) {      // only the largest mass is needed
+                uint32_t mx = 0u;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t fx = to_fx(xs[i]);
-                hist_add_warp(sh.h1, static_cast<uint32_t>(l1_bin(xs[i])), fx, p + i < F && fx != 0u);
-            }
-        }
-    }
-    __syncthreads();
-
-    // 4. level-1 cut: thread t owns bins (top_t - kL1PerThread, top_t] from the top
-    {
-        const int top = kL1Bins - 1 - tid * kL1PerThread;
-        unsigned long long mine = 0ull;
+                for (int i = 0; i < 4; ++i) mx = max(mx, p + i < F ? xs[i] : 0u);
+                mx = __reduce_max_sync(0xffffffffu, mx);
+                if (lane == 0) atomicMax(&sh.xmax, mx);
+            } else {
+                // masses below 2^-32 are 0 in fixed point and add nothing to
+                // the coverage histogram (most pages of a peaked group)
 #pragma unroll
-        for (int i = 0; i < kL1PerThread; ++i)
-            if (top - i >= 0) mine += sh.h1[top - i];
-        unsigned long long total;
-        unsigned long long acc = sel_excl_scan(mine, sh.scan, &total);
-        if (acc < gamma_fx && acc + mine >= gamma_fx) {
-#pragma unroll
-            for (int i = 0; i < kL1PerThread; ++i) {
-                const int b = top - i;
-                if (b < 0) break;
-                if (acc + sh.h1[b] >= gamma_fx) {
-                    sh.lo = l1_lo(b);
-                    sh.hi = l1_hi(b);
-                    sh.above = acc;
-                    sh.found = 1;
-                    break;
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t w = rule_weight(rule, xs[i]);
+                    hist_add_warp(sh.h1, static_cast<uint32_t>(l1_bin(xs[i])), w, p + i < F && w != 0u);
                 }
-                acc += sh.h1[b];
             }
         }
     }
     __syncthreads();
 
-    // 5. refine inside [lo, hi) until one bit pattern is left.  The pages of
-    //    the crossing bin are gathered first; when they fit in kCand (the
-    //    usual case: a level-1 bin spans 1/128 of an octave) one warp refines
-    //    them without block barriers, otherwise 256-bin passes run over all
-    //    pages.  Both use the same integer sums, so the cut is identical.
-    if (tid == 0) sh.ncand = 0;
-    __syncthreads();
-    if (sh.found) {
-        // ballots first, one slot reservation per warp, then the writes
-        const uint32_t lo = sh.lo, hi = sh.hi;
-        uint32_t xk[kSelStripes];
-        unsigned mk[kSelStripes];
-        int cntw = 0;
-#pragma unroll
-        for (int k = 0; k < kSelStripes; ++k) {
-            const int p = k * kSelThreads + tid;
-            xk[k] = p < F ? s_bits[p] : 0u;
-            mk[k] = __ballot_sync(0xffffffffu, p < F && xk[k] >= lo && xk[k] < hi);
-            cntw += __popc(mk[k]);
-        }
-        if (cntw) {                                          // warp-uniform
-            int base = 0;
-            if (lane == 0) base = atomicAdd(&sh.ncand, cntw);
-            base = __shfl_sync(0xffffffffu, base, 0);
-            const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-            for (int k = 0; k < kSelStripes; ++k) {
-                if ((mk[k] >> lane) & 1u) {
-                    const int slot = base + __popc(mk[k] & lt);
-                    if (slot < kCand) {
-                        sh.cand[slot] = xk[k];
-                        sh.cand_idx[slot] = static_cast<uint16_t>(k * kSelThreads + tid);
-                        if (slot < kPairMax) sh.cand_fx[slot] = to_fx(xk[k]);
+    if (rule != kRuleTopDelta) {             // block-uniform: top-delta needs no descent
+        // 4. level-1 cut: thread t owns bins (top_t - kL1PerThread, top_t] from the top
+        {
+            const int top = kL1Bins - 1 - tid * kL1PerThread;
+            unsigned long long mine = 0ull;
+    #pragma unroll
+            for (int i = 0; i < kL1PerThread; ++i)
+                if (top - i >= 0) mine += sh.h1[top - i];
+            unsigned long long total;
+            unsigned long long acc = sel_excl_scan(mine, sh.scan, &total);
+            if (acc < target && acc + mine >= target) {
+    #pragma unroll
+                for (int i = 0; i < kL1PerThread; ++i) {
+                    const int b = top - i;
+                    if (b < 0) break;
+                    if (acc + sh.h1[b] >= target) {
+                        sh.lo = l1_lo(b);
+                        sh.hi = l1_hi(b);
+                        sh.above = acc;
+                        sh.found = 1;
+                        break;
                     }
+                    acc += sh.h1[b];
                 }
-                base += __popc(mk[k]);
-            }
-        }
-    }
-    __syncthreads();
-    const bool use_pair = sh.found && sh.ncand <= kPairMax;
-    const bool use_cand = sh.found && !use_pair && sh.ncand <= kCand;
-    if (use_pair) {
-        // candidate c: masses ranked before it (larger, or equal with a lower
-        // page index); the candidate whose running sum crosses gamma is the
-        // cut.  2^lg threads (lanes of one warp) share a candidate's sums.
-        const int nc = sh.ncand;
-        const unsigned long long above0 = sh.above;
-        __syncthreads();                                 // every thread has read `above`
-        const int lg = nc <= 32 ? 5 : nc <= 64 ? 4 : nc <= 128 ? 3 : 2;
-        const int ci = tid >> lg, part = tid & ((1 << lg) - 1);
-        uint32_t gt_sum = 0u, tie_before = 0u;          // <= the total mass: fits 32 bits
-        uint32_t x = 0u, xi = 0u;
-        if (ci < nc) {
-            x = sh.cand[ci];
-            xi = sh.cand_idx[ci];
-#pragma unroll 4
-            for (int c = part; c < nc; c += 1 << lg) {
-                const uint32_t y = sh.cand[c];
-                const uint32_t fy = sh.cand_fx[c];
-                gt_sum += y > x ? fy : 0u;
-                tie_before += (y == x && sh.cand_idx[c] < xi) ? fy : 0u;
-            }
-        }
-        for (int o = 1; o < (1 << lg); o <<= 1) {
-            gt_sum += __shfl_xor_sync(0xffffffffu, gt_sum, o);
-            tie_before += __shfl_xor_sync(0xffffffffu, tie_before, o);
-        }
-        if (ci < nc && part == 0) {
-            const unsigned long long before = above0 + gt_sum + tie_before;
-            if (before < gamma_fx && before + sh.cand_fx[ci] >= gamma_fx) {   // exactly one candidate
-                sh.lo = x;
-                sh.hi = x + 1u;
-                sh.above = above0 + gt_sum;
             }
         }
         __syncthreads();
-    } else if (use_cand) {
-        if (warp == 0) {
+
+        // 5. refine inside [lo, hi) until one bit pattern is left.  The pages of
+        //    the crossing bin are gathered first; when they fit in kCand (the
+        //    usual case: a level-1 bin spans 1/128 of an octave) one warp refines
+        //    them without block barriers, otherwise 256-bin passes run over all
+        //    pages.  Both use the same integer sums, so the cut is identical.
+        if (tid == 0) sh.ncand = 0;
+        __syncthreads();
+        if (sh.found) {
+            // ballots first, one slot reservation per warp, then the writes
+            const uint32_t lo = sh.lo, hi = sh.hi;
+            uint32_t xk[kSelStripes];
+            unsigned mk[kSelStripes];
+            int cntw = 0;
+    #pragma unroll
+            for (int k = 0; k < kSelStripes; ++k) {
+                const int p = k * kSelThreads + tid;
+                xk[k] = p < F ? s_bits[p] : 0u;
+                mk[k] = __ballot_sync(0xffffffffu, p < F && xk[k] >= lo && xk[k] < hi);
+                cntw += __popc(mk[k]);
+            }
+            if (cntw) {                                          // warp-uniform
+                int base = 0;
+                if (lane == 0) base = atomicAdd(&sh.ncand, cntw);
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const unsigned lt = (1u << lane) - 1u;
+    #pragma unroll
+                for (int k = 0; k < kSelStripes; ++k) {
+                    if ((mk[k] >> lane) & 1u) {
+                        const int slot = base + __popc(mk[k] & lt);
+                        if (slot < kCand) {
+                            sh.cand[slot] = xk[k];
+                            sh.cand_idx[slot] = static_cast<uint16_t>(k * kSelThreads + tid);
+                            if (slot < kPairMax) sh.cand_fx[slot] = rule_weight(rule, xk[k]);
+                        }
+                    }
+                    base += __popc(mk[k]);
+                }
+            }
+        }
+        __syncthreads();
+        const bool use_pair = sh.found && sh.ncand <= kPairMax;
+        const bool use_cand = sh.found && !use_pair && sh.ncand <= kCand;
+        if (use_pair) {
+            // candidate c: masses ranked before it (larger, or equal with a lower
+            // page index); the candidate whose running sum crosses gamma is the
+            // cut.  2^lg threads (lanes of one warp) share a candidate's sums.
             const int nc = sh.ncand;
-            uint32_t lo = sh.lo, hi = sh.hi;
-            unsigned long long above = sh.above;
-            for (int pass = 0; hi - lo > 1u && pass < 6; ++pass) {
+            const unsigned long long above0 = sh.above;
+            __syncthreads();                                 // every thread has read `above`
+            const int lg = nc <= 32 ? 5 : nc <= 64 ? 4 : nc <= 128 ? 3 : 2;
+            const int ci = tid >> lg, part = tid & ((1 << lg) - 1);
+            uint32_t gt_sum = 0u, tie_before = 0u;          // <= the total mass: fits 32 bits
+            uint32_t x = 0u, xi = 0u;
+            if (ci < nc) {
+                x = sh.cand[ci];
+                xi = sh.cand_idx[ci];
+    #pragma unroll 4
+                for (int c = part; c < nc; c += 1 << lg) {
+                    const uint32_t y = sh.cand[c];
+                    const uint32_t fy = sh.cand_fx[c];
+                    gt_sum += y > x ? fy : 0u;
+                    tie_before += (y == x && sh.cand_idx[c] < xi) ? fy : 0u;
+                }
+            }
+            for (int o = 1; o < (1 << lg); o <<= 1) {
+                gt_sum += __shfl_xor_sync(0xffffffffu, gt_sum, o);
+                tie_before += __shfl_xor_sync(0xffffffffu, tie_before, o);
+            }
+            if (ci < nc && part == 0) {
+                const unsigned long long before = above0 + gt_sum + tie_before;
+                if (before < target && before + sh.cand_fx[ci] >= target) {   // exactly one candidate
+                    sh.lo = x;
+                    sh.hi = x + 1u;
+                    sh.above = above0 + gt_sum;
+                }
+            }
+            __syncthreads();
+        } else if (use_cand) {
+            if (warp == 0) {
+                const int nc = sh.ncand;
+                uint32_t lo = sh.lo, hi = sh.hi;
+                unsigned long long above = sh.above;
+                for (int pass = 0; hi - lo > 1u && pass < 6; ++pass) {
+                    const uint32_t width = hi - lo;
+                    const int nbits = 32 - __clz(width - 1u);
+                    const int shift = nbits > 8 ? nbits - 8 : 0;
+                    const int nb = static_cast<int>((width - 1u) >> shift) + 1;
+    #pragma unroll
+                    for (int i = 0; i < kL2Bins / 32; ++i) sh.h2[lane + 32 * i] = 0u;
+                    __syncwarp();
+                    for (int c = lane; c < nc; c += 32) {
+                        const uint32_t x = sh.cand[c];
+                        if (x >= lo && x < hi) atomicAdd(&sh.h2[(x - lo) >> shift], rule_weight(rule, x));
+                    }
+                    __syncwarp();
+                    const int top = nb - 1 - 8 * lane;
+                    unsigned long long mine = 0ull;
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (top - i >= 0) mine += sh.h2[top - i];
+                    unsigned long long xs = mine;
+    #pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned long long y = __shfl_up_sync(0xffffffffu, xs, o);
+                        if (lane >= o) xs += y;
+                    }
+                    unsigned long long acc = above + xs - mine;
+                    int fb = -1;
+                    unsigned long long fa = 0ull;
+                    if (acc < target && acc + mine >= target) {
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int b = top - i;
+                            if (b < 0) break;
+                            if (acc + sh.h2[b] >= target) {
+                                fb = b;
+                                fa = acc;
+                                break;
+                            }
+                            acc += sh.h2[b];
+                        }
+                    }
+                    const unsigned who = __ballot_sync(0xffffffffu, fb >= 0);
+                    if (!who) break;                             // cannot happen: exact integer sums
+                    const int src = __ffs(who) - 1;
+                    fb = __shfl_sync(0xffffffffu, fb, src);
+                    above = __shfl_sync(0xffffffffu, fa, src);
+                    const uint32_t nlo = lo + (static_cast<uint32_t>(fb) << shift);
+                    const uint32_t span = 1u << shift;
+                    hi = (hi - nlo < span) ? hi : nlo + span;
+                    lo = nlo;
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    sh.lo = lo;
+                    sh.hi = hi;
+                    sh.above = above;
+                    if (hi - lo > 1u) raise_status(status, kDevBadLen);
+                }
+            }
+            __syncthreads();
+        } else {
+            for (int pass = 0; sh.found && sh.hi - sh.lo > 1u; ++pass) {
+                if (pass >= 6) {                               // cannot happen: exact integer sums
+                    if (tid == 0) raise_status(status, kDevBadLen);
+                    break;
+                }
+                const uint32_t lo = sh.lo, hi = sh.hi;
                 const uint32_t width = hi - lo;
                 const int nbits = 32 - __clz(width - 1u);
                 const int shift = nbits > 8 ? nbits - 8 : 0;
                 const int nb = static_cast<int>((width - 1u) >> shift) + 1;
-#pragma unroll
-                for (int i = 0; i < kL2Bins / 32; ++i) sh.h2[lane + 32 * i] = 0u;
-                __syncwarp();
-                for (int c = lane; c < nc; c += 32) {
-                    const uint32_t x = sh.cand[c];
-                    if (x >= lo && x < hi) atomicAdd(&sh.h2[(x - lo) >> shift], to_fx(x));
+                if (tid < kL2Bins) sh.h2[tid] = 0u;
+                __syncthreads();
+    #pragma unroll
+                for (int k = 0; k < kSelStripes; ++k) {
+                    const int p = k * kSelThreads + tid;
+                    if (k * kSelThreads >= F) break;              // warp-uniform
+                    const uint32_t x = p < F ? s_bits[p] : 0u;
+                    hist_add_warp(sh.h2, (x - lo) >> shift, rule_weight(rule, x), p < F && x >= lo && x < hi);
                 }
-                __syncwarp();
-                const int top = nb - 1 - 8 * lane;
-                unsigned long long mine = 0ull;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (top - i >= 0) mine += sh.h2[top - i];
-                unsigned long long xs = mine;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long y = __shfl_up_sync(0xffffffffu, xs, o);
-                    if (lane >= o) xs += y;
-                }
-                unsigned long long acc = above + xs - mine;
-                int fb = -1;
-                unsigned long long fa = 0ull;
-                if (acc < gamma_fx && acc + mine >= gamma_fx) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int b = top - i;
-                        if (b < 0) break;
-                        if (acc + sh.h2[b] >= gamma_fx) {
-                            fb = b;
-                            fa = acc;
-                            break;
+                __syncthreads();
+                if (warp == 0) {
+                    const int top = nb - 1 - 8 * lane;
+                    unsigned long long mine = 0ull;
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (top - i >= 0) mine += sh.h2[top - i];
+                    unsigned long long x = mine;
+    #pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    unsigned long long acc = sh.above + x - mine;
+                    if (acc < target && acc + mine >= target) {
+    #pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int b = top - i;
+                            if (b < 0) break;
+                            if (acc + sh.h2[b] >= target) {
+                                const uint32_t nlo = lo + (static_cast<uint32_t>(b) << shift);
+                                const uint32_t span = 1u << shift;
+                                sh.lo = nlo;
+                                sh.hi = (hi - nlo < span) ? hi : nlo + span;
+                                sh.above = acc;
+                                break;
+                            }
+                            acc += sh.h2[b];
                         }
-                        acc += sh.h2[b];
                     }
                 }
-                const unsigned who = __ballot_sync(0xffffffffu, fb >= 0);
-                if (!who) break;                             // cannot happen: exact integer sums
-                const int src = __ffs(who) - 1;
-                fb = __shfl_sync(0xffffffffu, fb, src);
-                above = __shfl_sync(0xffffffffu, fa, src);
-                const uint32_t nlo = lo + (static_cast<uint32_t>(fb) << shift);
-                const uint32_t span = 1u << shift;
-                hi = (hi - nlo < span) ? hi : nlo + span;
-                lo = nlo;
-                __syncwarp();
+                __syncthreads();
             }
-            if (lane == 0) {
-                sh.lo = lo;
-                sh.hi = hi;
-                sh.above = above;
-                if (hi - lo > 1u) raise_status(status, kDevBadLen);
-            }
-        }
-        __syncthreads();
-    } else {
-        for (int pass = 0; sh.found && sh.hi - sh.lo > 1u; ++pass) {
-            if (pass >= 6) {                               // cannot happen: exact integer sums
-                if (tid == 0) raise_status(status, kDevBadLen);
-                break;
-            }
-            const uint32_t lo = sh.lo, hi = sh.hi;
-            const uint32_t width = hi - lo;
-            const int nbits = 32 - __clz(width - 1u);
-            const int shift = nbits > 8 ? nbits - 8 : 0;
-            const int nb = static_cast<int>((width - 1u) >> shift) + 1;
-            if (tid < kL2Bins) sh.h2[tid] = 0u;
-            __syncthreads();
-#pragma unroll
-            for (int k = 0; k < kSelStripes; ++k) {
-                const int p = k * kSelThreads + tid;
-                if (k * kSelThreads >= F) break;              // warp-uniform
-                const uint32_t x = p < F ? s_bits[p] : 0u;
-                hist_add_warp(sh.h2, (x - lo) >> shift, to_fx(x), p < F && x >= lo && x < hi);
-            }
-            __syncthreads();
-            if (warp == 0) {
-                const int top = nb - 1 - 8 * lane;
-                unsigned long long mine = 0ull;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (top - i >= 0) mine += sh.h2[top - i];
-                unsigned long long x = mine;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += y;
-                }
-                unsigned long long acc = sh.above + x - mine;
-                if (acc < gamma_fx && acc + mine >= gamma_fx) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int b = top - i;
-                        if (b < 0) break;
-                        if (acc + sh.h2[b] >= gamma_fx) {
-                            const uint32_t nlo = lo + (static_cast<uint32_t>(b) << shift);
-                            const uint32_t span = 1u << shift;
-                            sh.lo = nlo;
-                            sh.hi = (hi - nlo < span) ? hi : nlo + span;
-                            sh.above = acc;
-                            break;
-                        }
-                        acc += sh.h2[b];
-                    }
-                }
-            }
-            __syncthreads();
         }
     }
 
     // 6. cut value and how many pages tied at it are needed
     // (32-bit: gamma - above <= 2^31 and the cut's fixed-point mass < 2^32)
     uint32_t cut, need_tied;
-    if (sh.found) {
+    if (rule == kRuleTopDelta) {              // keep mass >= delta * max: every page at or above
+        const float thr = fmaxf(delta * __uint_as_float(sh.xmax), 0.f);
+        cut = __float_as_uint(thr);
+        need_tied = 0xFFFFFFFFu;
+    } else if (sh.found) {
         cut = sh.lo;
-        const uint32_t cfx = to_fx(cut);                          // > 0: it carried the crossing
-        const uint32_t d = static_cast<uint32_t>(gamma_fx - sh.above);
+        const uint32_t cfx = rule_weight(rule, cut);               // > 0: it carried the crossing
+        const uint32_t d = static_cast<uint32_t>(target - sh.above);
         need_tied = d / cfx + (d % cfx != 0u ? 1u : 0u);
     } else {                                                      // total < gamma: keep all
         cut = 0u;
@@ -723,8 +755,9 @@ cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_ta
 
 cudaError_t launch_select(const float *weights, const float *chunks, const int32_t *page_table,
                           const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
-                          long long num_pages, unsigned long long gamma_fx, bool dense,
-                          int32_t *lists, int32_t *lengths, uint32_t *status, cudaStream_t stream)
+                          long long num_pages, int rule, unsigned long long target, float delta,
+                          bool dense, int32_t *lists, int32_t *lengths, uint32_t *status,
+                          cudaStream_t stream)
 {
     const int ldc = chunks_ld(max_pages);
     const size_t smem = dense ? 0 : select_smem_bytes(max_pages, ldc);
@@ -735,7 +768,7 @@ cudaError_t launch_select(const float *weights, const float *chunks, const int32
     }
     return launch_pdl(k_select, dim3(batch * hkv), dim3(kSelThreads), smem, stream, weights, chunks,
                       page_table, seq_lens, hq, hkv, max_pages, weights_ld(max_pages), ldc,
-                      num_pages, gamma_fx, dense ? 1 : 0, lists, lengths, status);
+                      num_pages, rule, target, delta, dense ? 1 : 0, lists, lengths, status);
 }
 
 }  // namespace moira

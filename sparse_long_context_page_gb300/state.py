@@ -53,6 +53,13 @@ class DecodeState:
                   self.sm_scale, lists, lengths, self.ws)
         return lists, lengths
 
+    def select_layer_rule(self, l: int, rule: int, param: float, lists=None, lengths=None):
+        lists = self.lists if lists is None else lists
+        lengths = self.lengths[l] if lengths is None else lengths
+        mb.select_rule(self.shape, self.w.q[l], self.summ[l], self.page_table, self.seq_lens, rule,
+                       param, self.sm_scale, lists, lengths, self.ws)
+        return lists, lengths
+
     def attend_layer(self, l: int, lists, lengths, out=None):
         out = self.out[l] if out is None else out
         mb.attend(self.shape, self.w.q[l], self.w.k_pool[l], self.w.v_pool[l], lists, lengths,

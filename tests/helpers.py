@@ -123,3 +123,45 @@ def out_errors(got: np.ndarray, ref: np.ndarray):
     den = np.linalg.norm(ref, axis=1)
     rel = np.where(den > 0, num / np.maximum(den, 1e-300), num)
     return max_abs, float(rel.max()) if rel.size else 0.0
+
+
+# Width of the fp32-vs-fp64 band for the alternative rules: a page may be
+# decided differently only when its oracle mass is within RULE_BAND
+# (relative) of the rule's boundary mass (the k-th largest mass, or delta *
+# the largest mass), or when both are below RULE_FLOOR: fp32 masses of that
+# size underflow in the chunk-relative products, so their order is not kept
+# (a fixed budget larger than the pages that carry any mass ends among them).
+RULE_BAND = 1e-5
+RULE_FLOOR = 1e-30
+
+
+def check_rule_list(ud: UnitData, gpu_phys: np.ndarray, rule: int, param: float) -> str | None:
+    """None if the CUDA list under top-k / top-delta is acceptable against the
+    oracle rule applied to the oracle masses, else a reason."""
+    lg = ud.to_logical(gpu_phys)
+    if np.any(lg < 0):
+        return f"unknown physical page ids {gpu_phys[lg < 0][:5]}"
+    if len(lg) > 1 and np.any(np.diff(lg) <= 0):
+        return "list not in ascending logical order"
+    tail = ud.L % 16 != 0
+    if tail and (len(lg) == 0 or lg[-1] != ud.F):
+        return "partial tail page missing or not last"
+    if ud.F == 0:
+        return None if len(lg) == int(tail) else "pages listed for an empty context"
+    _, mass, order, _ = ud.select(0.5)
+    full_g = set(int(x) for x in lg if x < ud.F)
+    if rule == oracle.RULE_TOPK:
+        keep = oracle.topk(mass, int(param))
+        k = min(int(param), ud.F)
+        if len(full_g) != k:
+            return f"top-k kept {len(full_g)} full pages, want {k}"
+        edge = mass[order[k - 1]] if k > 0 else 0.0
+    else:
+        keep = oracle.topdelta(mass, param)
+        edge = param * mass.max()
+    full_o = set(int(x) for x in np.flatnonzero(keep))
+    bad = [p for p in full_g ^ full_o
+           if abs(mass[p] - edge) > RULE_BAND * edge and max(mass[p], edge) > RULE_FLOOR]
+    if bad:
+        return f"{len(bad)} pages decided differently away from the boundary, e.g. {bad[:3]}"
+    return None

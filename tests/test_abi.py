@@ -62,6 +62,25 @@ def test_select_rejects_bad_arguments_on_host():
     assert _select(lib, moira.Shape.of(32, 8, 1 << 25)) == 4  # TMA rows beyond 2^31
 
 
+def test_select_rule_rejects_bad_rules_and_params_on_host():
+    lib = moira.load_library()
+    ok = moira.Shape.of(32, 8, 1024)
+
+    def call(rule, param, sm=0.088):
+        return lib.moira_select_rule(ctypes.byref(ok), FAKE, FAKE, FAKE, FAKE, 2, 64, rule, param, sm,
+                                     FAKE, FAKE, FAKE, 1 << 30, None)
+
+    for rule, param in [(3, 0.5), (-1, 0.5),                               # unknown rule
+                        (mb.RULE_COVERAGE, 0.0), (mb.RULE_COVERAGE, 1.5),
+                        (mb.RULE_COVERAGE, float("nan")),
+                        (mb.RULE_TOPK, -1.0), (mb.RULE_TOPK, 2.5),           # not a whole count
+                        (mb.RULE_TOPK, float(1 << 25)), (mb.RULE_TOPK, float("inf")),
+                        (mb.RULE_TOPDELTA, 0.0), (mb.RULE_TOPDELTA, 1.01),
+                        (mb.RULE_TOPDELTA, float("nan"))]:
+        assert call(rule, param) == 1, (rule, param)
+    assert call(mb.RULE_TOPK, 3.0, sm=0.0) == 1
+
+
 def test_attend_and_step_reject_bad_arguments_on_host():
     lib = moira.load_library()
     ok = moira.Shape.of(32, 8, 1024)

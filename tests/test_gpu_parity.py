@@ -300,3 +300,58 @@ def test_select_all_masses_tied(F):
             logical = ud.to_logical(lh[0, j, :nh[0, j]])
             if abs(g * F - round(g * F)) > 1e-3:           # away from an integer: exact
                 assert list(logical) == list(range(k)) + [F], f"F={F} gamma={g}: {len(logical)} vs {k}+1"
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", {}),
+    ("llama8b_32k", dict(layers=1)),
+    ("serving_ragged", dict(batch=3, layers=1)),
+    ("stress_regimes", dict(batch=4, context=(16 * 2000 + 9,))),
+])
+def test_select_rules_topk_and_topdelta(name, over):
+    """Fixed-budget and relative-threshold rules through the same kernels:
+    lists against the oracle rules on the oracle masses, and attention over
+    the GPU's own lists against the oracle's attention."""
+    w, st = _state(name, seed=29, **over)
+    G = w.group
+    cases = [(mb.RULE_TOPK, 0), (mb.RULE_TOPK, 1), (mb.RULE_TOPK, 37), (mb.RULE_TOPK, 600),
+             (mb.RULE_TOPK, 1 << 20), (mb.RULE_TOPDELTA, 1.0), (mb.RULE_TOPDELTA, 0.3),
+             (mb.RULE_TOPDELTA, 1e-3)]
+    units = [(r, j) for r in range(w.spec.batch) for j in range(w.spec.kv_heads)]
+    uds = {u: H.UnitData(w, 0, u[0], u[1]) for u in units}
+    for rule, param in cases:
+        lists = torch.full_like(st.lists, -7)
+        lengths = torch.zeros((w.spec.batch, w.spec.kv_heads), dtype=torch.int32, device="cuda")
+        st.select_layer_rule(0, rule, float(param), lists, lengths)
+        out = torch.zeros_like(st.out[0])
+        st.attend_layer(0, lists, lengths, out)
+        torch.cuda.synchronize()
+        assert st.device_status() == 0, (name, rule, param)
+        lh, nh, oh = lists.cpu().numpy(), lengths.cpu().numpy(), out.cpu().numpy()
+        for (r, j) in units:
+            ud = uds[(r, j)]
+            gl = lh[r, j, :nh[r, j]]
+            why = H.check_rule_list(ud, gl, rule, float(param))
+            assert why is None, f"{name} rule {rule} param {param} req {r} kv {j}: {why}"
+            lg = ud.to_logical(gl)
+            if len(lg):
+                ma, rl = H.out_errors(oh[r, j * G:(j + 1) * G], ud.attend(lg))
+                assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"{name} {rule}/{param} r{r} j{j}: {ma:.3g} {rl:.3g}"
+    del st, w
+    torch.cuda.empty_cache()
+
+
+def test_select_rule_coverage_is_select_bit_for_bit():
+    w, st = _state("serving_ragged", seed=31, batch=3, layers=1)
+    for g in (0.5, 0.9, 0.99):
+        g = float(np.float32(g))
+        a_l, a_n = torch.full_like(st.lists, -7), torch.zeros_like(st.lengths[0])
+        b_l, b_n = torch.full_like(st.lists, -7), torch.zeros_like(st.lengths[0])
+        st.select_layer(0, g, a_l, a_n)
+        st.select_layer_rule(0, mb.RULE_COVERAGE, g, b_l, b_n)
+        torch.cuda.synchronize()
+        assert torch.equal(a_n, b_n)
+        for r in range(w.spec.batch):
+            for j in range(w.spec.kv_heads):
+                n = int(a_n[r, j])
+                assert torch.equal(a_l[r, j, :n], b_l[r, j, :n])
