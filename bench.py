@@ -280,6 +280,72 @@ def time_parts(st, gamma, steps, warmup):
     return out[0], out[1]
 
 
+def capture_fn(fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        fn()                                             # eager warm-up outside capture
+        with torch.cuda.graph(g, stream=s):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+def compare_rules(st, w, head, results, args):
+    """Coverage (gamma = head) against top-k and top-delta at equal pages read.
+    k is the coverage rule's mean full pages per unit; delta is bisected (in
+    log space) until the total pages match within 0.5%.  Each rule's step is
+    captured and timed like the headline step; its output is compared with
+    the dense (gamma = 1) step's: relative L2 per (layer, request, query head)."""
+    import sparse_long_context_page_gb300 as moira
+    sp = w.spec
+    st.step(1.0)
+    torch.cuda.synchronize()
+    dense_out = st.out.clone()
+    full = (st.seq_lens // 16).to(torch.float64)                         # full pages per request
+    tails = int((st.seq_lens % 16 != 0).sum()) * sp.kv_heads * sp.layers
+
+    def pages_of(rule, param):
+        for l in range(sp.layers):
+            st.select_layer_rule(l, rule, param, st.lists, st.lengths[l])
+        torch.cuda.synchronize()
+        return int(st.lengths.sum())
+
+    target = pages_of(moira.RULE_COVERAGE, head)
+    units = sp.layers * sp.batch * sp.kv_heads
+    k = int(round((target - tails) / units))
+    lo, hi = 1e-12, 1.0
+    delta = 1e-3
+    for _ in range(40):                                   # pages fall as delta grows
+        delta = math.sqrt(lo * hi)
+        n = pages_of(moira.RULE_TOPDELTA, delta)
+        if abs(n - target) <= 0.005 * target:
+            break
+        if n > target:
+            lo = delta
+        else:
+            hi = delta
+    out = {}
+    for name, rule, param in (("coverage", moira.RULE_COVERAGE, head), ("topk", moira.RULE_TOPK, float(k)),
+                              ("topdelta", moira.RULE_TOPDELTA, delta)):
+        g = capture_fn(lambda: st.step_rule(rule, param))
+        ms, _ = time_graph(g, max(3, args.steps // 2), args.warmup, 1)
+        g.replay()
+        torch.cuda.synchronize()
+        pages = int(st.lengths.sum())
+        err = (st.out - dense_out).norm(dim=-1) / dense_out.norm(dim=-1).clamp_min(1e-30)
+        err = err.flatten().double().cpu().numpy()
+        out[name] = {"param": round(float(param), 8), "pages_read": pages,
+                     "pages_fraction": round(pages / float(full.sum() * sp.kv_heads * sp.layers + tails), 4),
+                     "us_per_step": round(ms * 1e3, 2),
+                     "out_rel_l2_vs_dense": {"mean": float(np.mean(err)), "p99": float(np.percentile(err, 99)),
+                                             "max": float(np.max(err))}}
+        del g
+    return out
+
+
 def run_ours(args):
     import sparse_long_context_page_gb300 as moira
     from sparse_long_context_page_gb300 import workloads as W
@@ -328,6 +394,11 @@ def run_ours(args):
     traffic = None
     if ATTEND_TRAFFIC["dram_bytes_per_entry"] and ATTEND_TRAFFIC["sources_sha256"] == digest:
         traffic = int(round(ATTEND_TRAFFIC["dram_bytes_per_entry"] * entries))
+
+    # the same step under the fixed-budget and relative-threshold rules, tuned
+    # to read the same pages as coverage at the headline gamma; quality is the
+    # attention output against the dense step's
+    rules = compare_rules(st, w, head, results, args) if not args.no_rules else None
 
     # end to end: host q in, host out back, through moira_decode_step_host
     q_host = w.q.cpu().pin_memory()
@@ -409,6 +480,7 @@ def run_ours(args):
         "gpu_launches": args.steps * launches_per_step,
         "clocks": hd["clocks"],
         "cpu_baseline": cpu,
+        "rules_at_equal_pages": rules,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -466,6 +538,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-layers", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rules", action="store_true",
+                    help="skip the top-k / top-delta comparison at equal pages")
     ap.add_argument("--layers", type=int, default=0,
                     help="fewer layers than the workload's (small profiling cases only)")
     args = ap.parse_args()

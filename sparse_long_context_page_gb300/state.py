@@ -46,6 +46,13 @@ class DecodeState:
                        self.page_table, self.seq_lens, gamma, self.sm_scale, self.lists,
                        self.lengths, self.out, self.ws)
 
+    def step_rule(self, rule: int, param: float):
+        """One decode-attention step under a page rule: per layer moira_select_rule
+        then moira_attend, in order on the current stream."""
+        for l in range(self.layers):
+            self.select_layer_rule(l, rule, param, self.lists, self.lengths[l])
+            self.attend_layer(l, self.lists, self.lengths[l], self.out[l])
+
     def select_layer(self, l: int, gamma: float, lists=None, lengths=None):
         lists = self.lists if lists is None else lists
         lengths = self.lengths[l] if lengths is None else lengths
