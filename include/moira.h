@@ -114,6 +114,30 @@ moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream
 moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool, void *summ,
                                     const int32_t *phys_pages, int32_t n, moira_stream_t stream);
 
+/* Append one token per request to one layer's paged KV cache and keep the
+ * page summaries current: the north star's "moira_update_summaries when a page
+ * fills", fused with the append a serving loop does every step (the pages
+ * leave the append itself to the serving system).  Request r's new token is
+ * token seq_lens[r] - 1, i.e. seq_lens counts it, as moira_select and
+ * moira_attend expect afterwards.  Its key and value go to slot
+ * (seq_lens[r]-1) % S of logical page (seq_lens[r]-1) / S; when that is the
+ * page's last slot, summ[page][j] is recomputed exactly as
+ * moira_update_summaries would.
+ *   k_new, v_new : bf16 [batch][Hkv][d]        the new token's keys / values
+ *   k_pool, v_pool : bf16 [P][Hkv][S][d]       one layer's pools (written)
+ *   summ       : bf16 [P][Hkv][d]              that layer's summaries (written
+ *                                              for pages that fill)
+ *   page_table : int32 [batch][max_pages]      logical -> physical page
+ *   seq_lens   : int32 [batch]                 tokens after the append; 0
+ *                                              appends nothing for that request
+ * A length beyond max_pages * S or a page id outside [0, P) skips that
+ * request (no workspace, so nothing is recorded).  All buffers device,
+ * 16-byte aligned. */
+moira_status moira_append_kv(const moira_shape *shape, const void *k_new, const void *v_new,
+                             void *k_pool, void *v_pool, void *summ, const int32_t *page_table,
+                             const int32_t *seq_lens, int32_t batch, int32_t max_pages,
+                             moira_stream_t stream);
+
 /* The coverage rule ("MOIRA" abstract: "a coverage rule keeps the smallest
  * set of pages whose estimated attention mass reaches a fraction gamma"),
  * for every (request, KV head) of one layer.

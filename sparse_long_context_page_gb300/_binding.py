@@ -31,7 +31,7 @@ MAX_PAGES_PER_SEQ, MAX_UNITS = 8192, 4096
 EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summaries",
            "moira_select", "moira_attend", "moira_decode_step", "moira_decode_step_host",
            "moira_read_device_status", "moira_attend_grid_blocks", "moira_status_string",
-           "moira_select_noalloc", "moira_select_rule")
+           "moira_select_noalloc", "moira_select_rule", "moira_append_kv")
 
 # page rules of moira_select_rule (moira_rule in include/moira.h)
 RULE_COVERAGE, RULE_TOPK, RULE_TOPDELTA = 0, 1, 2
@@ -75,6 +75,8 @@ def load_library(build_if_missing: bool = True):
     lib.moira_workspace_init.argtypes = [_vp, ctypes.c_size_t, _vp]
     lib.moira_workspace_init.restype = ctypes.c_int
     lib.moira_update_summaries.argtypes = [sp, _vp, _vp, _vp, _i32, _vp]
+    lib.moira_append_kv.argtypes = [sp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp]
+    lib.moira_append_kv.restype = ctypes.c_int
     lib.moira_update_summaries.restype = ctypes.c_int
     lib.moira_select.argtypes = [sp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, ctypes.c_float,
                                  _vp, _vp, _vp, ctypes.c_size_t, _vp]
@@ -163,6 +165,19 @@ def update_summaries(shape: Shape, k_pool: torch.Tensor, summ: torch.Tensor,
                                       _dev(phys_pages, "phys_pages", torch.int32, 1),
                                       phys_pages.numel(), _stream(stream)),
            "moira_update_summaries")
+
+
+def append_kv(shape: Shape, k_new, v_new, k_pool, v_pool, summ, page_table, seq_lens, stream=None):
+    """Write each request's new token (token seq_lens[r]-1) into its page and
+    recompute the summary of every page that this fills."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    _check(lib.moira_append_kv(ctypes.byref(shape), _dev(k_new, "k_new", torch.bfloat16),
+                               _dev(v_new, "v_new", torch.bfloat16), _dev(k_pool, "k_pool", torch.bfloat16),
+                               _dev(v_pool, "v_pool", torch.bfloat16), _dev(summ, "summ", torch.bfloat16),
+                               _dev(page_table, "page_table", torch.int32, 2),
+                               _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                               _stream(stream)), "moira_append_kv")
 
 
 def select(shape: Shape, q, summ, page_table, seq_lens, gamma: float, sm_scale: float, lists,

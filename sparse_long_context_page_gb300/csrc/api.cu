@@ -210,6 +210,24 @@ moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
+moira_status moira_append_kv(const moira_shape *shape, const void *k_new, const void *v_new,
+                             void *k_pool, void *v_pool, void *summ, const int32_t *page_table,
+                             const int32_t *seq_lens, int32_t batch, int32_t max_pages,
+                             moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (!k_new || !v_new || !k_pool || !v_pool || !summ || !page_table || !seq_lens)
+        return MOIRA_EINVAL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(summ))
+        return MOIRA_EINVAL;
+    return cuda_status(launch_append(k_new, v_new, k_pool, v_pool, summ, page_table, seq_lens,
+                                     batch, shape->num_kv_heads, max_pages,
+                                     shape->num_phys_pages, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moira_status moira_select(const moira_shape *shape, const void *q, const void *summ,
                           const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
                           int32_t max_pages, float gamma, float sm_scale, int32_t *lists,

@@ -10,6 +10,11 @@ namespace moira {
 cudaError_t launch_summarize(const void *k_pool, void *summ, const int32_t *phys_pages, int n,
                              int hkv, long long num_pages, uint32_t *status, cudaStream_t stream);
 
+cudaError_t launch_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool,
+                          void *summ, const int32_t *page_table, const int32_t *seq_lens,
+                          int batch, int hkv, int max_pages, long long num_pages,
+                          cudaStream_t stream);
+
 cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_table,
                          const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
                          long long num_pages, float scale_log2, float *scores, float *chunks,

@@ -64,6 +64,60 @@ __global__ void __launch_bounds__(64) k_summarize(const uint32_t *__restrict__ k
     summ[blk * (kHeadDim / 2) + threadIdx.x] = blo | (bhi << 16);
 }
 
+// Append one token per request to a paged pool (one block per (request, KV
+// head); 64 threads, two dimensions each).  The token of request r is token
+// seq_lens[r] - 1: slot (L-1) % S of logical page (L-1) / S.  When that slot
+// is the page's last, the page has just filled and its summary is computed
+// here: the 15 earlier keys are read back from the pool, the new one is
+// still in registers, and the mean is formed and rounded as in k_summarize.
+__global__ void __launch_bounds__(64) k_append(const uint32_t *__restrict__ k_new,
+                                               const uint32_t *__restrict__ v_new,
+                                               uint32_t *__restrict__ k_pool, uint32_t *__restrict__ v_pool,
+                                               uint32_t *__restrict__ summ,
+                                               const int32_t *__restrict__ page_table,
+                                               const int32_t *__restrict__ seq_lens, int hkv,
+                                               int max_pages, long long num_pages)
+{
+    const int r = blockIdx.x / hkv, j = blockIdx.x % hkv;
+    const int L = seq_lens[r];
+    if (L <= 0 || L > max_pages * kPageSize) return;       // nothing to append / out of range
+    const int pos = L - 1, lp = pos / kPageSize, slot = pos % kPageSize;
+    const int p = page_table[static_cast<size_t>(r) * max_pages + lp];
+    if (p < 0 || p >= num_pages) return;
+    const size_t blk = static_cast<size_t>(p) * hkv + j;
+    const size_t src = (static_cast<size_t>(r) * hkv + j) * (kHeadDim / 2) + threadIdx.x;
+    const uint32_t kn = k_new[src], vn = v_new[src];
+    uint32_t *kb = k_pool + blk * (kPageSize * kHeadDim / 2) + threadIdx.x;
+    kb[slot * (kHeadDim / 2)] = kn;
+    v_pool[blk * (kPageSize * kHeadDim / 2) + slot * (kHeadDim / 2) + threadIdx.x] = vn;
+    if (slot == kPageSize - 1) {
+        double lo = 0.0, hi = 0.0;
+#pragma unroll
+        for (int t = 0; t < kPageSize - 1; ++t) {
+            const uint32_t v = kb[t * (kHeadDim / 2)];
+            lo += static_cast<double>(bf16_lo(v));
+            hi += static_cast<double>(bf16_hi(v));
+        }
+        lo += static_cast<double>(bf16_lo(kn));
+        hi += static_cast<double>(bf16_hi(kn));
+        const uint32_t blo = f64_to_bf16_rne(lo * (1.0 / kPageSize));
+        const uint32_t bhi = f64_to_bf16_rne(hi * (1.0 / kPageSize));
+        summ[blk * (kHeadDim / 2) + threadIdx.x] = blo | (bhi << 16);
+    }
+}
+
+cudaError_t launch_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool,
+                          void *summ, const int32_t *page_table, const int32_t *seq_lens,
+                          int batch, int hkv, int max_pages, long long num_pages,
+                          cudaStream_t stream)
+{
+    k_append<<<static_cast<unsigned>(batch) * hkv, 64, 0, stream>>>(
+        static_cast<const uint32_t *>(k_new), static_cast<const uint32_t *>(v_new),
+        static_cast<uint32_t *>(k_pool), static_cast<uint32_t *>(v_pool),
+        static_cast<uint32_t *>(summ), page_table, seq_lens, hkv, max_pages, num_pages);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_summarize(const void *k_pool, void *summ, const int32_t *phys_pages, int n,
                              int hkv, long long num_pages, uint32_t *status, cudaStream_t stream)
 {

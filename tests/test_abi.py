@@ -81,6 +81,20 @@ def test_select_rule_rejects_bad_rules_and_params_on_host():
     assert call(mb.RULE_TOPK, 3.0, sm=0.0) == 1
 
 
+def test_append_kv_rejects_bad_arguments_on_host():
+    lib = moira.load_library()
+    ok = moira.Shape.of(32, 8, 1024)
+
+    def call(shape=ok, k=FAKE, v=FAKE, kp=FAKE, vp=FAKE, summ=FAKE, pt=FAKE, sl=FAKE, batch=2, max_pages=64):
+        return lib.moira_append_kv(ctypes.byref(shape), k, v, kp, vp, summ, pt, sl, batch, max_pages, None)
+
+    assert call(k=0) == 1 and call(summ=0) == 1 and call(sl=0) == 1     # null pointers
+    assert call(kp=FAKE + 4) == 1                                       # misaligned
+    assert call(batch=0) == 1
+    assert call(max_pages=mb.MAX_PAGES_PER_SEQ + 1) == 4
+    assert call(shape=moira.Shape.of(32, 8, 1024, head_dim=64)) == 4
+
+
 def test_attend_and_step_reject_bad_arguments_on_host():
     lib = moira.load_library()
     ok = moira.Shape.of(32, 8, 1024)
