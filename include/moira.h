@@ -260,6 +260,15 @@ moira_status moira_select_noalloc(const moira_shape *shape, const void *q, const
                                   int32_t batch, int32_t max_pages, float gamma, float sm_scale,
                                   int32_t *lists, int32_t *lengths, moira_stream_t stream);
 
+/* Diagnostic of the device-side failure path: launches one block that waits,
+ * exactly as the kernels' mbarrier waits do, on a barrier nothing will ever
+ * complete, gives up after `limit_ns` nanoseconds (1 .. 10^10) and ORs
+ * MOIRA_DEV_TIMEOUT into the workspace status word.  Lets a caller check that
+ * a wait that runs out is reported through moira_read_device_status and
+ * leaves the context usable.  No paper counterpart. */
+moira_status moira_diag_wait_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns,
+                                     moira_stream_t stream);
+
 /* Synchronise `stream`, copy the device status word (MOIRA_DEV_* bits) to
  * *status_out (HOST pointer) and clear it when `clear` is non-zero.  A host
  * call: never issue it while `stream` is being captured. */

@@ -31,7 +31,8 @@ MAX_PAGES_PER_SEQ, MAX_UNITS = 8192, 4096
 EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summaries",
            "moira_select", "moira_attend", "moira_decode_step", "moira_decode_step_host",
            "moira_read_device_status", "moira_attend_grid_blocks", "moira_status_string",
-           "moira_select_noalloc", "moira_select_rule", "moira_append_kv")
+           "moira_select_noalloc", "moira_select_rule", "moira_append_kv",
+           "moira_diag_wait_timeout")
 
 # page rules of moira_select_rule (moira_rule in include/moira.h)
 RULE_COVERAGE, RULE_TOPK, RULE_TOPDELTA = 0, 1, 2
@@ -96,6 +97,8 @@ def load_library(build_if_missing: bool = True):
                                            ctypes.c_size_t, _vp]
     lib.moira_decode_step_host.restype = ctypes.c_int
     lib.moira_read_device_status.argtypes = [_vp, ctypes.c_size_t, _u32p, _i32, _vp]
+    lib.moira_diag_wait_timeout.argtypes = [_vp, ctypes.c_size_t, ctypes.c_uint64, _vp]
+    lib.moira_diag_wait_timeout.restype = ctypes.c_int
     lib.moira_read_device_status.restype = ctypes.c_int
     lib.moira_attend_grid_blocks.argtypes = []
     lib.moira_attend_grid_blocks.restype = _i32
@@ -278,6 +281,14 @@ def read_device_status(ws, clear: bool = True, stream=None) -> int:
                                         ctypes.byref(out), 1 if clear else 0, _stream(stream)),
            "moira_read_device_status")
     return int(out.value)
+
+
+def diag_wait_timeout(ws, limit_ns: int, stream=None):
+    """Launch the bounded-wait diagnostic: a wait that runs out after
+    ``limit_ns`` and sets DEV_TIMEOUT in the workspace status word."""
+    lib = load_library()
+    _check(lib.moira_diag_wait_timeout(_dev(ws, "workspace", torch.uint8), ws.numel(), int(limit_ns),
+                                       _stream(stream)), "moira_diag_wait_timeout")
 
 
 def attend_grid_blocks() -> int:

@@ -379,6 +379,14 @@ moira_status moira_read_device_status(void *workspace, size_t ws_bytes, uint32_t
 
 int32_t moira_attend_grid_blocks(void) { return attend_blocks(); }
 
+moira_status moira_diag_wait_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns,
+                                     moira_stream_t stream)
+{
+    if (!workspace || ws_bytes < 256 || limit_ns < 1 || limit_ns > 10000000000ull) return MOIRA_EINVAL;
+    return cuda_status(launch_wait_timeout(static_cast<uint32_t *>(workspace), limit_ns,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 const char *moira_status_string(moira_status status)
 {
     switch (status) {

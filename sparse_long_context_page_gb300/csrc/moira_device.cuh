@@ -131,10 +131,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete, giving up after kWaitLimitNs.
-// Returns false on timeout (the caller records MOIRA_DEV_TIMEOUT and goes on,
-// so the control flow of the block never changes and nothing hangs).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Wait for the phase of `parity` to complete, giving up after `limit_ns`
+// (kWaitLimitNs in the kernels).  Returns false on timeout (the caller
+// records MOIRA_DEV_TIMEOUT and goes on, so the control flow of the block
+// never changes and nothing hangs).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
@@ -142,7 +144,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity)
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
 }
 

@@ -51,6 +51,9 @@ cudaError_t launch_attend(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
 
 int attend_blocks_per_sm();
 
+// Diagnostic: a bounded wait on an mbarrier nothing arrives at (see diag.cu).
+cudaError_t launch_wait_timeout(uint32_t *status, unsigned long long limit_ns, cudaStream_t stream);
+
 // Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
 template <typename... Params, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,

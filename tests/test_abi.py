@@ -95,6 +95,14 @@ def test_append_kv_rejects_bad_arguments_on_host():
     assert call(shape=moira.Shape.of(32, 8, 1024, head_dim=64)) == 4
 
 
+def test_diag_wait_timeout_rejects_bad_arguments_on_host():
+    lib = moira.load_library()
+    assert lib.moira_diag_wait_timeout(None, 1 << 20, 1000, None) == 1
+    assert lib.moira_diag_wait_timeout(FAKE, 16, 1000, None) == 1        # smaller than the status block
+    assert lib.moira_diag_wait_timeout(FAKE, 1 << 20, 0, None) == 1
+    assert lib.moira_diag_wait_timeout(FAKE, 1 << 20, 10 ** 10 + 1, None) == 1
+
+
 def test_attend_and_step_reject_bad_arguments_on_host():
     lib = moira.load_library()
     ok = moira.Shape.of(32, 8, 1024)

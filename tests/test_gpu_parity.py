@@ -355,3 +355,20 @@ def test_select_rule_coverage_is_select_bit_for_bit():
             for j in range(w.spec.kv_heads):
                 n = int(a_n[r, j])
                 assert torch.equal(a_l[r, j, :n], b_l[r, j, :n])
+
+
+def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable():
+    """The bounded device wait, made to run out on purpose (an mbarrier that
+    nothing completes, 50 ms limit): MOIRA_DEV_TIMEOUT reaches the host through
+    the status word, and the same workspace then serves a normal step."""
+    import time
+    w, st = _state("tiny", seed=0)
+    assert st.device_status() == 0
+    t0 = time.perf_counter()
+    mb.diag_wait_timeout(st.ws, 50_000_000)
+    status = mb.read_device_status(st.ws)                 # synchronises, clears
+    took = time.perf_counter() - t0
+    assert status & mb.DEV_TIMEOUT, hex(status)
+    assert 0.04 < took < 5.0, took
+    _check_layer(w, st, 0, float(np.float32(0.9)))        # select + attend still correct
+    assert st.device_status() == 0
