@@ -576,8 +576,8 @@ static cudaError_t launch_attend_ns(const CUtensorMap &tmap_k, const CUtensorMap
                                     const AttendArgs &args, int blocks, cudaStream_t stream)
 {
     const size_t smem = attend_smem_bytes<NS>(args.units);
-    cudaError_t e = cudaFuncSetAttribute(k_attend<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static std::atomic<int> seen[64];
+    cudaError_t e = raise_smem_limit(k_attend<NS>, smem, seen);
     if (e != cudaSuccess) return e;
     return launch_pdl(k_attend<NS>, dim3(blocks), dim3(kAttThreads), smem, stream, tmap_k, tmap_v,
                       args);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace moira {
 
 cudaError_t launch_summarize(const void *k_pool, void *summ, const int32_t *phys_pages, int n,
@@ -53,6 +55,24 @@ int attend_blocks_per_sm();
 
 // Diagnostic: a bounded wait on an mbarrier nothing arrives at (see diag.cu).
 cudaError_t launch_wait_timeout(uint32_t *status, unsigned long long limit_ns, cudaStream_t stream);
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute stays set in the device's context, so it is
+// set once per (kernel, device, larger size) instead of on every launch; the
+// caller keeps the per-device record (`seen`, 64 devices).
+template <typename Kernel>
+cudaError_t raise_smem_limit(Kernel kernel, size_t bytes, std::atomic<int> *seen)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(bytes));
+    if (seen[dev].load(std::memory_order_relaxed) >= static_cast<int>(bytes)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(bytes));
+    if (e == cudaSuccess) seen[dev].store(static_cast<int>(bytes), std::memory_order_relaxed);
+    return e;
+}
 
 // Launch with programmatic stream serialisation (see pdl_wait / pdl_trigger).
 template <typename... Params, typename... Args>

@@ -744,8 +744,8 @@ cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_ta
     const int nh = hkv < kScoreHeads ? hkv : kScoreHeads;
     dim3 grid(n_chunks, batch, hkv / nh);
     const size_t smem = static_cast<size_t>(kScoreChunk) * (nh * kHeadDim * 2 + 16);
-    cudaError_t e = cudaFuncSetAttribute(k_score, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    static std::atomic<int> seen[64];
+    cudaError_t e = raise_smem_limit(k_score, smem, seen);
     if (e != cudaSuccess) return e;
     return launch_pdl(k_score, grid, dim3(kScoreThreads), smem, stream,
                       static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(summ),
@@ -762,8 +762,8 @@ cudaError_t launch_select(const float *weights, const float *chunks, const int32
     const int ldc = chunks_ld(max_pages);
     const size_t smem = dense ? 0 : select_smem_bytes(max_pages, ldc);
     if (!dense) {
-        cudaError_t e = cudaFuncSetAttribute(k_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        static std::atomic<int> seen[64];
+        cudaError_t e = raise_smem_limit(k_select, smem, seen);
         if (e != cudaSuccess) return e;
     }
     return launch_pdl(k_select, dim3(batch * hkv), dim3(kSelThreads), smem, stream, weights, chunks,
