@@ -4,13 +4,13 @@
  * The library implements the data-parallel hot path of MOIRA-style sparse
  * decoding described in "MOIRA: Mass-Oriented Indexing with Ragged Attention
  * for Long-Context Decoding" (arXiv 2610.04313), abstract:
- *   - for every request, layer, KV head and decode step, a coverage rule keeps
- *     the smallest set of KV-cache pages whose estimated attention mass
- *     reaches a fraction gamma                          -> moira_select
- *   - a self-planning attention kernel reads only those pages; every thread
- *     block derives its own share of the work from the list lengths, so no
- *     host-side plan runs and the whole step can live in one CUDA graph
- *                                                       -> moira_attend
+ *   - per request, layer and KV head, at each decode step, a selection picks
+ *     the fewest KV-cache pages whose estimated share of the attention adds
+ *     up to at least gamma                              -> moira_select
+ *   - an attention kernel then reads only the picked pages; each block works
+ *     out on the device, from the list lengths alone, which pages it
+ *     handles, so there is no host-side plan and a whole step can be
+ *     captured as one CUDA graph                        -> moira_attend
  *   - the per-page estimate needs per-page metadata; following the
  *     mean-vector summaries named in "Faster Flash Decoding" (arXiv
  *     2609.00097), section 2, a page's summary is the bf16 mean of its keys
@@ -100,8 +100,9 @@ size_t moira_workspace_bytes(const moira_shape *shape, int32_t batch, int32_t ma
  * memset on `stream`; returns MOIRA_ECUDA if that fails. */
 moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream_t stream);
 
-/* Page summaries (north-star entry point "moira_update_summaries when a page
- * fills"; estimator form: mean vectors, "Faster Flash Decoding" section 2).
+/* Page summaries, made when a page fills (the per-page metadata the "MOIRA"
+ * abstract's estimate needs; estimator form: mean vectors, "Faster Flash
+ * Decoding" section 2).
  * For each listed physical page p and KV head j:
  *   summ[p][j][:] = bf16_rne( mean over the S tokens of k_pool[p][j][:][:] ),
  * accumulated in fp64 so that the mean is rounded once.
@@ -115,8 +116,8 @@ moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool
                                     const int32_t *phys_pages, int32_t n, moira_stream_t stream);
 
 /* Append one token per request to one layer's paged KV cache and keep the
- * page summaries current: the north star's "moira_update_summaries when a page
- * fills", fused with the append a serving loop does every step (the pages
+ * page summaries current: moira_update_summaries for every page the append
+ * fills, fused with the append a serving loop does every step (the pages
  * leave the append itself to the serving system).  Request r's new token is
  * token seq_lens[r] - 1, i.e. seq_lens counts it, as moira_select and
  * moira_attend expect afterwards.  Its key and value go to slot
@@ -138,9 +139,8 @@ moira_status moira_append_kv(const moira_shape *shape, const void *k_new, const 
                              const int32_t *seq_lens, int32_t batch, int32_t max_pages,
                              moira_stream_t stream);
 
-/* The coverage rule ("MOIRA" abstract: "a coverage rule keeps the smallest
- * set of pages whose estimated attention mass reaches a fraction gamma"),
- * for every (request, KV head) of one layer.
+/* The coverage rule of the "MOIRA" abstract (the fewest pages whose estimated
+ * attention share reaches gamma), for every (request, KV head) of one layer.
  *   q          : bf16 [batch][Hq][d]          this layer's queries
  *   summ       : bf16 [P][Hkv][d]             this layer's page summaries
  *   page_table : int32 [batch][max_pages]     logical -> physical page
@@ -184,9 +184,9 @@ moira_status moira_select_rule(const moira_shape *shape, const void *q, const vo
                                int32_t *lists, int32_t *lengths, void *workspace, size_t ws_bytes,
                                moira_stream_t stream);
 
-/* Self-planning ragged attention ("MOIRA" abstract: "lets each thread block
- * derive its own share of the work from the list lengths, so the whole
- * decode step stays inside the CUDA graph").  A fixed grid (a multiple of
+/* Self-planning ragged attention (the "MOIRA" abstract: blocks plan their own
+ * work from the list lengths on the device, which keeps the step graph-
+ * capturable).  A fixed grid (a multiple of
  * the SM count) splits the concatenated lists into equal page ranges; each
  * block finds its range from a device-side scan of `lengths`, computes
  * online-softmax partials per list segment, and the last block to finish a

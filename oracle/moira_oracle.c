@@ -9,10 +9,10 @@
  * Sources (the method is described only in prose, so every step below is the
  * plainest reading of that prose; readings are listed beside each function):
  *   [MOIRA]  "MOIRA: Mass-Oriented Indexing with Ragged Attention for
- *            Long-Context Decoding" (arXiv 2610.04313), abstract: per request,
- *            layer, KV head and step, a coverage rule keeps the smallest set
- *            of KV-cache pages whose *estimated* attention mass reaches a
- *            fraction gamma; attention then reads only those pages.
+ *            Long-Context Decoding" (arXiv 2610.04313), abstract: at every
+ *            decode step and for each request, layer and KV head, the fewest
+ *            KV-cache pages whose estimated share of the attention adds up to
+ *            gamma are picked, and attention reads only those pages.
  *   [FFD]    "Faster Flash Decoding" (FFD, arXiv 2609.00097; the page is a
  *            Chinese translation), section 2 (related work): metadata
  *            estimators summarise a block by its mean vector (Quest/SparQ);
@@ -142,8 +142,8 @@ static int by_mass_desc_then_index(const void *a, const void *b)
     return (x->p > y->p) - (x->p < y->p);
 }
 
-/* [MOIRA] abstract: keep the smallest set of pages whose estimated mass
- * reaches gamma.  Sorting by mass and taking the shortest prefix whose running
+/* [MOIRA] abstract: pick the fewest pages whose estimated mass adds up to
+ * gamma.  Sorting by mass and taking the shortest prefix whose running
  * sum is >= gamma gives a smallest such set (any k pages have no more mass
  * than the k largest).  gamma >= 1 keeps every page.  If rounding keeps the
  * running sum below gamma, every page is kept.

@@ -1,10 +1,10 @@
 """GB300-native (sm_103a) hot path of MOIRA-style sparse decoding.
 
 MOIRA ("Mass-Oriented Indexing with Ragged Attention for Long-Context
-Decoding", arXiv 2610.04313): per request, layer and KV head, a coverage rule
-keeps the smallest set of KV-cache pages whose estimated attention mass
-reaches gamma, and a self-planning ragged attention kernel reads only those
-pages.  The compute lives in ``libmoira.so`` (hand-written CUDA, C ABI in
+Decoding", arXiv 2610.04313): at each decode step, per request, layer and KV
+head, the fewest KV-cache pages whose estimated share of the attention adds
+up to gamma are picked, and an attention kernel that plans its own work from
+the list lengths reads only those pages.  The compute lives in ``libmoira.so`` (hand-written CUDA, C ABI in
 ``include/moira.h``); this package only marshals torch tensors into it.
 The library is loaded on first use; there is no CPU fallback.
 """

@@ -26,21 +26,9 @@ int current_sm_count()
     return sms;
 }
 
-// The attention grid is a fixed multiple of the SM count: blocks_per_sm
-// resident blocks per SM times `waves` (MOIRA_ATTEND_WAVES, default 1).  More
-// waves give smaller page ranges, so SMs that finish early pick up pending
-// blocks; the value is read once per process.
-int attend_waves()
-{
-    static int waves = [] {
-        const char *e = std::getenv("MOIRA_ATTEND_WAVES");
-        const int v = e ? std::atoi(e) : 1;
-        return v < 1 ? 1 : (v > 16 ? 16 : v);
-    }();
-    return waves;
-}
-
-int attend_blocks() { return current_sm_count() * attend_blocks_per_sm() * attend_waves(); }
+// The attention grid: every SM holds attend_blocks_per_sm() resident blocks
+// (one wave; each block takes an equal range of the concatenated lists).
+int attend_blocks() { return current_sm_count() * attend_blocks_per_sm(); }
 
 moira_status check_shape(const moira_shape *s)
 {

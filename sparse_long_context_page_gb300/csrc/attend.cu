@@ -1,7 +1,7 @@
 // Self-planning ragged paged attention ("MOIRA: Mass-Oriented Indexing with
-// Ragged Attention for Long-Context Decoding", abstract: "each thread block
-// derive[s] its own share of the work from the list lengths, so the whole
-// decode step stays inside the CUDA graph"), with sequence-split partials
+// Ragged Attention for Long-Context Decoding", abstract: the blocks plan
+// their own work on the device from the list lengths, so no host plan runs
+// and the step can be captured as one CUDA graph), with sequence-split partials
 // merged by log-sum-exp (FlashDecoding, "Faster Flash Decoding" section 2).
 //
 // Work plan, computed by every block from device data only:

@@ -1,7 +1,7 @@
 // The gamma-coverage selection of "MOIRA: Mass-Oriented Indexing with Ragged
-// Attention for Long-Context Decoding", abstract: for every request, layer,
-// KV head and step, keep the smallest set of pages whose estimated attention
-// mass reaches gamma.
+// Attention for Long-Context Decoding", abstract: per request, layer and KV
+// head at each decode step, pick the fewest pages whose estimated share of
+// the attention adds up to gamma.
 //
 // Two kernels per layer:
 //  k_score  : all SMs stream the page summaries once (bulk copies into shared
