@@ -61,7 +61,7 @@ typedef enum moira_status {
     MOIRA_EINVAL = 1,        /* an argument failed a host-side check; nothing launched */
     MOIRA_EWORKSPACE = 2,    /* workspace NULL, misaligned or smaller than required */
     MOIRA_ECUDA = 3,         /* a CUDA runtime call or a kernel launch failed */
-    MOIRA_EUNSUPPORTED = 4   /* a shape this build does not implement (see moira_shape) */
+    MOIRA_EUNSUPPORTED = 4   /* a shape this library does not implement (see moira_shape) */
 } moira_status;
 
 /* Bits of the device status word (sticky until cleared). */
@@ -69,7 +69,7 @@ typedef enum moira_status {
 #define MOIRA_DEV_BADLEN  0x2u   /* a seq_len or list length out of range was clamped */
 #define MOIRA_DEV_TIMEOUT 0x4u   /* a bounded device wait ran out; results are invalid */
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define MOIRA_HEAD_DIM 128               /* d */
 #define MOIRA_PAGE_SIZE 16               /* S, tokens per page */
 #define MOIRA_GROUP 4                    /* G = Hq / Hkv */

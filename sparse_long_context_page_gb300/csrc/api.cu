@@ -382,7 +382,7 @@ const char *moira_status_string(moira_status status)
     case MOIRA_EINVAL: return "invalid argument";
     case MOIRA_EWORKSPACE: return "workspace missing, misaligned or too small";
     case MOIRA_ECUDA: return "CUDA runtime error";
-    case MOIRA_EUNSUPPORTED: return "shape not supported by this build";
+    case MOIRA_EUNSUPPORTED: return "shape not supported by this library";
     }
     return "unknown status";
 }
