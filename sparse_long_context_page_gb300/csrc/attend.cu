@@ -10,7 +10,7 @@
 //   [b*W/n, (b+1)*W/n) of the lists laid end to end and splits its range at
 //   list boundaries into segments.  A segment's partial goes to slot b + u
 //   (u = list index), which is unique.  Partials are merged by
-//   log-sum-exp in two levels: the last block to finish in each group of 16
+//   log-sum-exp in two levels: the last block to finish in each group of 12
 //   consecutive blocks of a list merges the group, and the last group to
 //   finish writes the output (arrival counters, self-resetting); a list held
 //   by one block, or by one group, is written by that block or group merge.
@@ -62,7 +62,8 @@ __host__ __device__ inline size_t attend_smem_bytes(int units)
            sizeof(int) * static_cast<size_t>(units + 1);
 }
 
-constexpr int kMergeSpan = 16;            // partials merged per batch (and per group)
+constexpr int kMergeSpan = 12;            // blocks per first-level merge group
+constexpr int kMergeBatch = 12;           // partials loaded together in a merge
 
 // Online log-sum-exp merge of `count` partials stored at slots first,
 // first + stride, ... for this thread's head h and dims d0..d0+3: returns the
@@ -74,11 +75,11 @@ __device__ __forceinline__ void merge_partials(const float *partials, int first,
 {
     float Mrun = -INFINITY, la = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = 0; k0 < count; k0 += kMergeSpan) {
-        float mv[kMergeSpan], lv[kMergeSpan];
-        float4 ov[kMergeSpan];
+    for (int k0 = 0; k0 < count; k0 += kMergeBatch) {
+        float mv[kMergeBatch], lv[kMergeBatch];
+        float4 ov[kMergeBatch];
 #pragma unroll
-        for (int k = 0; k < kMergeSpan; ++k) {
+        for (int k = 0; k < kMergeBatch; ++k) {
             mv[k] = -INFINITY;
             lv[k] = 0.f;
             ov[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -91,13 +92,13 @@ __device__ __forceinline__ void merge_partials(const float *partials, int first,
         }
         float mb = Mrun;
 #pragma unroll
-        for (int k = 0; k < kMergeSpan; ++k) mb = fmaxf(mb, mv[k]);
+        for (int k = 0; k < kMergeBatch; ++k) mb = fmaxf(mb, mv[k]);
         const float ms = mb == -INFINITY ? 0.f : mb;
         const float sc = exp2f(Mrun - ms);
         acc.x *= sc; acc.y *= sc; acc.z *= sc; acc.w *= sc;
         la *= sc;
 #pragma unroll
-        for (int k = 0; k < kMergeSpan; ++k) {
+        for (int k = 0; k < kMergeBatch; ++k) {
             const float e = exp2f(mv[k] - ms);
             acc.x += e * ov[k].x; acc.y += e * ov[k].y; acc.z += e * ov[k].z; acc.w += e * ov[k].w;
             la += e * lv[k];
