@@ -34,6 +34,7 @@ namespace moira {
 // ---------------------------------------------------------------------------
 constexpr int kScoreThreads = 256;        // 8 warps: one (KV head, 16-page half) item each
 constexpr int kScoreHeads = 4;            // KV heads per block; blockIdx.z picks the slice
+static_assert(kScoreHeads * 2 <= kScoreThreads / 32, "one (KV head, 16-page half) item per warp");
 
 // One block scores kScoreChunk (32) consecutive full pages of one request for
 // kScoreHeads KV heads (Hkv = 8 takes two blocks per chunk, so about four
