@@ -95,6 +95,60 @@ void oracle_summaries(const uint16_t *k_blocks, int64_t n_blocks, int32_t S,
     }
 }
 
+/* ---- low-bit page summaries ------------------------------------------- */
+
+/* The same mean-key summary stored in `bits` bits per element, after the
+ * low-bit key "thumbnails" of "Faster Flash Decoding" (section 3.1: a
+ * symmetric mid-rise quantiser, which has no zero level, so every element
+ * keeps its sign).  Applied here to the page's mean key, not to each token:
+ *   mean_i = (1/S) sum_t K[t][i]            fp64, token order (no bf16 rounding)
+ *   a      = max_i |mean_i|
+ *   step   = a / (2^(bits-1) - 1/2), rounded once to fp32
+ *   code_i = floor(mean_i / step), clamped to [-2^(bits-1), 2^(bits-1) - 1]
+ *   value  = (code_i + 1/2) * step
+ * so the outermost levels sit at +-a.  A block with a non-finite mean element,
+ * with a == 0 or with a step that rounds to 0 gets step 0 and codes 0 (value
+ * 0).  bits is 8 or 2.
+ *   k_blocks  : [n_blocks][S][d] bf16 bit patterns
+ *   codes_out : [n_blocks][d]    one code per element (unpacked)
+ *   step_out  : [n_blocks]       fp32 step */
+void oracle_summaries_lowbit(const uint16_t *k_blocks, int64_t n_blocks, int32_t S, int32_t d,
+                             int32_t bits, int8_t *codes_out, float *step_out)
+{
+    const double half_levels = ldexp(1.0, bits - 1);            /* 2^(bits-1) */
+    double *mean = (double *)malloc(sizeof(double) * (size_t)d);
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        double a = 0.0;
+        int finite = 1;
+        for (int32_t i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int32_t t = 0; t < S; ++t)
+                acc += bf16_to_double(k_blocks[((size_t)b * S + t) * d + i]);
+            mean[i] = acc / (double)S;
+            if (!isfinite(mean[i])) finite = 0;
+            else if (fabs(mean[i]) > a) a = fabs(mean[i]);
+        }
+        float step = finite ? (float)(a / (half_levels - 0.5)) : 0.0f;
+        step_out[b] = step;
+        for (int32_t i = 0; i < d; ++i) {
+            double c = 0.0;
+            if (step > 0.0f) {
+                c = floor(mean[i] / (double)step);
+                if (c < -half_levels) c = -half_levels;
+                if (c > half_levels - 1.0) c = half_levels - 1.0;
+            }
+            codes_out[(size_t)b * d + i] = (int8_t)c;
+        }
+    }
+    free(mean);
+}
+
+/* The value a low-bit summary stands for (exact in fp64). */
+static double lowbit_value(int8_t code, float step)
+{
+    return ((double)code + 0.5) * (double)step;
+}
+
 /* ---- estimated page mass ------------------------------------------------ */
 
 /* Scores and masses for one (request, KV head) unit.
@@ -283,6 +337,76 @@ int32_t oracle_select_unit_rule(const uint16_t *q_group, const uint16_t *summ_po
         if (keep[p]) list_out[n++] = p;
     if (T) list_out[n++] = F;
     free(summ);
+    free(mass);
+    free(keep);
+    return n;
+}
+
+/* Scores and masses of one unit from low-bit summaries: oracle_page_mass
+ * with kbar_p[i] = (code + 1/2) * step.
+ *   codes : [F][d] (logical order), steps : [F] */
+void oracle_page_mass_lowbit(const uint16_t *q_group, const int8_t *codes, const float *steps,
+                             int32_t G, int32_t F, int32_t d, double sm_scale, double *scores,
+                             double *mass)
+{
+    double *s = (double *)malloc(sizeof(double) * (size_t)(F > 0 ? F : 1));
+    for (int32_t p = 0; p < F; ++p) mass[p] = 0.0;
+    for (int32_t h = 0; h < G; ++h) {
+        double smax = -INFINITY;
+        for (int32_t p = 0; p < F; ++p) {
+            double dot = 0.0;
+            for (int32_t i = 0; i < d; ++i)
+                dot += bf16_to_double(q_group[(size_t)h * d + i]) *
+                       lowbit_value(codes[(size_t)p * d + i], steps[p]);
+            s[p] = sm_scale * dot;
+            if (scores) scores[(size_t)h * F + p] = s[p];
+            if (s[p] > smax) smax = s[p];
+        }
+        double z = 0.0;
+        for (int32_t p = 0; p < F; ++p) z += exp(s[p] - smax);
+        for (int32_t p = 0; p < F; ++p) mass[p] += exp(s[p] - smax) / z / (double)G;
+    }
+    free(s);
+}
+
+/* One unit's selection from low-bit summaries under `rule` (0 = coverage,
+ * 1 = top-k, 2 = top-delta, as oracle_select_unit_rule): the estimator reads
+ * (code + 1/2) * step instead of the bf16 mean; the tail page and the list
+ * order are unchanged.
+ *   codes_pool : [*][Hkv][d] by physical page, steps_pool : [*][Hkv]
+ *   mass_out   : [F] out (nullable; left untouched when no estimate is made)
+ * Returns the list length. */
+int32_t oracle_select_unit_lowbit(const uint16_t *q_group, const int8_t *codes_pool,
+                                  const float *steps_pool, int32_t Hkv, int32_t j,
+                                  const int32_t *page_row, int32_t seq_len, int32_t S, int32_t G,
+                                  int32_t d, int32_t rule, double param, double sm_scale,
+                                  int32_t *list_out, double *mass_out)
+{
+    int32_t F = seq_len / S, T = (seq_len % S) != 0;
+    int32_t n = 0;
+    if (F == 0 || (rule == 0 && param >= 1.0)) {
+        for (int32_t p = 0; p < F + T; ++p) list_out[n++] = p;
+        return n;
+    }
+    int8_t *codes = (int8_t *)malloc((size_t)F * d);
+    float *steps = (float *)malloc(sizeof(float) * (size_t)F);
+    for (int32_t p = 0; p < F; ++p) {
+        size_t blk = (size_t)page_row[p] * Hkv + j;
+        memcpy(codes + (size_t)p * d, codes_pool + blk * d, (size_t)d);
+        steps[p] = steps_pool[blk];
+    }
+    double *mass = (double *)malloc(sizeof(double) * (size_t)F);
+    uint8_t *keep = (uint8_t *)malloc((size_t)F);
+    oracle_page_mass_lowbit(q_group, codes, steps, G, F, d, sm_scale, NULL, mass);
+    if (rule == 0) oracle_cover(mass, F, param, keep, NULL, NULL);
+    else if (rule == 1) oracle_topk(mass, F, (int32_t)param, keep);
+    else oracle_topdelta(mass, F, param, keep);
+    for (int32_t p = 0; p < F; ++p)
+        if (keep[p]) list_out[n++] = p;
+    if (T) list_out[n++] = F;
+    if (mass_out) memcpy(mass_out, mass, sizeof(double) * (size_t)F);
+    free(codes);
+    free(steps);
     free(mass);
     free(keep);
     return n;

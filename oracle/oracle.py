@@ -24,6 +24,8 @@ _u16p = ctypes.POINTER(ctypes.c_uint16)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _f64p = ctypes.POINTER(ctypes.c_double)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
+_i8p = ctypes.POINTER(ctypes.c_int8)
+_f32p = ctypes.POINTER(ctypes.c_float)
 
 
 def build(force: bool = False) -> str:
@@ -72,6 +74,17 @@ def _load():
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32,
                                        ctypes.c_double, ctypes.c_double, _i32p, _f64p, ctypes.c_int32]
     lib.oracle_decode_step.restype = ctypes.c_int32
+    lib.oracle_summaries_lowbit.argtypes = [_u16p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, _i8p, _f32p]
+    lib.oracle_summaries_lowbit.restype = None
+    lib.oracle_page_mass_lowbit.argtypes = [_u16p, _i8p, _f32p, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_double, _f64p, _f64p]
+    lib.oracle_page_mass_lowbit.restype = None
+    lib.oracle_select_unit_lowbit.argtypes = [_u16p, _i8p, _f32p, ctypes.c_int32, ctypes.c_int32,
+                                              _i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, ctypes.c_int32, ctypes.c_double,
+                                              ctypes.c_double, _i32p, _f64p]
+    lib.oracle_select_unit_lowbit.restype = ctypes.c_int32
     _lib = lib
     return lib
 
@@ -225,3 +238,55 @@ def decode_step(q, summ, k_pool, v_pool, page_table, seq_lens, gamma, sm_scale, 
                                   float(gamma), float(sm_scale), lengths.ctypes.data_as(_i32p),
                                   out.ctypes.data_as(_f64p), int(n_threads))
     return lengths, out, int(used)
+
+
+def summaries_lowbit(k_blocks: np.ndarray, bits: int = 8):
+    """Mid-rise low-bit mean key of each block.  ``k_blocks``: uint16
+    [n][S][d] -> (codes int8 [n][d], steps float32 [n]); the summary stands
+    for (codes + 1/2) * steps."""
+    lib = _load()
+    n, S, d = k_blocks.shape
+    kb, kp = _c(k_blocks, np.uint16, _u16p)
+    codes = np.empty((n, d), np.int8)
+    steps = np.empty(n, np.float32)
+    lib.oracle_summaries_lowbit(kp, n, S, d, int(bits), codes.ctypes.data_as(_i8p),
+                                steps.ctypes.data_as(_f32p))
+    return codes, steps
+
+
+def page_mass_lowbit(q_group: np.ndarray, codes: np.ndarray, steps: np.ndarray, sm_scale: float):
+    """Scores [G][F] and masses [F] of one unit from low-bit summaries in
+    logical order (codes int8 [F][d], steps float32 [F])."""
+    lib = _load()
+    G, d = q_group.shape
+    F = codes.shape[0]
+    qa, qp = _c(q_group, np.uint16, _u16p)
+    ca, cp = _c(codes.reshape(F, d), np.int8, _i8p)
+    sa, sp = _c(steps.reshape(F), np.float32, _f32p)
+    scores = np.empty((G, F), np.float64)
+    mass = np.empty(F, np.float64)
+    lib.oracle_page_mass_lowbit(qp, cp, sp, G, F, d, float(sm_scale), scores.ctypes.data_as(_f64p),
+                                mass.ctypes.data_as(_f64p))
+    return scores, mass
+
+
+def select_unit_lowbit(q_group, codes_pool, steps_pool, j, page_row, seq_len, rule, param,
+                       sm_scale, page_size=16):
+    """Selection for one unit from low-bit summaries under `rule` ->
+    (kept LOGICAL pages, mass [F]; zeros when no estimate is made).
+    ``codes_pool``: int8 [*][Hkv][d], ``steps_pool``: float32 [*][Hkv], both by
+    physical page."""
+    lib = _load()
+    G, d = q_group.shape
+    Hkv = codes_pool.shape[-2]
+    F = seq_len // page_size
+    qa, qp = _c(q_group, np.uint16, _u16p)
+    ca, cp = _c(codes_pool, np.int8, _i8p)
+    sa, sp = _c(steps_pool, np.float32, _f32p)
+    ra, rp = _c(page_row, np.int32, _i32p)
+    lst = np.empty(F + 1, np.int32)
+    mass = np.zeros(F, np.float64)
+    n = lib.oracle_select_unit_lowbit(qp, cp, sp, Hkv, j, rp, seq_len, page_size, G, d, int(rule),
+                                      float(param), float(sm_scale), lst.ctypes.data_as(_i32p),
+                                      mass.ctypes.data_as(_f64p))
+    return lst[:n].copy(), mass
