@@ -346,6 +346,48 @@ def compare_rules(st, w, head, results, args):
     return out
 
 
+def compare_summaries(w, head, args):
+    """The headline step with each page-summary format: the bf16 mean key and
+    its 8-bit and 2-bit mid-rise codes.  Per format: step time (graph), the
+    in-graph selection and attention halves per layer, pages read, summary
+    bytes per step, and the attention output against the dense (gamma = 1)
+    step's (relative L2 per (layer, request, query head))."""
+    import sparse_long_context_page_gb300 as moira
+    from sparse_long_context_page_gb300.state import DecodeState
+    sp = w.spec
+    out = {}
+    dense_out = None
+    full = int((torch.from_numpy(w.seq_lens.astype(np.int64)) // 16).sum())     # full pages, one layer
+    for name, fmt in (("bf16", moira.SUMM_BF16), ("q8", moira.SUMM_Q8), ("q2", moira.SUMM_Q2)):
+        st = DecodeState(w, fmt=fmt)
+        st.summarize()
+        if dense_out is None:
+            st.step(1.0)
+            torch.cuda.synchronize()
+            dense_out = st.out.clone()
+        g = capture_fn(lambda: st.step(head))
+        ms, _ = time_graph(g, max(3, args.steps // 2), args.warmup, 1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert moira.read_device_status(st.ws) == 0
+        pages = int(st.lengths.sum())
+        tails = int((st.seq_lens % 16 != 0).sum()) * sp.kv_heads * sp.layers
+        err = (st.out - dense_out).norm(dim=-1) / dense_out.norm(dim=-1).clamp_min(1e-30)
+        err = err.flatten().double().cpu().numpy()
+        sel_ms, att_ms = time_parts(st, head, max(3, args.steps // 4), args.warmup)
+        out[name] = {"us_per_step": round(ms * 1e3, 2),
+                     "per_layer_us": {"select": round(sel_ms * 1e3, 2), "attend": round(att_ms * 1e3, 2)},
+                     "summary_bytes_per_step": full * sp.layers * moira.summary_page_bytes(st.shape, fmt),
+                     "pages_fraction": round(pages / float(full * sp.kv_heads * sp.layers + tails), 4),
+                     "out_rel_l2_vs_dense": {"mean": float(np.mean(err)), "p99": float(np.percentile(err, 99)),
+                                             "max": float(np.max(err))}}
+        log(f"[bench] summaries {name}: {ms * 1e3:.1f} us/step, select {sel_ms * 1e3:.2f} us/layer, "
+            f"pages {out[name]['pages_fraction']:.4f}, rel-L2 mean {np.mean(err):.4f}")
+        del g, st
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import sparse_long_context_page_gb300 as moira
     from sparse_long_context_page_gb300 import workloads as W
@@ -399,6 +441,7 @@ def run_ours(args):
     # to read the same pages as coverage at the headline gamma; quality is the
     # attention output against the dense step's
     rules = compare_rules(st, w, head, results, args) if not args.no_rules else None
+    formats = compare_summaries(w, head, args) if not args.no_rules else None
 
     # end to end: host q in, host out back, through moira_decode_step_host
     q_host = w.q.cpu().pin_memory()
@@ -491,6 +534,7 @@ def run_ours(args):
         "clocks": hd["clocks"],
         "cpu_baseline": cpu,
         "rules_at_equal_pages": rules,
+        "summary_formats": formats,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -548,7 +592,7 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rules", action="store_true",
-                    help="skip the top-k / top-delta comparison at equal pages")
+                    help="skip the comparisons: top-k / top-delta at equal pages, and the summary formats")
     ap.add_argument("--layers", type=int, default=0,
                     help="fewer layers than the workload's (small profiling cases only)")
     args = ap.parse_args()

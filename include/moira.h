@@ -100,6 +100,37 @@ size_t moira_workspace_bytes(const moira_shape *shape, int32_t batch, int32_t ma
  * memset on `stream`; returns MOIRA_ECUDA if that fails. */
 moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream_t stream);
 
+/* Page-summary formats.  The estimator reads one summary per (page, KV head).
+ * MOIRA_SUMM_BF16 stores the mean key as bf16 [P][Hkv][d].  The low-bit
+ * formats store the same mean key (taken in fp64, before any rounding) with
+ * the symmetric mid-rise quantiser that "Faster Flash Decoding" (section
+ * 3.1) uses for its low-bit key thumbnails, here with b = 8 or 2 bits:
+ *   step   = max_i |mean_i| / (2^(b-1) - 1/2), rounded once to fp32
+ *   code_i = floor(mean_i / step), clamped to [-2^(b-1), 2^(b-1) - 1]
+ * and the summary stands for (code_i + 1/2) * step.  The quantiser has no
+ * zero level, so every element keeps its sign.  A mean with a non-finite
+ * element, an all-zero mean, or a step that rounds to 0 gets step 0 and
+ * codes 0.
+ * Low-bit layout: one record of moira_summary_page_bytes() bytes per
+ * physical page, and per record:
+ *   bytes [0, Hkv*cb)               codes, KV head j at [j*cb, (j+1)*cb), cb = d*b/8
+ *                                   Q8: byte i = code of element i (int8)
+ *                                   Q2: element i in bits 2*(i%4)+1 .. 2*(i%4) of
+ *                                       byte i/4, stored as code + 2 (0..3)
+ *   bytes [Hkv*cb, Hkv*cb + 4*Hkv)  fp32 step of each KV head
+ *   then zero bytes up to a multiple of 16
+ * At Hkv = 8 a page's summaries take 2048 (BF16), 1056 (Q8) or 288 (Q2) bytes. */
+typedef enum {
+    MOIRA_SUMM_BF16 = 0,
+    MOIRA_SUMM_Q8 = 1,
+    MOIRA_SUMM_Q2 = 2
+} moira_summ_format;
+
+/* Bytes of one physical page's summaries (all KV heads) in `format`, i.e.
+ * one layer's summary buffer holds num_phys_pages times this.  0 if the shape
+ * or the format is invalid. */
+size_t moira_summary_page_bytes(const moira_shape *shape, int32_t format);
+
 /* Page summaries, made when a page fills (the per-page metadata the "MOIRA"
  * abstract's estimate needs; estimator form: mean vectors, "Faster Flash
  * Decoding" section 2).
@@ -114,6 +145,14 @@ moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream
  * Not part of the decode step: call it when pages fill or after prefill. */
 moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool, void *summ,
                                     const int32_t *phys_pages, int32_t n, moira_stream_t stream);
+
+/* moira_update_summaries in any summary format (moira_summ_format): `summ`
+ * is that layer's summary buffer, num_phys_pages * moira_summary_page_bytes()
+ * bytes, 16-byte aligned.  MOIRA_SUMM_BF16 is exactly moira_update_summaries.
+ * An unknown format returns MOIRA_EINVAL. */
+moira_status moira_update_summaries_ex(const moira_shape *shape, int32_t format, const void *k_pool,
+                                       void *summ, const int32_t *phys_pages, int32_t n,
+                                       moira_stream_t stream);
 
 /* Append one token per request to one layer's paged KV cache and keep the
  * page summaries current: moira_update_summaries for every page the append
@@ -138,6 +177,13 @@ moira_status moira_append_kv(const moira_shape *shape, const void *k_new, const 
                              void *k_pool, void *v_pool, void *summ, const int32_t *page_table,
                              const int32_t *seq_lens, int32_t batch, int32_t max_pages,
                              moira_stream_t stream);
+
+/* moira_append_kv with the summaries of filled pages written in `format`
+ * (as moira_update_summaries_ex would write them). */
+moira_status moira_append_kv_ex(const moira_shape *shape, int32_t format, const void *k_new,
+                                const void *v_new, void *k_pool, void *v_pool, void *summ,
+                                const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                                int32_t max_pages, moira_stream_t stream);
 
 /* The coverage rule of the "MOIRA" abstract (the fewest pages whose estimated
  * attention share reaches gamma), for every (request, KV head) of one layer.
@@ -184,6 +230,16 @@ moira_status moira_select_rule(const moira_shape *shape, const void *q, const vo
                                int32_t *lists, int32_t *lengths, void *workspace, size_t ws_bytes,
                                moira_stream_t stream);
 
+/* moira_select_rule reading summaries in `format` (moira_summ_format): the
+ * estimator takes the summary's value, (code + 1/2) * step for the low-bit
+ * formats, in place of the bf16 mean key; everything else is unchanged.
+ * MOIRA_SUMM_BF16 is exactly moira_select_rule. */
+moira_status moira_select_ex(const moira_shape *shape, int32_t format, const void *q,
+                             const void *summ, const int32_t *page_table, const int32_t *seq_lens,
+                             int32_t batch, int32_t max_pages, int32_t rule, float param,
+                             float sm_scale, int32_t *lists, int32_t *lengths, void *workspace,
+                             size_t ws_bytes, moira_stream_t stream);
+
 /* Self-planning ragged attention (the "MOIRA" abstract: blocks plan their own
  * work from the list lengths on the device, which keeps the step graph-
  * capturable).  A fixed grid (a multiple of
@@ -224,6 +280,19 @@ moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, con
                                float gamma, float sm_scale, int32_t *lists, int32_t *lengths_all,
                                float *out_all, void *workspace, size_t ws_bytes,
                                moira_stream_t stream);
+
+/* moira_decode_step with any summary format and page rule: per layer
+ * moira_select_ex(format, rule, param) then moira_attend.  summ_all holds
+ * the layers' summary buffers back to back, num_phys_pages *
+ * moira_summary_page_bytes() bytes each. */
+moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int32_t num_layers,
+                                  const void *q_all, const void *k_pool_all,
+                                  const void *v_pool_all, const void *summ_all,
+                                  const int32_t *page_table, const int32_t *seq_lens,
+                                  int32_t batch, int32_t max_pages, int32_t rule, float param,
+                                  float sm_scale, int32_t *lists, int32_t *lengths_all,
+                                  float *out_all, void *workspace, size_t ws_bytes,
+                                  moira_stream_t stream);
 
 /* The same step with the per-step inputs and outputs in HOST memory:
  * q_host (bf16 [L][batch][Hq][d]) is copied to the device staging buffer

@@ -10,14 +10,16 @@ The library is loaded on first use; there is no CPU fallback.
 """
 from ._binding import (DEV_BADLEN, DEV_BADPAGE, DEV_TIMEOUT, EXPORTS, GROUP, HEAD_DIM,
                        MAX_PAGES_PER_SEQ, MAX_UNITS, PAGE_SIZE, RULE_COVERAGE, RULE_TOPDELTA,
-                       RULE_TOPK, MoiraError, Shape, append_kv, attend, attend_grid_blocks, decode_step,
-                       decode_step_host, library_path, load_library, make_workspace,
-                       read_device_status, select, select_rule, shape_of, update_summaries,
-                       workspace_bytes, workspace_init)
+                       RULE_TOPK, SUMM_BF16, SUMM_Q2, SUMM_Q8, MoiraError, Shape, append_kv, attend,
+                       attend_grid_blocks, decode_step, decode_step_ex, decode_step_host,
+                       library_path, load_library, make_summaries, make_workspace,
+                       read_device_status, select, select_ex, select_rule, shape_of,
+                       summary_page_bytes, update_summaries, workspace_bytes, workspace_init)
 
 __all__ = ["DEV_BADLEN", "DEV_BADPAGE", "DEV_TIMEOUT", "EXPORTS", "GROUP", "HEAD_DIM",
            "MAX_PAGES_PER_SEQ", "MAX_UNITS", "PAGE_SIZE", "RULE_COVERAGE", "RULE_TOPDELTA",
-           "RULE_TOPK", "MoiraError", "Shape", "append_kv", "attend", "attend_grid_blocks", "decode_step",
-           "decode_step_host", "library_path", "load_library", "make_workspace",
-           "read_device_status", "select", "select_rule", "shape_of", "update_summaries",
-           "workspace_bytes", "workspace_init"]
+           "RULE_TOPK", "SUMM_BF16", "SUMM_Q2", "SUMM_Q8", "MoiraError", "Shape", "append_kv",
+           "attend", "attend_grid_blocks", "decode_step", "decode_step_ex", "decode_step_host",
+           "library_path", "load_library", "make_summaries", "make_workspace",
+           "read_device_status", "select", "select_ex", "select_rule", "shape_of",
+           "summary_page_bytes", "update_summaries", "workspace_bytes", "workspace_init"]

@@ -32,10 +32,13 @@ EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summar
            "moira_select", "moira_attend", "moira_decode_step", "moira_decode_step_host",
            "moira_read_device_status", "moira_attend_grid_blocks", "moira_status_string",
            "moira_select_noalloc", "moira_select_rule", "moira_append_kv",
-           "moira_diag_wait_timeout")
+           "moira_diag_wait_timeout", "moira_summary_page_bytes", "moira_update_summaries_ex",
+           "moira_append_kv_ex", "moira_select_ex", "moira_decode_step_ex")
 
 # page rules of moira_select_rule (moira_rule in include/moira.h)
 RULE_COVERAGE, RULE_TOPK, RULE_TOPDELTA = 0, 1, 2
+# page-summary formats (moira_summ_format in include/moira.h)
+SUMM_BF16, SUMM_Q8, SUMM_Q2 = 0, 1, 2
 
 
 class MoiraError(RuntimeError):
@@ -105,6 +108,19 @@ def load_library(build_if_missing: bool = True):
     lib.moira_select_noalloc.argtypes = [sp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
                                          ctypes.c_float, _vp, _vp, _vp]
     lib.moira_select_noalloc.restype = ctypes.c_int
+    lib.moira_summary_page_bytes.argtypes = [sp, _i32]
+    lib.moira_summary_page_bytes.restype = ctypes.c_size_t
+    lib.moira_update_summaries_ex.argtypes = [sp, _i32, _vp, _vp, _vp, _i32, _vp]
+    lib.moira_update_summaries_ex.restype = ctypes.c_int
+    lib.moira_append_kv_ex.argtypes = [sp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp]
+    lib.moira_append_kv_ex.restype = ctypes.c_int
+    lib.moira_select_ex.argtypes = [sp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, ctypes.c_float,
+                                    ctypes.c_float, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.moira_select_ex.restype = ctypes.c_int
+    lib.moira_decode_step_ex.argtypes = [sp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                         _i32, ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp,
+                                         ctypes.c_size_t, _vp]
+    lib.moira_decode_step_ex.restype = ctypes.c_int
     lib.moira_status_string.argtypes = [ctypes.c_int]
     lib.moira_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -159,28 +175,61 @@ def workspace_init(ws: torch.Tensor, stream=None):
                                                _stream(stream)), "moira_workspace_init")
 
 
+def summary_page_bytes(shape: Shape, fmt: int = SUMM_BF16) -> int:
+    """Bytes of one physical page's summaries (all KV heads) in format `fmt`."""
+    n = load_library().moira_summary_page_bytes(ctypes.byref(shape), int(fmt))
+    if n == 0:
+        raise MoiraError(1, "moira_summary_page_bytes")
+    return int(n)
+
+
+def make_summaries(shape: Shape, fmt: int = SUMM_BF16, layers: int | None = None, device=None):
+    """Zeroed summary buffer(s) for `fmt`: bf16 [(layers,) P, Hkv, d] for
+    SUMM_BF16, else uint8 [(layers,) P, page_bytes] records."""
+    lead = () if layers is None else (layers,)
+    P = shape.num_phys_pages
+    if fmt == SUMM_BF16:
+        return torch.zeros(lead + (P, shape.num_kv_heads, shape.head_dim), dtype=torch.bfloat16,
+                           device=device or "cuda")
+    return torch.zeros(lead + (P, summary_page_bytes(shape, fmt)), dtype=torch.uint8,
+                       device=device or "cuda")
+
+
+def _summ(summ: torch.Tensor, fmt: int):
+    return _dev(summ, "summ", torch.bfloat16 if fmt == SUMM_BF16 else torch.uint8)
+
+
 def update_summaries(shape: Shape, k_pool: torch.Tensor, summ: torch.Tensor,
-                     phys_pages: torch.Tensor, stream=None):
-    """summ[p] = bf16 mean of k_pool[p]'s keys for every listed physical page p."""
+                     phys_pages: torch.Tensor, stream=None, fmt: int = SUMM_BF16):
+    """Summaries of every listed physical page p from k_pool[p]'s keys: the
+    bf16 mean key (SUMM_BF16) or its low-bit record (SUMM_Q8 / SUMM_Q2)."""
     lib = load_library()
-    _check(lib.moira_update_summaries(ctypes.byref(shape), _dev(k_pool, "k_pool", torch.bfloat16),
-                                      _dev(summ, "summ", torch.bfloat16),
-                                      _dev(phys_pages, "phys_pages", torch.int32, 1),
-                                      phys_pages.numel(), _stream(stream)),
-           "moira_update_summaries")
+    pp = _dev(phys_pages, "phys_pages", torch.int32, 1)
+    if fmt == SUMM_BF16:
+        st = lib.moira_update_summaries(ctypes.byref(shape), _dev(k_pool, "k_pool", torch.bfloat16),
+                                        _summ(summ, fmt), pp, phys_pages.numel(), _stream(stream))
+    else:
+        st = lib.moira_update_summaries_ex(ctypes.byref(shape), int(fmt),
+                                           _dev(k_pool, "k_pool", torch.bfloat16), _summ(summ, fmt),
+                                           pp, phys_pages.numel(), _stream(stream))
+    _check(st, "moira_update_summaries")
 
 
-def append_kv(shape: Shape, k_new, v_new, k_pool, v_pool, summ, page_table, seq_lens, stream=None):
+def append_kv(shape: Shape, k_new, v_new, k_pool, v_pool, summ, page_table, seq_lens, stream=None,
+              fmt: int = SUMM_BF16):
     """Write each request's new token (token seq_lens[r]-1) into its page and
-    recompute the summary of every page that this fills."""
+    recompute the summary (in format `fmt`) of every page that this fills."""
     lib = load_library()
     batch, max_pages = page_table.shape
-    _check(lib.moira_append_kv(ctypes.byref(shape), _dev(k_new, "k_new", torch.bfloat16),
-                               _dev(v_new, "v_new", torch.bfloat16), _dev(k_pool, "k_pool", torch.bfloat16),
-                               _dev(v_pool, "v_pool", torch.bfloat16), _dev(summ, "summ", torch.bfloat16),
-                               _dev(page_table, "page_table", torch.int32, 2),
-                               _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
-                               _stream(stream)), "moira_append_kv")
+    args = (_dev(k_new, "k_new", torch.bfloat16), _dev(v_new, "v_new", torch.bfloat16),
+            _dev(k_pool, "k_pool", torch.bfloat16), _dev(v_pool, "v_pool", torch.bfloat16),
+            _summ(summ, fmt), _dev(page_table, "page_table", torch.int32, 2),
+            _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages, _stream(stream))
+    if fmt == SUMM_BF16:
+        st = lib.moira_append_kv(ctypes.byref(shape), *args)
+    else:
+        st = lib.moira_append_kv_ex(ctypes.byref(shape), int(fmt), *args)
+    _check(st, "moira_append_kv")
 
 
 def select(shape: Shape, q, summ, page_table, seq_lens, gamma: float, sm_scale: float, lists,
@@ -214,6 +263,21 @@ def select_rule(shape: Shape, q, summ, page_table, seq_lens, rule: int, param: f
            "moira_select_rule")
 
 
+def select_ex(shape: Shape, fmt: int, q, summ, page_table, seq_lens, rule: int, param: float,
+              sm_scale: float, lists, lengths, ws, stream=None):
+    """select_rule reading summaries in format `fmt` (SUMM_BF16 / SUMM_Q8 /
+    SUMM_Q2); see include/moira.h."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    _check(lib.moira_select_ex(ctypes.byref(shape), int(fmt), _dev(q, "q", torch.bfloat16),
+                               _summ(summ, fmt), _dev(page_table, "page_table", torch.int32, 2),
+                               _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                               int(rule), float(param), float(sm_scale),
+                               _dev(lists, "lists", torch.int32), _dev(lengths, "lengths", torch.int32),
+                               _dev(ws, "workspace", torch.uint8), ws.numel(), _stream(stream)),
+           "moira_select_ex")
+
+
 def attend(shape: Shape, q, k_pool, v_pool, lists, lengths, seq_lens, max_pages: int,
            sm_scale: float, out, ws, stream=None):
     """Attention of one layer over the listed pages; writes fp32 ``out``."""
@@ -245,6 +309,27 @@ def decode_step(shape: Shape, q_all, k_pool_all, v_pool_all, summ_all, page_tabl
                                  _dev(out_all, "out_all", torch.float32),
                                  _dev(ws, "workspace", torch.uint8), ws.numel(), _stream(stream)),
            "moira_decode_step")
+
+
+def decode_step_ex(shape: Shape, fmt: int, q_all, k_pool_all, v_pool_all, summ_all, page_table,
+                   seq_lens, rule: int, param: float, sm_scale: float, lists, lengths_all, out_all,
+                   ws, stream=None):
+    """decode_step with summaries in format `fmt` and any page rule."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    _check(lib.moira_decode_step_ex(ctypes.byref(shape), int(fmt), q_all.shape[0],
+                                    _dev(q_all, "q_all", torch.bfloat16),
+                                    _dev(k_pool_all, "k_pool_all", torch.bfloat16),
+                                    _dev(v_pool_all, "v_pool_all", torch.bfloat16),
+                                    _summ(summ_all, fmt),
+                                    _dev(page_table, "page_table", torch.int32, 2),
+                                    _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                                    int(rule), float(param), float(sm_scale),
+                                    _dev(lists, "lists", torch.int32),
+                                    _dev(lengths_all, "lengths_all", torch.int32),
+                                    _dev(out_all, "out_all", torch.float32),
+                                    _dev(ws, "workspace", torch.uint8), ws.numel(), _stream(stream)),
+           "moira_decode_step_ex")
 
 
 def decode_step_host(shape: Shape, q_host, q_dev, k_pool_all, v_pool_all, summ_all, page_table,

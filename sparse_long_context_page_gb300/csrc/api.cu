@@ -99,7 +99,7 @@ bool make_pool_map(CUtensorMap *map, const void *pool, const moira_shape *s)
 
 moira_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOIRA_OK : MOIRA_ECUDA; }
 
-moira_status select_impl(const moira_shape *shape, const void *q, const void *summ,
+moira_status select_impl(const moira_shape *shape, int32_t fmt, const void *q, const void *summ,
                          const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
                          int32_t max_pages, int32_t rule, float param, float sm_scale,
                          int32_t *lists, int32_t *lengths, void *ws, size_t ws_bytes,
@@ -108,6 +108,8 @@ moira_status select_impl(const moira_shape *shape, const void *q, const void *su
     static_assert(MOIRA_RULE_COVERAGE == kRuleCoverage && MOIRA_RULE_TOPK == kRuleTopK &&
                       MOIRA_RULE_TOPDELTA == kRuleTopDelta,
                   "public rule values match the kernels'");
+    static_assert(MOIRA_SUMM_BF16 == kSummBf16 && MOIRA_SUMM_Q8 == kSummQ8 && MOIRA_SUMM_Q2 == kSummQ2,
+                  "public summary formats match the kernels'");
     const float gamma = rule == MOIRA_RULE_COVERAGE ? param : 0.5f;
     const WsLayout L = layout_for(shape, batch, max_pages);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -125,7 +127,7 @@ moira_status select_impl(const moira_shape *shape, const void *q, const void *su
     const float delta = rule == MOIRA_RULE_TOPDELTA ? param : 0.f;
     if (!dense) {
         const float scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
-        cudaError_t e = launch_score(q, summ, page_table, seq_lens, batch, shape->num_q_heads,
+        cudaError_t e = launch_score(q, summ, fmt, page_table, seq_lens, batch, shape->num_q_heads,
                                      shape->num_kv_heads, max_pages, shape->num_phys_pages,
                                      scale_log2, scores, chunks, status, stream);
         if (e != cudaSuccess) return MOIRA_ECUDA;
@@ -166,6 +168,25 @@ moira_status attend_impl(const moira_shape *shape, const void *q, const void *k_
 
 bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
 
+bool valid_format(int32_t fmt)
+{
+    return fmt == MOIRA_SUMM_BF16 || fmt == MOIRA_SUMM_Q8 || fmt == MOIRA_SUMM_Q2;
+}
+
+// The range of each rule's parameter (moira_rule).
+bool valid_rule(int32_t rule, float param)
+{
+    switch (rule) {
+    case MOIRA_RULE_COVERAGE:
+    case MOIRA_RULE_TOPDELTA:
+        return param > 0.f && param <= 1.f;
+    case MOIRA_RULE_TOPK:
+        return param >= 0.f && param <= 16777216.f && param == std::floor(param);
+    default:
+        return false;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -183,19 +204,52 @@ moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream
     return cuda_status(cudaMemsetAsync(workspace, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool, void *summ,
-                                    const int32_t *phys_pages, int32_t n, moira_stream_t stream)
+size_t moira_summary_page_bytes(const moira_shape *shape, int32_t format)
+{
+    if (check_shape(shape) != MOIRA_OK || !valid_format(format)) return 0;
+    return static_cast<size_t>(summ_page_bytes(format, shape->num_kv_heads));
+}
+
+moira_status moira_update_summaries_ex(const moira_shape *shape, int32_t format, const void *k_pool,
+                                       void *summ, const int32_t *phys_pages, int32_t n,
+                                       moira_stream_t stream)
 {
     moira_status st = check_shape(shape);
     if (st != MOIRA_OK) return st;
+    if (!valid_format(format)) return MOIRA_EINVAL;
     if (n < 0 || (n > 0 && (!k_pool || !summ || !phys_pages))) return MOIRA_EINVAL;
     if (n == 0) return MOIRA_OK;
     if (!aligned16(k_pool) || !aligned16(summ)) return MOIRA_EINVAL;
     // This call takes no workspace, so there is no status word: page ids out
     // of range are skipped without a record (select and attend flag them).
     return cuda_status(launch_summarize(k_pool, summ, phys_pages, n, shape->num_kv_heads,
-                                        shape->num_phys_pages, nullptr,
+                                        shape->num_phys_pages, format, nullptr,
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool, void *summ,
+                                    const int32_t *phys_pages, int32_t n, moira_stream_t stream)
+{
+    return moira_update_summaries_ex(shape, MOIRA_SUMM_BF16, k_pool, summ, phys_pages, n, stream);
+}
+
+moira_status moira_append_kv_ex(const moira_shape *shape, int32_t format, const void *k_new,
+                                const void *v_new, void *k_pool, void *v_pool, void *summ,
+                                const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                                int32_t max_pages, moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (!valid_format(format)) return MOIRA_EINVAL;
+    if (!k_new || !v_new || !k_pool || !v_pool || !summ || !page_table || !seq_lens)
+        return MOIRA_EINVAL;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        !aligned16(summ))
+        return MOIRA_EINVAL;
+    return cuda_status(launch_append(k_new, v_new, k_pool, v_pool, summ, page_table, seq_lens,
+                                     batch, shape->num_kv_heads, max_pages, shape->num_phys_pages,
+                                     format, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moira_status moira_append_kv(const moira_shape *shape, const void *k_new, const void *v_new,
@@ -203,17 +257,27 @@ moira_status moira_append_kv(const moira_shape *shape, const void *k_new, const 
                              const int32_t *seq_lens, int32_t batch, int32_t max_pages,
                              moira_stream_t stream)
 {
+    return moira_append_kv_ex(shape, MOIRA_SUMM_BF16, k_new, v_new, k_pool, v_pool, summ,
+                              page_table, seq_lens, batch, max_pages, stream);
+}
+
+moira_status moira_select_ex(const moira_shape *shape, int32_t format, const void *q,
+                             const void *summ, const int32_t *page_table, const int32_t *seq_lens,
+                             int32_t batch, int32_t max_pages, int32_t rule, float param,
+                             float sm_scale, int32_t *lists, int32_t *lengths, void *workspace,
+                             size_t ws_bytes, moira_stream_t stream)
+{
     moira_status st = check_shape(shape);
     if (st != MOIRA_OK) return st;
     if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
-    if (!k_new || !v_new || !k_pool || !v_pool || !summ || !page_table || !seq_lens)
+    if (!valid_format(format) || !valid_rule(rule, param) || !finite_pos(sm_scale))
         return MOIRA_EINVAL;
-    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
-        !aligned16(summ))
-        return MOIRA_EINVAL;
-    return cuda_status(launch_append(k_new, v_new, k_pool, v_pool, summ, page_table, seq_lens,
-                                     batch, shape->num_kv_heads, max_pages,
-                                     shape->num_phys_pages, reinterpret_cast<cudaStream_t>(stream)));
+    if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
+    if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
+    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
+    return select_impl(shape, format, q, summ, page_table, seq_lens, batch, max_pages, rule, param,
+                       sm_scale, lists, lengths, workspace, ws_bytes,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 moira_status moira_select(const moira_shape *shape, const void *q, const void *summ,
@@ -221,16 +285,9 @@ moira_status moira_select(const moira_shape *shape, const void *q, const void *s
                           int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
                           int32_t *lengths, void *workspace, size_t ws_bytes, moira_stream_t stream)
 {
-    moira_status st = check_shape(shape);
-    if (st != MOIRA_OK) return st;
-    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
-    if (!(gamma > 0.f && gamma <= 1.f) || !finite_pos(sm_scale)) return MOIRA_EINVAL;
-    if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
-    if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
-    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
-    return select_impl(shape, q, summ, page_table, seq_lens, batch, max_pages,
-                       MOIRA_RULE_COVERAGE, gamma, sm_scale, lists, lengths, workspace, ws_bytes,
-                       reinterpret_cast<cudaStream_t>(stream));
+    return moira_select_ex(shape, MOIRA_SUMM_BF16, q, summ, page_table, seq_lens, batch, max_pages,
+                           MOIRA_RULE_COVERAGE, gamma, sm_scale, lists, lengths, workspace,
+                           ws_bytes, stream);
 }
 
 moira_status moira_select_rule(const moira_shape *shape, const void *q, const void *summ,
@@ -239,29 +296,8 @@ moira_status moira_select_rule(const moira_shape *shape, const void *q, const vo
                                int32_t *lists, int32_t *lengths, void *workspace, size_t ws_bytes,
                                moira_stream_t stream)
 {
-    moira_status st = check_shape(shape);
-    if (st != MOIRA_OK) return st;
-    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
-    if (!finite_pos(sm_scale)) return MOIRA_EINVAL;
-    switch (rule) {
-    case MOIRA_RULE_COVERAGE:
-        if (!(param > 0.f && param <= 1.f)) return MOIRA_EINVAL;
-        break;
-    case MOIRA_RULE_TOPK:
-        if (!(param >= 0.f && param <= 16777216.f) || param != std::floor(param)) return MOIRA_EINVAL;
-        break;
-    case MOIRA_RULE_TOPDELTA:
-        if (!(param > 0.f && param <= 1.f)) return MOIRA_EINVAL;
-        break;
-    default:
-        return MOIRA_EINVAL;
-    }
-    if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
-    if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
-    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
-    return select_impl(shape, q, summ, page_table, seq_lens, batch, max_pages, rule, param,
-                       sm_scale, lists, lengths, workspace, ws_bytes,
-                       reinterpret_cast<cudaStream_t>(stream));
+    return moira_select_ex(shape, MOIRA_SUMM_BF16, q, summ, page_table, seq_lens, batch, max_pages,
+                           rule, param, sm_scale, lists, lengths, workspace, ws_bytes, stream);
 }
 
 moira_status moira_attend(const moira_shape *shape, const void *q, const void *k_pool,
@@ -282,19 +318,21 @@ moira_status moira_attend(const moira_shape *shape, const void *q, const void *k
                        sm_scale, out, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
-moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, const void *q_all,
-                               const void *k_pool_all, const void *v_pool_all,
-                               const void *summ_all, const int32_t *page_table,
-                               const int32_t *seq_lens, int32_t batch, int32_t max_pages,
-                               float gamma, float sm_scale, int32_t *lists, int32_t *lengths_all,
-                               float *out_all, void *workspace, size_t ws_bytes,
-                               moira_stream_t stream)
+moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int32_t num_layers,
+                                  const void *q_all, const void *k_pool_all,
+                                  const void *v_pool_all, const void *summ_all,
+                                  const int32_t *page_table, const int32_t *seq_lens,
+                                  int32_t batch, int32_t max_pages, int32_t rule, float param,
+                                  float sm_scale, int32_t *lists, int32_t *lengths_all,
+                                  float *out_all, void *workspace, size_t ws_bytes,
+                                  moira_stream_t stream)
 {
     moira_status st = check_shape(shape);
     if (st != MOIRA_OK) return st;
     if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
     if (num_layers <= 0) return MOIRA_EINVAL;
-    if (!(gamma > 0.f && gamma <= 1.f) || !finite_pos(sm_scale)) return MOIRA_EINVAL;
+    if (!valid_format(format) || !valid_rule(rule, param) || !finite_pos(sm_scale))
+        return MOIRA_EINVAL;
     if (!q_all || !k_pool_all || !v_pool_all || !summ_all || !page_table || !seq_lens || !lists ||
         !lengths_all || !out_all)
         return MOIRA_EINVAL;
@@ -306,15 +344,16 @@ moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, con
     const size_t d = kHeadDim;
     const size_t q_layer = static_cast<size_t>(batch) * shape->num_q_heads * d;      // elements
     const size_t kv_layer = static_cast<size_t>(shape->num_phys_pages) * shape->num_kv_heads * kPageSize * d;
-    const size_t sm_layer = static_cast<size_t>(shape->num_phys_pages) * shape->num_kv_heads * d;
+    const size_t sm_layer = static_cast<size_t>(shape->num_phys_pages) *
+                            summ_page_bytes(format, shape->num_kv_heads);            // bytes
     const size_t len_layer = static_cast<size_t>(batch) * shape->num_kv_heads;
     const uint16_t *q = static_cast<const uint16_t *>(q_all);
     const uint16_t *kp = static_cast<const uint16_t *>(k_pool_all);
     const uint16_t *vp = static_cast<const uint16_t *>(v_pool_all);
-    const uint16_t *sp = static_cast<const uint16_t *>(summ_all);
+    const uint8_t *sp = static_cast<const uint8_t *>(summ_all);
     for (int l = 0; l < num_layers; ++l) {
-        st = select_impl(shape, q + l * q_layer, sp + l * sm_layer, page_table, seq_lens, batch,
-                         max_pages, MOIRA_RULE_COVERAGE, gamma, sm_scale, lists,
+        st = select_impl(shape, format, q + l * q_layer, sp + l * sm_layer, page_table, seq_lens,
+                         batch, max_pages, rule, param, sm_scale, lists,
                          lengths_all + l * len_layer, workspace, ws_bytes, s);
         if (st != MOIRA_OK) return st;
         st = attend_impl(shape, q + l * q_layer, kp + l * kv_layer, vp + l * kv_layer, lists,
@@ -323,6 +362,20 @@ moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, con
         if (st != MOIRA_OK) return st;
     }
     return MOIRA_OK;
+}
+
+moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, const void *q_all,
+                               const void *k_pool_all, const void *v_pool_all,
+                               const void *summ_all, const int32_t *page_table,
+                               const int32_t *seq_lens, int32_t batch, int32_t max_pages,
+                               float gamma, float sm_scale, int32_t *lists, int32_t *lengths_all,
+                               float *out_all, void *workspace, size_t ws_bytes,
+                               moira_stream_t stream)
+{
+    return moira_decode_step_ex(shape, MOIRA_SUMM_BF16, num_layers, q_all, k_pool_all, v_pool_all,
+                                summ_all, page_table, seq_lens, batch, max_pages,
+                                MOIRA_RULE_COVERAGE, gamma, sm_scale, lists, lengths_all, out_all,
+                                workspace, ws_bytes, stream);
 }
 
 moira_status moira_decode_step_host(const moira_shape *shape, int32_t num_layers,

@@ -19,6 +19,31 @@ constexpr uint32_t kDevBadPage = 0x1u;
 constexpr uint32_t kDevBadLen = 0x2u;
 constexpr uint32_t kDevTimeout = 0x4u;
 
+// ---- page-summary formats ----------------------------------------------------
+// kSummBf16 : bf16 [P][Hkv][d], the mean key rounded to bf16.
+// kSummQ8 / kSummQ2 : one record per physical page, the mean key in 8 or 2
+//   bits per element (symmetric mid-rise: value = (code + 1/2) * step):
+//     bytes [0, Hkv*cb)              codes, head j at [j*cb, (j+1)*cb),
+//                                    cb = d * bits / 8; Q8: byte i = int8 code
+//                                    of element i; Q2: element i in bits
+//                                    2*(i%4) .. 2*(i%4)+1 of byte i/4, holding
+//                                    code + 2 (0..3)
+//     bytes [Hkv*cb, Hkv*cb + 4*Hkv) fp32 step of each head
+//     then zeros up to a multiple of 16 bytes
+constexpr int kSummBf16 = 0;
+constexpr int kSummQ8 = 1;
+constexpr int kSummQ2 = 2;
+
+__host__ __device__ constexpr int summ_bits(int fmt) { return fmt == kSummQ8 ? 8 : (fmt == kSummQ2 ? 2 : 16); }
+__host__ __device__ constexpr int lowbit_code_bytes(int bits) { return kHeadDim * bits / 8; }
+__host__ __device__ constexpr int lowbit_step_bytes(int hkv) { return (hkv * 4 + 15) / 16 * 16; }
+// Bytes of one physical page's summaries (all KV heads).
+__host__ __device__ constexpr int summ_page_bytes(int fmt, int hkv)
+{
+    return fmt == kSummBf16 ? hkv * kHeadDim * 2
+                            : hkv * lowbit_code_bytes(summ_bits(fmt)) + lowbit_step_bytes(hkv);
+}
+
 // A bounded device wait gives up after this long (ns of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

@@ -9,15 +9,17 @@
 
 namespace moira {
 
+// `fmt` is a summary format (kSummBf16 / kSummQ8 / kSummQ2, moira_device.cuh).
 cudaError_t launch_summarize(const void *k_pool, void *summ, const int32_t *phys_pages, int n,
-                             int hkv, long long num_pages, uint32_t *status, cudaStream_t stream);
+                             int hkv, long long num_pages, int fmt, uint32_t *status,
+                             cudaStream_t stream);
 
 cudaError_t launch_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool,
                           void *summ, const int32_t *page_table, const int32_t *seq_lens,
-                          int batch, int hkv, int max_pages, long long num_pages,
+                          int batch, int hkv, int max_pages, long long num_pages, int fmt,
                           cudaStream_t stream);
 
-cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_table,
+cudaError_t launch_score(const void *q, const void *summ, int fmt, const int32_t *page_table,
                          const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
                          long long num_pages, float scale_log2, float *scores, float *chunks,
                          uint32_t *status, cudaStream_t stream);

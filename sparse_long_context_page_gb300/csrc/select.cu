@@ -36,6 +36,44 @@ constexpr int kScoreThreads = 256;        // 8 warps: one (KV head, 16-page half
 constexpr int kScoreHeads = 4;            // KV heads per block; blockIdx.z picks the slice
 static_assert(kScoreHeads * 2 <= kScoreThreads / 32, "one (KV head, 16-page half) item per warp");
 
+// Per query head of a score block: chunk max, chunk sum and the chunk-
+// relative weights from the block's logits s_s[local head][page] (log2
+// domain, -inf for pages that do not count); 8 lanes per head (4 pages
+// each), 4 heads per warp instruction.
+__device__ __forceinline__ void score_chunk_stats(const float *s_s, int nh, int jb, int r, int chunk,
+                                                  int p0, int hq, int ld, int ldc,
+                                                  float *__restrict__ weights,
+                                                  float *__restrict__ chunks)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hql = nh * kGroup;
+    for (int h0 = warp * 4; h0 < hql; h0 += 4 * (kScoreThreads / 32)) {
+        const int hl = h0 + (lane >> 3);
+        const int sub = lane & 7;
+        float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        if (hl < hql) v = *reinterpret_cast<const float4 *>(&s_s[hl * kScoreChunk + sub * 4]);
+        float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        const float ms = mx == -INFINITY ? 0.f : mx;
+        const float4 e = make_float4(exp2f(v.x - ms), exp2f(v.y - ms), exp2f(v.z - ms), exp2f(v.w - ms));
+        float sum = (e.x + e.y) + (e.z + e.w);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if (hl < hql) {
+            const int h = jb * kGroup + hl;
+            float *dst = weights + (static_cast<size_t>(r) * hq + h) * ld + p0 + sub * 4;
+            *reinterpret_cast<float4 *>(dst) = e;          // pages past F are never read
+            if (sub == 0) {
+                float *c = chunks + (static_cast<size_t>(r) * hq + h) * ldc + chunk * 2;
+                *reinterpret_cast<float2 *>(c) = make_float2(mx, sum);
+            }
+        }
+    }
+}
+
 // One block scores kScoreChunk (32) consecutive full pages of one request for
 // kScoreHeads KV heads (Hkv = 8 takes two blocks per chunk, so about four
 // blocks share an SM and one block's loads overlap another's arithmetic).
@@ -138,34 +176,158 @@ __global__ void __launch_bounds__(kScoreThreads, 4) k_score(
         }
     }
     __syncthreads();
-    // per query head of the block: chunk max, chunk sum and the chunk-relative
-    // weights; 8 lanes per head (4 pages each), 4 heads per warp instruction
-    const int hql = nh * kGroup;
-    for (int h0 = warp * 4; h0 < hql; h0 += 4 * (kScoreThreads / 32)) {
-        const int hl = h0 + (lane >> 3);
-        const int sub = lane & 7;
-        float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        if (hl < hql) v = *reinterpret_cast<const float4 *>(&s_s[hl * kScoreChunk + sub * 4]);
-        float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        const float ms = mx == -INFINITY ? 0.f : mx;
-        const float4 e = make_float4(exp2f(v.x - ms), exp2f(v.y - ms), exp2f(v.z - ms), exp2f(v.w - ms));
-        float sum = (e.x + e.y) + (e.z + e.w);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        if (hl < hql) {
-            const int h = jb * kGroup + hl;
-            float *dst = weights + (static_cast<size_t>(r) * hq + h) * ld + p0 + sub * 4;
-            *reinterpret_cast<float4 *>(dst) = e;          // pages past F are never read
-            if (sub == 0) {
-                float *c = chunks + (static_cast<size_t>(r) * hq + h) * ldc + chunk * 2;
-                *reinterpret_cast<float2 *>(c) = make_float2(mx, sum);
+    score_chunk_stats(s_s, nh, jb, r, chunk, p0, hq, ld, ldc, weights, chunks);
+}
+
+
+// bf16 pair {lo, hi} (lo in the low half) from two exactly representable floats.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Mid-rise level c + 1/2 of two 8-bit codes (the low 16 bits of v), as a bf16
+// pair: |2c + 1| <= 255 has at most 8 significant bits, so it is exact.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t v)
+{
+    return pack_bf16x2(static_cast<float>(static_cast<int8_t>(v & 0xFFu)) + 0.5f,
+                       static_cast<float>(static_cast<int8_t>((v >> 8) & 0xFFu)) + 0.5f);
+}
+
+// Mid-rise level of two 2-bit codes (the low nibble of v, stored as code + 2):
+// u - 3/2 for u in 0..3.
+__device__ __forceinline__ uint32_t q2_pair(uint32_t v)
+{
+    return pack_bf16x2(static_cast<float>(v & 3u) - 1.5f, static_cast<float>((v >> 2) & 3u) - 1.5f);
+}
+
+// Shared-memory stride of one page slot of k_score_lowbit: the block's codes
+// and the page's step row, padded so that the lanes of one load phase (8
+// lanes of 16-byte loads for Q8, 16 lanes of 8-byte loads for Q2) hit
+// distinct banks.
+__host__ __device__ constexpr int score_lowbit_stride(int bits, int nh, int hkv)
+{
+    return (nh * lowbit_code_bytes(bits) + lowbit_step_bytes(hkv) + 127) / 128 * 128 + (bits == 8 ? 16 : 32);
+}
+
+// k_score for low-bit summaries (8 or 2 bits, mid-rise: value = (code + 1/2)
+// * step): the same blocks, logits and outputs.  Per listed page two bulk
+// copies bring the block's code bytes (nh * cb) and the page's step row
+// (Hkv fp32).  Codes feed the B fragments of mma.m16n8k16 directly: at
+// k-step s lane t of a quad holds elements 32t + 4s .. 32t + 4s + 3 (a
+// permutation of the contraction index, applied to the query fragments
+// as well), so a lane reads one 32-byte (Q8) or 8-byte (Q2) run per page and
+// turns each code into the bf16 level c + 1/2.  The logit of page p for
+// query head h is step_p * (q_h . (c_p + 1/2)), times the score scale.
+template <int kBits>
+__global__ void __launch_bounds__(kScoreThreads, 4) k_score_lowbit(
+    const uint16_t *__restrict__ q, const uint8_t *__restrict__ summ,
+    const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
+    int max_pages, int ld, long long num_pages, float scale_log2, float *__restrict__ weights,
+    float *__restrict__ chunks, int ldc, uint32_t *status)
+{
+    constexpr int kCb = lowbit_code_bytes(kBits);
+    extern __shared__ __align__(128) uint8_t s_summ[];     // [32 pages][stride]
+    __shared__ __align__(16) float s_s[kScoreHeads * kGroup * kScoreChunk];
+    __shared__ int s_phys[kScoreChunk];
+    __shared__ __align__(8) unsigned long long s_bar;
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.y;
+    const int chunk = blockIdx.x;
+    const int nh = min(hkv, kScoreHeads);
+    const int jb = blockIdx.z * nh;
+    const int p0 = chunk * kScoreChunk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t code_bytes = static_cast<uint32_t>(nh) * kCb;
+    const uint32_t step_bytes = static_cast<uint32_t>(lowbit_step_bytes(hkv));
+    const uint32_t stride = static_cast<uint32_t>(score_lowbit_stride(kBits, nh, hkv));
+    const size_t rec = static_cast<size_t>(hkv) * kCb + step_bytes;
+    const uint32_t bar = smem_u32(&s_bar);
+    const int hrow = (lane >> 2) & 3;
+    const int t = lane & 3;
+    const bool has_item = warp < nh * 2;
+    const int jl = warp >> 1, half = warp & 1;
+
+    int L = seq_lens[r];
+    const int pid_pre = (threadIdx.x < kScoreChunk && p0 + static_cast<int>(threadIdx.x) < max_pages)
+                            ? __ldg(page_table + static_cast<size_t>(r) * max_pages + p0 + threadIdx.x)
+                            : -1;
+    uint32_t aq[8][2];
+    {
+        const int j = jb + (has_item ? jl : 0);
+        const uint16_t *qrow = q + (static_cast<size_t>(r) * hq + j * kGroup + hrow) * kHeadDim + 32 * t;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            aq[ks][0] = has_item ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 4 * ks)) : 0u;
+            aq[ks][1] = has_item ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 4 * ks + 2)) : 0u;
+        }
+    }
+    L = L < 0 ? 0 : (L > max_pages * kPageSize ? max_pages * kPageSize : L);
+    const int F = L / kPageSize;
+    if (p0 >= F) return;
+    const int np = min(kScoreChunk, F - p0);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    if (threadIdx.x < kScoreChunk) s_phys[threadIdx.x] = static_cast<int>(threadIdx.x) < np ? pid_pre : -1;
+    __syncthreads();
+    if (warp == 0) {
+        const int phys = s_phys[lane];
+        const bool ok = lane < np && phys >= 0 && phys < num_pages;
+        const unsigned okm = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) mbar_arrive_expect_tx(bar, __popc(okm) * (code_bytes + step_bytes));
+        __syncwarp();
+        if (ok) {
+            const uint8_t *src = summ + static_cast<size_t>(phys) * rec;
+            bulk_load(smem_u32(s_summ + lane * stride), src + jb * kCb, code_bytes, bar);
+            bulk_load(smem_u32(s_summ + lane * stride + code_bytes), src + hkv * kCb, step_bytes, bar);
+        }
+        if (lane < np && !ok && blockIdx.z == 0) raise_status(status, kDevBadPage);
+    }
+    if (!mbar_wait(bar, 0) && threadIdx.x == 0) raise_status(status, kDevTimeout);
+
+    if (has_item) {                                          // warp-uniform
+        float acc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            const uint8_t *src = s_summ + (half * 16 + nt * 8 + (lane >> 2)) * stride + jl * kCb + t * (kCb / 4);
+            if constexpr (kBits == 8) {
+                const uint4 x0 = *reinterpret_cast<const uint4 *>(src);
+                const uint4 x1 = *reinterpret_cast<const uint4 *>(src + 16);
+                const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_16816(acc[nt], aq[ks][0], 0u, aq[ks][1], 0u, q8_pair(w[ks]), q8_pair(w[ks] >> 16));
+            } else {
+                const uint2 x = *reinterpret_cast<const uint2 *>(src);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t b = ((ks < 4 ? x.x : x.y) >> (8 * (ks & 3))) & 0xFFu;
+                    mma_bf16_16816(acc[nt], aq[ks][0], 0u, aq[ks][1], 0u, q2_pair(b), q2_pair(b >> 4));
+                }
+            }
+        }
+        if (lane < 16) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int pl = half * 16 + nt * 8 + 2 * t;
+                const int hl = jl * kGroup + hrow;
+                const float st0 = reinterpret_cast<const float *>(s_summ + pl * stride + code_bytes)[jb + jl];
+                const float st1 = reinterpret_cast<const float *>(s_summ + (pl + 1) * stride + code_bytes)[jb + jl];
+                float s0 = acc[nt][0] * st0 * scale_log2, s1 = acc[nt][1] * st1 * scale_log2;
+                if (pl >= np || s_phys[pl] < 0 || s_phys[pl] >= num_pages) s0 = -INFINITY;
+                if (pl + 1 >= np || s_phys[pl + 1] < 0 || s_phys[pl + 1] >= num_pages) s1 = -INFINITY;
+                *reinterpret_cast<float2 *>(&s_s[hl * kScoreChunk + pl]) = make_float2(s0, s1);
             }
         }
     }
+    __syncthreads();
+    score_chunk_stats(s_s, nh, jb, r, chunk, p0, hq, ld, ldc, weights, chunks);
 }
 
 // ---------------------------------------------------------------------------
@@ -736,7 +898,7 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
 }
 
 // ---------------------------------------------------------------------------
-cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_table,
+cudaError_t launch_score(const void *q, const void *summ, int fmt, const int32_t *page_table,
                          const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
                          long long num_pages, float scale_log2, float *weights, float *chunks,
                          uint32_t *status, cudaStream_t stream)
@@ -744,6 +906,18 @@ cudaError_t launch_score(const void *q, const void *summ, const int32_t *page_ta
     const int n_chunks = (max_pages + kScoreChunk - 1) / kScoreChunk;
     const int nh = hkv < kScoreHeads ? hkv : kScoreHeads;
     dim3 grid(n_chunks, batch, hkv / nh);
+    if (fmt == kSummQ8 || fmt == kSummQ2) {
+        const int bits = summ_bits(fmt);
+        const size_t smem = static_cast<size_t>(kScoreChunk) * score_lowbit_stride(bits, nh, hkv);
+        auto kernel = fmt == kSummQ8 ? k_score_lowbit<8> : k_score_lowbit<2>;
+        static std::atomic<int> seen8[64], seen2[64];
+        cudaError_t e = raise_smem_limit(kernel, smem, fmt == kSummQ8 ? seen8 : seen2);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(kernel, grid, dim3(kScoreThreads), smem, stream,
+                          static_cast<const uint16_t *>(q), static_cast<const uint8_t *>(summ),
+                          page_table, seq_lens, hq, hkv, max_pages, weights_ld(max_pages), num_pages,
+                          scale_log2, weights, chunks, chunks_ld(max_pages), status);
+    }
     const size_t smem = static_cast<size_t>(kScoreChunk) * (nh * kHeadDim * 2 + 16);
     static std::atomic<int> seen[64];
     cudaError_t e = raise_smem_limit(k_score, smem, seen);

@@ -9,6 +9,15 @@
 // The 16 keys are summed in fp64 (exact for bf16 inputs of moderate range)
 // and the mean is rounded once to bf16, ties to even.  This runs when a page
 // fills, outside the decode step, so fp64 throughput does not matter here.
+//
+// Low-bit formats store the same fp64 mean in 8 or 2 bits per element with
+// the symmetric mid-rise quantiser that "Faster Flash Decoding", section 3.1,
+// uses for its low-bit key thumbnails: one fp32 step per (page, KV head),
+//   step = max_i |mean_i| / (2^(bits-1) - 1/2)   (fp64, rounded once to fp32)
+//   code = floor(mean_i / step), clamped to [-2^(bits-1), 2^(bits-1) - 1]
+// standing for (code + 1/2) * step; no zero level, so signs survive.  A
+// non-finite mean element, a zero mean or a step that rounds to 0 gives
+// step 0 and codes 0.
 #include "moira_device.cuh"
 #include "moira_launch.h"
 
@@ -36,6 +45,67 @@ __device__ __forceinline__ uint32_t f64_to_bf16_rne(double x)
     return sign | static_cast<uint32_t>(grid);
 }
 
+// fp64 sums over the page's 16 tokens of this thread's two dimensions
+// (2*tid, 2*tid+1), in token order; `src` points at the thread's word of
+// token 0.
+__device__ __forceinline__ void token_sums(const uint32_t *src, double &lo, double &hi)
+{
+    lo = 0.0;
+    hi = 0.0;
+#pragma unroll
+    for (int t = 0; t < kPageSize; ++t) {
+        const uint32_t v = __ldg(src + t * (kHeadDim / 2));
+        lo += static_cast<double>(bf16_lo(v));
+        hi += static_cast<double>(bf16_hi(v));
+    }
+}
+
+// Write the low-bit summary of KV head j of one page into its record `rec`
+// from this thread's two fp64 means (dimensions 2*tid, 2*tid+1).  Called by
+// all 64 threads of the block (it synchronises them); head 0's block also
+// zeroes the record's padding.
+template <int kBits>
+__device__ void store_lowbit(double lo, double hi, uint8_t *rec, int j, int hkv)
+{
+    __shared__ double s_a[2];
+    __shared__ int s_bad[2];
+    constexpr int kCb = lowbit_code_bytes(kBits);
+    constexpr double kHalf = static_cast<double>(1 << (kBits - 1));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool bad = !isfinite(lo) || !isfinite(hi);
+    double a = bad ? 0.0 : fmax(fabs(lo), fabs(hi));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) a = fmax(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        s_a[warp] = a;
+        s_bad[warp] = any_bad;
+    }
+    __syncthreads();
+    a = fmax(s_a[0], s_a[1]);
+    const float step = (s_bad[0] | s_bad[1]) ? 0.f : __double2float_rn(a / (kHalf - 0.5));
+    int c0 = 0, c1 = 0;
+    if (step > 0.f) {
+        c0 = static_cast<int>(fmin(fmax(floor(lo / static_cast<double>(step)), -kHalf), kHalf - 1.0));
+        c1 = static_cast<int>(fmin(fmax(floor(hi / static_cast<double>(step)), -kHalf), kHalf - 1.0));
+    }
+    if constexpr (kBits == 8) {
+        *reinterpret_cast<uint16_t *>(rec + j * kCb + 2 * tid) =
+            static_cast<uint16_t>((c0 & 0xFF) | ((c1 & 0xFF) << 8));
+    } else {
+        // element i sits in bits 2*(i%4) of byte i/4: this thread's pair is
+        // one nibble, the low nibble for even tid
+        const uint32_t nib = static_cast<uint32_t>(c0 + 2) | (static_cast<uint32_t>(c1 + 2) << 2);
+        const uint32_t up = __shfl_down_sync(0xffffffffu, nib, 1);
+        if ((tid & 1) == 0) rec[j * kCb + (tid >> 1)] = static_cast<uint8_t>(nib | (up << 4));
+    }
+    if (tid == 0) *reinterpret_cast<float *>(rec + hkv * kCb + 4 * j) = step;
+    if (j == 0) {
+        const int pad0 = hkv * kCb + 4 * hkv, pad1 = hkv * kCb + lowbit_step_bytes(hkv);
+        if (pad0 + 4 * tid < pad1) *reinterpret_cast<uint32_t *>(rec + pad0 + 4 * tid) = 0u;
+    }
+}
+
 // One block per (listed page, KV head); 64 threads, two dimensions each.
 __global__ void __launch_bounds__(64) k_summarize(const uint32_t *__restrict__ k_pool,
                                                   uint32_t *__restrict__ summ,
@@ -51,17 +121,29 @@ __global__ void __launch_bounds__(64) k_summarize(const uint32_t *__restrict__ k
         return;
     }
     const size_t blk = (static_cast<size_t>(p) * hkv + j);
-    const uint32_t *src = k_pool + blk * (kPageSize * kHeadDim / 2) + threadIdx.x;
-    double lo = 0.0, hi = 0.0;
-#pragma unroll
-    for (int t = 0; t < kPageSize; ++t) {
-        const uint32_t v = __ldg(src + t * (kHeadDim / 2));
-        lo += static_cast<double>(bf16_lo(v));
-        hi += static_cast<double>(bf16_hi(v));
-    }
+    double lo, hi;
+    token_sums(k_pool + blk * (kPageSize * kHeadDim / 2) + threadIdx.x, lo, hi);
     const uint32_t blo = f64_to_bf16_rne(lo * (1.0 / kPageSize));
     const uint32_t bhi = f64_to_bf16_rne(hi * (1.0 / kPageSize));
     summ[blk * (kHeadDim / 2) + threadIdx.x] = blo | (bhi << 16);
+}
+
+// Low-bit summaries: one block per (listed page, KV head), 64 threads.
+template <int kBits>
+__global__ void __launch_bounds__(64) k_summarize_lowbit(const uint32_t *__restrict__ k_pool,
+                                                         uint8_t *__restrict__ summ,
+                                                         const int32_t *__restrict__ phys_pages,
+                                                         int hkv, long long num_pages, int rec_bytes)
+{
+    const int item = blockIdx.x;
+    const int j = item % hkv;
+    const int p = phys_pages[item / hkv];
+    if (p < 0 || p >= num_pages) return;                     // block-uniform
+    double lo, hi;
+    token_sums(k_pool + (static_cast<size_t>(p) * hkv + j) * (kPageSize * kHeadDim / 2) + threadIdx.x,
+               lo, hi);
+    store_lowbit<kBits>(lo * (1.0 / kPageSize), hi * (1.0 / kPageSize),
+                        summ + static_cast<size_t>(p) * rec_bytes, j, hkv);
 }
 
 // Append one token per request to a paged pool (one block per (request, KV
@@ -69,14 +151,15 @@ __global__ void __launch_bounds__(64) k_summarize(const uint32_t *__restrict__ k
 // seq_lens[r] - 1: slot (L-1) % S of logical page (L-1) / S.  When that slot
 // is the page's last, the page has just filled and its summary is computed
 // here: the 15 earlier keys are read back from the pool, the new one is
-// still in registers, and the mean is formed and rounded as in k_summarize.
+// still in registers, and the mean is formed and stored as in k_summarize
+// (or k_summarize_lowbit, by `fmt`).
 __global__ void __launch_bounds__(64) k_append(const uint32_t *__restrict__ k_new,
                                                const uint32_t *__restrict__ v_new,
                                                uint32_t *__restrict__ k_pool, uint32_t *__restrict__ v_pool,
-                                               uint32_t *__restrict__ summ,
+                                               uint8_t *__restrict__ summ,
                                                const int32_t *__restrict__ page_table,
                                                const int32_t *__restrict__ seq_lens, int hkv,
-                                               int max_pages, long long num_pages)
+                                               int max_pages, long long num_pages, int fmt)
 {
     const int r = blockIdx.x / hkv, j = blockIdx.x % hkv;
     const int L = seq_lens[r];
@@ -100,31 +183,48 @@ __global__ void __launch_bounds__(64) k_append(const uint32_t *__restrict__ k_ne
         }
         lo += static_cast<double>(bf16_lo(kn));
         hi += static_cast<double>(bf16_hi(kn));
-        const uint32_t blo = f64_to_bf16_rne(lo * (1.0 / kPageSize));
-        const uint32_t bhi = f64_to_bf16_rne(hi * (1.0 / kPageSize));
-        summ[blk * (kHeadDim / 2) + threadIdx.x] = blo | (bhi << 16);
+        lo *= 1.0 / kPageSize;
+        hi *= 1.0 / kPageSize;
+        uint8_t *rec = summ + static_cast<size_t>(p) * summ_page_bytes(fmt, hkv);
+        if (fmt == kSummQ8) {
+            store_lowbit<8>(lo, hi, rec, j, hkv);
+        } else if (fmt == kSummQ2) {
+            store_lowbit<2>(lo, hi, rec, j, hkv);
+        } else {
+            reinterpret_cast<uint32_t *>(summ)[blk * (kHeadDim / 2) + threadIdx.x] =
+                f64_to_bf16_rne(lo) | (f64_to_bf16_rne(hi) << 16);
+        }
     }
 }
 
 cudaError_t launch_append(const void *k_new, const void *v_new, void *k_pool, void *v_pool,
                           void *summ, const int32_t *page_table, const int32_t *seq_lens,
-                          int batch, int hkv, int max_pages, long long num_pages,
+                          int batch, int hkv, int max_pages, long long num_pages, int fmt,
                           cudaStream_t stream)
 {
     k_append<<<static_cast<unsigned>(batch) * hkv, 64, 0, stream>>>(
         static_cast<const uint32_t *>(k_new), static_cast<const uint32_t *>(v_new),
         static_cast<uint32_t *>(k_pool), static_cast<uint32_t *>(v_pool),
-        static_cast<uint32_t *>(summ), page_table, seq_lens, hkv, max_pages, num_pages);
+        static_cast<uint8_t *>(summ), page_table, seq_lens, hkv, max_pages, num_pages, fmt);
     return cudaGetLastError();
 }
 
 cudaError_t launch_summarize(const void *k_pool, void *summ, const int32_t *phys_pages, int n,
-                             int hkv, long long num_pages, uint32_t *status, cudaStream_t stream)
+                             int hkv, long long num_pages, int fmt, uint32_t *status,
+                             cudaStream_t stream)
 {
     if (n <= 0) return cudaSuccess;
-    k_summarize<<<static_cast<unsigned>(n) * hkv, 64, 0, stream>>>(
-        static_cast<const uint32_t *>(k_pool), static_cast<uint32_t *>(summ), phys_pages, hkv,
-        num_pages, status);
+    const unsigned grid = static_cast<unsigned>(n) * hkv;
+    const uint32_t *kp = static_cast<const uint32_t *>(k_pool);
+    if (fmt == kSummQ8)
+        k_summarize_lowbit<8><<<grid, 64, 0, stream>>>(kp, static_cast<uint8_t *>(summ), phys_pages,
+                                                       hkv, num_pages, summ_page_bytes(fmt, hkv));
+    else if (fmt == kSummQ2)
+        k_summarize_lowbit<2><<<grid, 64, 0, stream>>>(kp, static_cast<uint8_t *>(summ), phys_pages,
+                                                       hkv, num_pages, summ_page_bytes(fmt, hkv));
+    else
+        k_summarize<<<grid, 64, 0, stream>>>(kp, static_cast<uint32_t *>(summ), phys_pages, hkv,
+                                             num_pages, status);
     return cudaGetLastError();
 }
 

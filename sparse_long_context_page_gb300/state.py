@@ -13,7 +13,9 @@ from .workloads import Workload
 
 
 class DecodeState:
-    def __init__(self, w: Workload, max_pages: int | None = None):
+    """`fmt` picks the page-summary format (mb.SUMM_BF16 / SUMM_Q8 / SUMM_Q2)."""
+
+    def __init__(self, w: Workload, max_pages: int | None = None, fmt: int = mb.SUMM_BF16):
         sp = w.spec
         dev = w.q.device
         self.w = w
@@ -26,8 +28,8 @@ class DecodeState:
         pt[:, :w.max_pages] = torch.from_numpy(w.page_table)
         self.page_table = pt.to(dev)
         self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
-        self.summ = torch.zeros((sp.layers, w.num_phys_pages, sp.kv_heads, sp.head_dim),
-                                dtype=torch.bfloat16, device=dev)
+        self.fmt = fmt
+        self.summ = mb.make_summaries(self.shape, fmt, layers=sp.layers, device=dev)
         self.lists = torch.zeros((sp.batch, sp.kv_heads, self.max_pages), dtype=torch.int32, device=dev)
         self.lengths = torch.zeros((sp.layers, sp.batch, sp.kv_heads), dtype=torch.int32, device=dev)
         self.out = torch.zeros((sp.layers, sp.batch, sp.q_heads, sp.head_dim), dtype=torch.float32,
@@ -38,13 +40,18 @@ class DecodeState:
         """Summaries of every physical page of every layer (after prefill)."""
         pages = torch.arange(self.w.num_phys_pages, dtype=torch.int32, device=self.device)
         for l in range(self.layers):
-            mb.update_summaries(self.shape, self.w.k_pool[l], self.summ[l], pages)
+            mb.update_summaries(self.shape, self.w.k_pool[l], self.summ[l], pages, fmt=self.fmt)
 
     def step(self, gamma: float):
         """One decode-attention step over all layers (select + attend per layer)."""
-        mb.decode_step(self.shape, self.w.q, self.w.k_pool, self.w.v_pool, self.summ,
-                       self.page_table, self.seq_lens, gamma, self.sm_scale, self.lists,
-                       self.lengths, self.out, self.ws)
+        if self.fmt == mb.SUMM_BF16:
+            mb.decode_step(self.shape, self.w.q, self.w.k_pool, self.w.v_pool, self.summ,
+                           self.page_table, self.seq_lens, gamma, self.sm_scale, self.lists,
+                           self.lengths, self.out, self.ws)
+        else:
+            mb.decode_step_ex(self.shape, self.fmt, self.w.q, self.w.k_pool, self.w.v_pool,
+                              self.summ, self.page_table, self.seq_lens, mb.RULE_COVERAGE, gamma,
+                              self.sm_scale, self.lists, self.lengths, self.out, self.ws)
 
     def step_rule(self, rule: int, param: float):
         """One decode-attention step under a page rule: per layer moira_select_rule
@@ -56,15 +63,23 @@ class DecodeState:
     def select_layer(self, l: int, gamma: float, lists=None, lengths=None):
         lists = self.lists if lists is None else lists
         lengths = self.lengths[l] if lengths is None else lengths
-        mb.select(self.shape, self.w.q[l], self.summ[l], self.page_table, self.seq_lens, gamma,
-                  self.sm_scale, lists, lengths, self.ws)
+        if self.fmt == mb.SUMM_BF16:
+            mb.select(self.shape, self.w.q[l], self.summ[l], self.page_table, self.seq_lens, gamma,
+                      self.sm_scale, lists, lengths, self.ws)
+        else:
+            mb.select_ex(self.shape, self.fmt, self.w.q[l], self.summ[l], self.page_table,
+                         self.seq_lens, mb.RULE_COVERAGE, gamma, self.sm_scale, lists, lengths, self.ws)
         return lists, lengths
 
     def select_layer_rule(self, l: int, rule: int, param: float, lists=None, lengths=None):
         lists = self.lists if lists is None else lists
         lengths = self.lengths[l] if lengths is None else lengths
-        mb.select_rule(self.shape, self.w.q[l], self.summ[l], self.page_table, self.seq_lens, rule,
-                       param, self.sm_scale, lists, lengths, self.ws)
+        if self.fmt == mb.SUMM_BF16:
+            mb.select_rule(self.shape, self.w.q[l], self.summ[l], self.page_table, self.seq_lens,
+                           rule, param, self.sm_scale, lists, lengths, self.ws)
+        else:
+            mb.select_ex(self.shape, self.fmt, self.w.q[l], self.summ[l], self.page_table,
+                         self.seq_lens, rule, param, self.sm_scale, lists, lengths, self.ws)
         return lists, lengths
 
     def attend_layer(self, l: int, lists, lengths, out=None):

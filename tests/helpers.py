@@ -37,8 +37,9 @@ def u16(t: torch.Tensor) -> np.ndarray:
 class UnitData:
     """Host copy of one (layer, request, KV head) unit in logical page order."""
 
-    def __init__(self, w, l: int, r: int, j: int, with_v: bool = True):
+    def __init__(self, w, l: int, r: int, j: int, with_v: bool = True, fmt: int = 0):
         S = w.spec.page_size
+        self.fmt = fmt                     # summary format: 0 bf16, 1 eight-bit, 2 two-bit
         G = w.group
         self.L = int(w.seq_lens[r])
         self.n = self.L // S + (self.L % S != 0)
@@ -50,6 +51,7 @@ class UnitData:
         self.v = u16(w.v_pool[l].index_select(0, row)[:, j]) if with_v else None
         self.sm_scale = w.sm_scale
         self._summ = None
+        self._lowbit = None
 
     @property
     def summ(self):
@@ -57,11 +59,34 @@ class UnitData:
             self._summ = oracle.summaries(self.k[:self.F]) if self.F else np.zeros((0, 128), np.uint16)
         return self._summ
 
+    @property
+    def lowbit(self):
+        """Oracle low-bit summaries of the full pages: (codes [F][d], steps [F])."""
+        if self._lowbit is None:
+            bits = 8 if self.fmt == 1 else 2
+            if self.F:
+                self._lowbit = oracle.summaries_lowbit(self.k[:self.F], bits)
+            else:
+                self._lowbit = (np.zeros((0, 128), np.int8), np.zeros(0, np.float32))
+        return self._lowbit
+
     def select(self, gamma: float):
-        """Oracle selection: (logical list, mass, order, cum)."""
-        pool = self.summ[:, None, :] if self.F else np.zeros((1, 1, 128), np.uint16)
-        return oracle.select_unit(self.q, pool, 0, np.arange(max(self.F, 1), dtype=np.int32),
-                                  self.L, gamma, self.sm_scale)
+        """Oracle selection: (logical list, mass, order, cum), from the
+        summaries of this unit's format."""
+        rows = np.arange(max(self.F, 1), dtype=np.int32)
+        if self.fmt == 0:
+            pool = self.summ[:, None, :] if self.F else np.zeros((1, 1, 128), np.uint16)
+            return oracle.select_unit(self.q, pool, 0, rows, self.L, gamma, self.sm_scale)
+        codes, steps = self.lowbit
+        if not self.F:
+            codes, steps = np.zeros((1, 128), np.int8), np.zeros(1, np.float32)
+        lst, mass = oracle.select_unit_lowbit(self.q, codes[:, None, :], steps[:, None], 0, rows,
+                                              self.L, oracle.RULE_COVERAGE, gamma, self.sm_scale)
+        if gamma >= 1.0 or self.F == 0:
+            z = np.zeros(self.F)
+            return lst, z, np.zeros(self.F, np.int32), z
+        _, _, order, cum = oracle.cover(mass, gamma)
+        return lst, mass, order, cum
 
     def attend(self, logical_list) -> np.ndarray:
         return oracle.attend_unit(self.q, self.k[:, None], self.v[:, None], 0,
@@ -165,3 +190,22 @@ def check_rule_list(ud: UnitData, gpu_phys: np.ndarray, rule: int, param: float)
     if bad:
         return f"{len(bad)} pages decided differently away from the boundary, e.g. {bad[:3]}"
     return None
+
+
+def pack_lowbit(codes: np.ndarray, steps: np.ndarray, bits: int, rec_bytes: int) -> np.ndarray:
+    """Oracle codes [P][Hkv][d] and steps [P][Hkv] laid out as the library's
+    per-page records (include/moira.h): codes per KV head (one int8 each for
+    8 bits; element i at bits 2*(i%4) of byte i/4, as code + 2, for 2 bits),
+    then the fp32 steps, then zero padding to rec_bytes."""
+    P, Hkv, d = codes.shape
+    out = np.zeros((P, rec_bytes), np.uint8)
+    if bits == 8:
+        cb = d
+        out[:, :Hkv * cb] = codes.reshape(P, Hkv * d).view(np.uint8)
+    else:
+        cb = d // 4
+        u = (codes.astype(np.int16) + 2).astype(np.uint8).reshape(P, Hkv, cb, 4)
+        packed = u[..., 0] | (u[..., 1] << 2) | (u[..., 2] << 4) | (u[..., 3] << 6)
+        out[:, :Hkv * cb] = packed.reshape(P, Hkv * cb)
+    out[:, Hkv * cb:Hkv * cb + 4 * Hkv] = np.ascontiguousarray(steps, np.float32).view(np.uint8).reshape(P, 4 * Hkv)
+    return out

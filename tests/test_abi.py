@@ -129,3 +129,41 @@ def test_binding_rejects_host_tensors():
     t = torch.zeros(4, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         moira.update_summaries(shape, t, t, torch.zeros(1, dtype=torch.int32))
+
+
+@pytest.mark.parametrize("hkv,bf16,q8,q2", [(1, 256, 144, 48), (2, 512, 272, 80), (4, 1024, 528, 144),
+                                            (8, 2048, 1056, 288)])
+def test_summary_page_bytes_follow_the_record_layout(hkv, bf16, q8, q2):
+    """Hkv * d * 2 bytes for bf16; Hkv * d * b / 8 code bytes plus Hkv fp32
+    steps, padded to 16 bytes, for the low-bit formats."""
+    lib = moira.load_library()
+    shape = moira.Shape.of(4 * hkv, hkv, 1024)
+    got = [lib.moira_summary_page_bytes(ctypes.byref(shape), f)
+           for f in (mb.SUMM_BF16, mb.SUMM_Q8, mb.SUMM_Q2)]
+    assert got == [bf16, q8, q2]
+    assert lib.moira_summary_page_bytes(ctypes.byref(shape), 3) == 0
+    assert lib.moira_summary_page_bytes(ctypes.byref(moira.Shape.of(30, 8, 16)), mb.SUMM_Q8) == 0
+
+
+def test_format_entry_points_reject_bad_arguments_on_host():
+    lib = moira.load_library()
+    ok = moira.Shape.of(32, 8, 1024)
+    sp = ctypes.byref(ok)
+    for fmt in (-1, 3):
+        assert lib.moira_update_summaries_ex(sp, fmt, FAKE, FAKE, FAKE, 4, None) == 1
+        assert lib.moira_append_kv_ex(sp, fmt, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 64, None) == 1
+        assert lib.moira_select_ex(sp, fmt, FAKE, FAKE, FAKE, FAKE, 1, 64, mb.RULE_COVERAGE, 0.9, 0.1,
+                                   FAKE, FAKE, FAKE, 1 << 30, None) == 1
+        assert lib.moira_decode_step_ex(sp, fmt, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64,
+                                        mb.RULE_COVERAGE, 0.9, 0.1, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+                                        None) == 1
+    q8 = mb.SUMM_Q8
+    assert lib.moira_update_summaries_ex(sp, q8, FAKE, FAKE + 8, FAKE, 4, None) == 1     # misaligned
+    assert lib.moira_update_summaries_ex(sp, q8, FAKE, FAKE, FAKE, 0, None) == 0         # nothing to do
+    assert lib.moira_select_ex(sp, q8, FAKE, FAKE, FAKE, FAKE, 1, 64, mb.RULE_TOPK, 2.5, 0.1,
+                               FAKE, FAKE, FAKE, 1 << 30, None) == 1
+    assert lib.moira_select_ex(sp, q8, FAKE, FAKE, FAKE, FAKE, 1, mb.MAX_PAGES_PER_SEQ + 1,
+                               mb.RULE_COVERAGE, 0.9, 0.1, FAKE, FAKE, FAKE, 1 << 30, None) == 4
+    assert lib.moira_decode_step_ex(sp, q8, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64,
+                                    mb.RULE_TOPDELTA, 0.0, 0.1, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+                                    None) == 1
