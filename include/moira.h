@@ -112,14 +112,18 @@ moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream
  * element, an all-zero mean, or a step that rounds to 0 gets step 0 and
  * codes 0.
  * Low-bit layout: one record of moira_summary_page_bytes() bytes per
- * physical page, and per record:
- *   bytes [0, Hkv*cb)               codes, KV head j at [j*cb, (j+1)*cb), cb = d*b/8
- *                                   Q8: byte i = code of element i (int8)
- *                                   Q2: element i in bits 2*(i%4)+1 .. 2*(i%4) of
- *                                       byte i/4, stored as code + 2 (0..3)
- *   bytes [Hkv*cb, Hkv*cb + 4*Hkv)  fp32 step of each KV head
- *   then zero bytes up to a multiple of 16
- * At Hkv = 8 a page's summaries take 2048 (BF16), 1056 (Q8) or 288 (Q2) bytes. */
+ * physical page.  The record holds the KV heads in groups of gh = min(Hkv, 4)
+ * consecutive heads, group after group, and each group is
+ *   bytes [0, gh*cb)            codes, head jj of the group at [jj*cb, (jj+1)*cb),
+ *                               cb = d*b/8
+ *                               Q8: byte i = code of element i (int8)
+ *                               Q2: element i in bits 2*(i%4)+1 .. 2*(i%4) of
+ *                                   byte i/4, stored as code + 2 (0..3)
+ *   bytes [gh*cb, gh*cb + 4*gh) fp32 step of each head of the group
+ *   then zero bytes up to gh*cb + 16
+ * so the summaries of one group of heads are one contiguous, 16-byte aligned
+ * run.  At Hkv = 8 a page's summaries take 2048 (BF16), 1056 (Q8) or 288 (Q2)
+ * bytes. */
 typedef enum {
     MOIRA_SUMM_BF16 = 0,
     MOIRA_SUMM_Q8 = 1,

@@ -22,26 +22,34 @@ constexpr uint32_t kDevTimeout = 0x4u;
 // ---- page-summary formats ----------------------------------------------------
 // kSummBf16 : bf16 [P][Hkv][d], the mean key rounded to bf16.
 // kSummQ8 / kSummQ2 : one record per physical page, the mean key in 8 or 2
-//   bits per element (symmetric mid-rise: value = (code + 1/2) * step):
-//     bytes [0, Hkv*cb)              codes, head j at [j*cb, (j+1)*cb),
-//                                    cb = d * bits / 8; Q8: byte i = int8 code
-//                                    of element i; Q2: element i in bits
-//                                    2*(i%4) .. 2*(i%4)+1 of byte i/4, holding
-//                                    code + 2 (0..3)
-//     bytes [Hkv*cb, Hkv*cb + 4*Hkv) fp32 step of each head
-//     then zeros up to a multiple of 16 bytes
+//   bits per element (symmetric mid-rise: value = (code + 1/2) * step).  The
+//   KV heads are stored in groups of gh = min(Hkv, 4) consecutive heads, one
+//   group after another, each group
+//     bytes [0, gh*cb)            codes, head jj of the group at [jj*cb, (jj+1)*cb),
+//                                 cb = d * bits / 8; Q8: byte i = int8 code of
+//                                 element i; Q2: element i in bits 2*(i%4) ..
+//                                 2*(i%4)+1 of byte i/4, holding code + 2 (0..3)
+//     bytes [gh*cb, gh*cb + 4*gh) fp32 step of each head of the group
+//     then zeros up to gh*cb + 16
+//   so one group (the heads one score item reads) is one contiguous copy.
 constexpr int kSummBf16 = 0;
 constexpr int kSummQ8 = 1;
 constexpr int kSummQ2 = 2;
+constexpr int kSummGroup = 4;           // KV heads per low-bit group
 
 __host__ __device__ constexpr int summ_bits(int fmt) { return fmt == kSummQ8 ? 8 : (fmt == kSummQ2 ? 2 : 16); }
 __host__ __device__ constexpr int lowbit_code_bytes(int bits) { return kHeadDim * bits / 8; }
-__host__ __device__ constexpr int lowbit_step_bytes(int hkv) { return (hkv * 4 + 15) / 16 * 16; }
-// Bytes of one physical page's summaries (all KV heads).
+__host__ __device__ constexpr int lowbit_group_heads(int hkv) { return hkv < kSummGroup ? hkv : kSummGroup; }
+// Bytes of one low-bit head group: codes, gh fp32 steps, padding to 16 bytes.
+__host__ __device__ constexpr int lowbit_group_bytes(int bits, int hkv)
+{
+    return lowbit_group_heads(hkv) * lowbit_code_bytes(bits) + 16;
+}
+// Bytes of one physical page's summaries (all KV heads; Hkv in {1, 2, 4, 8}).
 __host__ __device__ constexpr int summ_page_bytes(int fmt, int hkv)
 {
     return fmt == kSummBf16 ? hkv * kHeadDim * 2
-                            : hkv * lowbit_code_bytes(summ_bits(fmt)) + lowbit_step_bytes(hkv);
+                            : (hkv / lowbit_group_heads(hkv)) * lowbit_group_bytes(summ_bits(fmt), hkv);
 }
 
 // A bounded device wait gives up after this long (ns of %globaltimer).
@@ -256,6 +264,17 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same MMA with fp16 operands (fp32 accumulate).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));

@@ -32,14 +32,22 @@ namespace moira {
 // ---------------------------------------------------------------------------
 // k_score
 // ---------------------------------------------------------------------------
-constexpr int kScoreThreads = 256;        // 8 warps: one (KV head, 16-page half) item each
-constexpr int kScoreHeads = 4;            // KV heads per block; blockIdx.z picks the slice
-static_assert(kScoreHeads * 2 <= kScoreThreads / 32, "one (KV head, 16-page half) item per warp");
+constexpr int kScoreConsumers = 8;        // warps: one (KV head, 16-page half) of an item each
+constexpr int kScoreThreads = (kScoreConsumers + 1) * 32;   // + one producer warp
+constexpr int kScoreHeads = 4;            // KV heads per item
+constexpr int kScoreMaxStages = 4;
+static_assert(kScoreHeads * 2 <= kScoreConsumers, "one (KV head, 16-page half) per consumer warp");
+static_assert(kScoreHeads == kSummGroup, "a score item reads one low-bit head group");
 
-// Per query head of a score block: chunk max, chunk sum and the chunk-
-// relative weights from the block's logits s_s[local head][page] (log2
-// domain, -inf for pages that do not count); 8 lanes per head (4 pages
-// each), 4 heads per warp instruction.
+__device__ __forceinline__ void score_consumer_bar()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kScoreConsumers * 32) : "memory");
+}
+
+// Per query head of an item: chunk max, chunk sum and the chunk-relative
+// weights from the item's logits s_s[local head][page] (log2 domain, -inf
+// for pages that do not count); 8 lanes per head (4 pages each), 4 heads
+// per warp instruction, consumer warps only.
 __device__ __forceinline__ void score_chunk_stats(const float *s_s, int nh, int jb, int r, int chunk,
                                                   int p0, int hq, int ld, int ldc,
                                                   float *__restrict__ weights,
@@ -47,7 +55,7 @@ __device__ __forceinline__ void score_chunk_stats(const float *s_s, int nh, int 
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hql = nh * kGroup;
-    for (int h0 = warp * 4; h0 < hql; h0 += 4 * (kScoreThreads / 32)) {
+    for (int h0 = warp * 4; h0 < hql; h0 += 4 * kScoreConsumers) {
         const int hl = h0 + (lane >> 3);
         const int sub = lane & 7;
         float4 v = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
@@ -74,260 +82,408 @@ __device__ __forceinline__ void score_chunk_stats(const float *s_s, int nh, int 
     }
 }
 
-// One block scores kScoreChunk (32) consecutive full pages of one request for
-// kScoreHeads KV heads (Hkv = 8 takes two blocks per chunk, so about four
-// blocks share an SM and one block's loads overlap another's arithmetic).
-// The page-table slice and the queries are read first; each listed page's
-// summaries for the block's heads (contiguous, 256 B per head) then arrive by
-// 1-D bulk copies on one mbarrier, at a padded shared-memory stride so that 8
-// consecutive pages fall in different banks.  Logits come from the tensor
-// cores: for KV head j and 16 pages,
-//   S^T[h][p] = sum_d q_{4j+h}[d] * kbar_p[d]   (mma.m16n8k16, fp32 accumulate)
-// with A = the group's 4 query rows (repeated in rows 4-7) and B = the
-// summaries via ldmatrix, i.e. 8 k-steps x 2 MMAs per (head, 16 pages).
-__global__ void __launch_bounds__(kScoreThreads, 4) k_score(
-    const uint16_t *__restrict__ q, const uint16_t *__restrict__ summ,
-    const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
-    int max_pages, int ld, long long num_pages, float scale_log2, float *__restrict__ weights,
-    float *__restrict__ chunks, int ldc, uint32_t *status)
-{
-    extern __shared__ __align__(128) uint8_t s_summ[];     // [32 pages][stride]
-    __shared__ __align__(16) float s_s[kScoreHeads * kGroup * kScoreChunk];  // [local q head][page]
-    __shared__ int s_phys[kScoreChunk];
-    __shared__ __align__(8) unsigned long long s_bar;
-    pdl_wait();                               // q and the score buffers follow earlier kernels
-    pdl_trigger();                            // after the wait: see k_select
-    const int r = blockIdx.y;
-    const int chunk = blockIdx.x;
-    const int nh = min(hkv, kScoreHeads);     // KV heads of this block: jb .. jb + nh - 1
-    const int jb = blockIdx.z * nh;
-    const int p0 = chunk * kScoreChunk;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t page_bytes = static_cast<uint32_t>(nh) * kHeadDim * 2;
-    const uint32_t stride = page_bytes + 16;
-    const uint32_t bar = smem_u32(&s_bar);
-    const int hrow = (lane >> 2) & 3;
-    const bool has_item = warp < nh * 2;      // (local KV head, 16-page half)
-    const int jl = warp >> 1, half = warp & 1;
-
-    // loads that do not need the sequence length first: page ids and the
-    // query fragments of this warp's item
-    int L = seq_lens[r];
-    const int pid_pre = (threadIdx.x < kScoreChunk && p0 + static_cast<int>(threadIdx.x) < max_pages)
-                            ? __ldg(page_table + static_cast<size_t>(r) * max_pages + p0 + threadIdx.x)
-                            : -1;
-    uint32_t aq[8][2];
-    {
-        const int j = jb + (has_item ? jl : 0);
-        const uint16_t *qrow = q + (static_cast<size_t>(r) * hq + j * kGroup + hrow) * kHeadDim + 2 * (lane & 3);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            aq[ks][0] = has_item ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16)) : 0u;
-            aq[ks][1] = has_item ? __ldg(reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8)) : 0u;
-        }
-    }
-    L = L < 0 ? 0 : (L > max_pages * kPageSize ? max_pages * kPageSize : L);
-    const int F = L / kPageSize;
-    if (p0 >= F) return;
-    const int np = min(kScoreChunk, F - p0);
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        mbar_fence_init();
-    }
-    if (threadIdx.x < kScoreChunk) s_phys[threadIdx.x] = static_cast<int>(threadIdx.x) < np ? pid_pre : -1;
-    __syncthreads();
-    if (warp == 0) {
-        const int phys = s_phys[lane];
-        const bool ok = lane < np && phys >= 0 && phys < num_pages;
-        const unsigned okm = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) mbar_arrive_expect_tx(bar, __popc(okm) * page_bytes);
-        __syncwarp();
-        if (ok)
-            bulk_load(smem_u32(s_summ + lane * stride),
-                      summ + (static_cast<size_t>(phys) * hkv + jb) * kHeadDim, page_bytes, bar);
-        if (lane < np && !ok && blockIdx.z == 0) raise_status(status, kDevBadPage);
-    }
-    if (!mbar_wait(bar, 0) && threadIdx.x == 0) raise_status(status, kDevTimeout);
-
-    if (has_item) {                                          // warp-uniform
-        float acc[2][4];
-#pragma unroll
-        for (int x = 0; x < 2; ++x) acc[x][0] = acc[x][1] = acc[x][2] = acc[x][3] = 0.f;
-        // ldmatrix rows: matrices (pages 0-7, dims +0), (pages 0-7, +8), (pages 8-15, +0), (8-15, +8)
-        const int prow = half * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const uint32_t rbase = smem_u32(s_summ) + prow * stride + jl * kHeadDim * 2 + (((lane >> 3) & 1) << 4);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(rbase + ks * 32, b0, b1, b2, b3);
-            mma_bf16_16816(acc[0], aq[ks][0], 0u, aq[ks][1], 0u, b0, b1);
-            mma_bf16_16816(acc[1], aq[ks][0], 0u, aq[ks][1], 0u, b2, b3);
-        }
-        if (lane < 16) {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int pl = half * 16 + nt * 8 + 2 * (lane & 3);
-                const int hl = jl * kGroup + hrow;
-                float s0 = acc[nt][0] * scale_log2, s1 = acc[nt][1] * scale_log2;
-                if (pl >= np || s_phys[pl] < 0 || s_phys[pl] >= num_pages) s0 = -INFINITY;
-                if (pl + 1 >= np || s_phys[pl + 1] < 0 || s_phys[pl + 1] >= num_pages) s1 = -INFINITY;
-                *reinterpret_cast<float2 *>(&s_s[hl * kScoreChunk + pl]) = make_float2(s0, s1);
-            }
-        }
-    }
-    __syncthreads();
-    score_chunk_stats(s_s, nh, jb, r, chunk, p0, hq, ld, ldc, weights, chunks);
-}
-
-
-// bf16 pair {lo, hi} (lo in the low half) from two exactly representable floats.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+// fp16 pair {lo, hi} (lo in the low half) from two floats, rounded to nearest.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
 {
     uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
-// Mid-rise level c + 1/2 of two 8-bit codes (the low 16 bits of v), as a bf16
-// pair: |2c + 1| <= 255 has at most 8 significant bits, so it is exact.
-__device__ __forceinline__ uint32_t q8_pair(uint32_t v)
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b)
 {
-    return pack_bf16x2(static_cast<float>(static_cast<int8_t>(v & 0xFFu)) + 0.5f,
-                       static_cast<float>(static_cast<int8_t>((v >> 8) & 0xFFu)) + 0.5f);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
-// Mid-rise level of two 2-bit codes (the low nibble of v, stored as code + 2):
-// u - 3/2 for u in 0..3.
+// Two 8-bit codes as an exact fp16 pair: byte u = c + 128 placed under the
+// exponent of 1024 reads as 1024 + u, and 1024 + u - 1152 = c.  `sel` picks
+// bytes 0,1 (0x5140) or 2,3 (0x5342) of the biased word.
+__device__ __forceinline__ uint32_t q8_pair(uint32_t biased, uint32_t sel)
+{
+    return hsub2(__byte_perm(biased, 0x64646464u, sel), 0x64806480u);
+}
+
+// Two 2-bit codes (stored as c + 2 at bits 0-1 and 16-17 of v) as an exact
+// fp16 pair: 1024 + u - 1026 = c.
 __device__ __forceinline__ uint32_t q2_pair(uint32_t v)
 {
-    return pack_bf16x2(static_cast<float>(v & 3u) - 1.5f, static_cast<float>((v >> 2) & 3u) - 1.5f);
+    return hsub2((v & 0x00030003u) | 0x64006400u, 0x64026402u);
 }
 
-// Shared-memory stride of one page slot of k_score_lowbit: the block's codes
-// and the page's step row, padded so that the lanes of one load phase (8
-// lanes of 16-byte loads for Q8, 16 lanes of 8-byte loads for Q2) hit
+// Shared-memory stride of one page slot for low-bit summaries: the page's
+// head group (codes and steps), padded so that the lanes of one load phase
+// (8 lanes of 16-byte loads for Q8, 16 lanes of 8-byte loads for Q2) hit
 // distinct banks.
-__host__ __device__ constexpr int score_lowbit_stride(int bits, int nh, int hkv)
+__host__ __device__ constexpr int score_lowbit_stride(int bits, int hkv)
 {
-    return (nh * lowbit_code_bytes(bits) + lowbit_step_bytes(hkv) + 127) / 128 * 128 + (bits == 8 ? 16 : 32);
+    return (lowbit_group_bytes(bits, hkv) + 127) / 128 * 128 + (bits == 8 ? 16 : 32);
 }
 
-// k_score for low-bit summaries (8 or 2 bits, mid-rise: value = (code + 1/2)
-// * step): the same blocks, logits and outputs.  Per listed page two bulk
-// copies bring the block's code bytes (nh * cb) and the page's step row
-// (Hkv fp32).  Codes feed the B fragments of mma.m16n8k16 directly: at
-// k-step s lane t of a quad holds elements 32t + 4s .. 32t + 4s + 3 (a
-// permutation of the contraction index, applied to the query fragments
-// as well), so a lane reads one 32-byte (Q8) or 8-byte (Q2) run per page and
-// turns each code into the bf16 level c + 1/2.  The logit of page p for
-// query head h is step_p * (q_h . (c_p + 1/2)), times the score scale.
-template <int kBits>
-__global__ void __launch_bounds__(kScoreThreads, 4) k_score_lowbit(
-    const uint16_t *__restrict__ q, const uint8_t *__restrict__ summ,
-    const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
-    int max_pages, int ld, long long num_pages, float scale_log2, float *__restrict__ weights,
-    float *__restrict__ chunks, int ldc, uint32_t *status)
+// Shared-memory stride of one page slot, by summary format: bf16 rows are
+// padded by 16 bytes so that the 8 ldmatrix rows of consecutive pages fall
+// in different banks; low-bit slots as score_lowbit_stride.
+__host__ __device__ constexpr int score_stride(int fmt, int nh, int hkv)
 {
-    constexpr int kCb = lowbit_code_bytes(kBits);
-    extern __shared__ __align__(128) uint8_t s_summ[];     // [32 pages][stride]
-    __shared__ __align__(16) float s_s[kScoreHeads * kGroup * kScoreChunk];
-    __shared__ int s_phys[kScoreChunk];
-    __shared__ __align__(8) unsigned long long s_bar;
-    pdl_wait();
-    pdl_trigger();
-    const int r = blockIdx.y;
-    const int chunk = blockIdx.x;
-    const int nh = min(hkv, kScoreHeads);
-    const int jb = blockIdx.z * nh;
-    const int p0 = chunk * kScoreChunk;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t code_bytes = static_cast<uint32_t>(nh) * kCb;
-    const uint32_t step_bytes = static_cast<uint32_t>(lowbit_step_bytes(hkv));
-    const uint32_t stride = static_cast<uint32_t>(score_lowbit_stride(kBits, nh, hkv));
-    const size_t rec = static_cast<size_t>(hkv) * kCb + step_bytes;
-    const uint32_t bar = smem_u32(&s_bar);
-    const int hrow = (lane >> 2) & 3;
-    const int t = lane & 3;
-    const bool has_item = warp < nh * 2;
-    const int jl = warp >> 1, half = warp & 1;
+    return fmt == kSummBf16 ? nh * kHeadDim * 2 + 16 : score_lowbit_stride(summ_bits(fmt), hkv);
+}
 
-    int L = seq_lens[r];
-    const int pid_pre = (threadIdx.x < kScoreChunk && p0 + static_cast<int>(threadIdx.x) < max_pages)
-                            ? __ldg(page_table + static_cast<size_t>(r) * max_pages + p0 + threadIdx.x)
-                            : -1;
-    uint32_t aq[8][2];
-    {
-        const int j = jb + (has_item ? jl : 0);
-        const uint16_t *qrow = q + (static_cast<size_t>(r) * hq + j * kGroup + hrow) * kHeadDim + 32 * t;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            aq[ks][0] = has_item ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 4 * ks)) : 0u;
-            aq[ks][1] = has_item ? __ldg(reinterpret_cast<const uint32_t *>(qrow + 4 * ks + 2)) : 0u;
-        }
-    }
+// Position of a score work item: request r, slice of nh KV heads, chunk of
+// 32 full pages.  In the persistent walk `nck` is the request's chunk count
+// (only chunks holding full pages are visited).
+struct ScoreCursor {
+    int r, slice, chunk, nck;
+};
+
+// Items of request r in the persistent walk: n_slices * ceil(F_r / 32).
+__device__ __forceinline__ int score_items_of(int L, int max_pages, int n_slices)
+{
     L = L < 0 ? 0 : (L > max_pages * kPageSize ? max_pages * kPageSize : L);
-    const int F = L / kPageSize;
-    if (p0 >= F) return;
-    const int np = min(kScoreChunk, F - p0);
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
+    return n_slices * ((L / kPageSize + kScoreChunk - 1) / kScoreChunk);
+}
+
+// Cursor of item g of the persistent walk (s_pref: exclusive prefix of the
+// requests' item counts, s_pref[batch] = total).
+__device__ __forceinline__ ScoreCursor score_cursor_at(int g, const int *s_pref, int batch, int n_slices)
+{
+    int lo = 0, hi = batch;                   // the last r with s_pref[r] <= g (never an empty request)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pref[mid] <= g) lo = mid;
+        else hi = mid;
+    }
+    ScoreCursor c;
+    c.r = lo;
+    c.nck = (s_pref[lo + 1] - s_pref[lo]) / n_slices;
+    const int local = g - s_pref[lo];
+    c.slice = local / c.nck;
+    c.chunk = local % c.nck;
+    return c;
+}
+
+__device__ __forceinline__ void score_cursor_next(ScoreCursor &c, const int *s_pref, int batch, int n_slices)
+{
+    if (++c.chunk < c.nck) return;
+    c.chunk = 0;
+    if (++c.slice < n_slices) return;
+    c.slice = 0;
+    do {
+        ++c.r;
+    } while (c.r < batch - 1 && s_pref[c.r + 1] == s_pref[c.r]);
+    if (c.r < batch) c.nck = (s_pref[c.r + 1] - s_pref[c.r]) / n_slices;
+}
+
+// Page logits of every (request, KV head, full page) and their per-chunk
+// softmax statistics.  A work item is (request, slice of kScoreHeads KV
+// heads, chunk of 32 consecutive full pages).
+//
+// Warp-specialised: the producer warp brings each valid page's summaries for
+// the item's heads into a shared-memory stage by 1-D bulk copies
+// (cp.async.bulk) on the stage's "full" mbarrier; the 8 consumer warps take
+// one (KV head, 16-page half) each, compute the logits on the tensor cores
+// and the chunk statistics, and free the stage on its "empty" mbarrier.
+// Two launch shapes (template argument kPersistent):
+//  * single wave: one block per item of the full
+//    (request, slice, chunk) grid, one stage; blocks past a request's full
+//    pages exit.  Page ids, the sequence length and the query fragments are
+//    all requested before the summaries are waited for;
+//  * persistent: a grid of resident blocks.  Every block
+//    scans the sequence lengths (exclusive prefix of the requests' item
+//    counts in shared memory), takes an equal range of the non-empty items
+//    in (request, slice, chunk) order and runs a ring of `stages` stages;
+//    the producer requests the next item's page ids while it issues the
+//    current copies, and consumers request the query fragments before
+//    waiting for the data.
+//
+// Logits, for KV head j and 16 pages: S^T[h][p] = sum_d q_{4j+h}[d] kbar_p[d]
+// by mma.m16n8k16 with A = the group's 4 query rows (repeated in rows 4-7):
+//  * bf16 summaries: B = the summary rows via ldmatrix, bf16 operands;
+//  * low-bit summaries (value = (c + 1/2) * step): fp16 operands.  A code c
+//    becomes an exact fp16 by placing its biased bits under the exponent of
+//    1024 and subtracting (a byte permute or mask and one f16x2 subtract per
+//    two codes); each query head is scaled by 2^k so that its largest element
+//    lies in [2^14, 2^15), which keeps its bf16 values exact in fp16; the 1/2
+//    of every level returns in the epilogue:
+//      s_p = step_p * (2^-k sum_i (2^k q_i) c_i + (1/2) sum_i q_i).
+//    Lane t of a quad holds elements 32t .. 32t+31 of its page (a 32-byte run
+//    for Q8, 8 bytes for Q2) and the contraction index is permuted so that
+//    every fp16 pair forms in place (Q8: 32t + 4s + {0,1} and {2,3} at k-step
+//    s; Q2: 32t + {s, s+8} and 32t + {16+s, 24+s}), the query fragments
+//    taking the same permutation.
+template <int kFmt, bool kPersistent>
+__global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
+    const uint16_t *__restrict__ q, const uint8_t *__restrict__ summ,
+    const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int batch, int hq,
+    int hkv, int max_pages, int ld, long long num_pages, float scale_log2,
+    float *__restrict__ weights, float *__restrict__ chunks, int ldc, int stages, uint32_t *status)
+{
+    constexpr bool kLow = kFmt != kSummBf16;
+    constexpr int kBits = summ_bits(kFmt);
+    constexpr int kCb = kLow ? lowbit_code_bytes(kBits) : kHeadDim * 2;   // code bytes per head
+    extern __shared__ __align__(128) uint8_t s_score[];       // [stages][32 pages][stride], s_pref
+    __shared__ __align__(16) float s_s[kScoreHeads * kGroup * kScoreChunk];  // [local q head][page]
+    __shared__ uint32_t s_ok[kScoreMaxStages];               // per stage: pages loaded
+    __shared__ int s_wsum[kScoreConsumers + 1];
+    __shared__ __align__(8) unsigned long long s_full[kScoreMaxStages], s_empty[kScoreMaxStages];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nh = min(hkv, kScoreHeads);
+    const int n_slices = hkv / nh;
+    const int n_chunks = (max_pages + kScoreChunk - 1) / kScoreChunk;
+    const uint32_t stride = static_cast<uint32_t>(score_stride(kFmt, nh, hkv));
+    const uint32_t code_bytes = static_cast<uint32_t>(nh) * kCb;
+    // bytes of one page that an item copies: its heads' bf16 rows, or its
+    // low-bit head group (codes, steps, padding)
+    const uint32_t copy_bytes = kLow ? static_cast<uint32_t>(lowbit_group_bytes(kBits, hkv)) : code_bytes;
+    const size_t rec = static_cast<size_t>(summ_page_bytes(kFmt, hkv));
+    int *s_pref = reinterpret_cast<int *>(s_score + static_cast<size_t>(stages) * kScoreChunk * stride);
+    if (tid == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_u32(&s_full[s]), 1);
+            mbar_init(smem_u32(&s_empty[s]), 1);
+        }
         mbar_fence_init();
     }
-    if (threadIdx.x < kScoreChunk) s_phys[threadIdx.x] = static_cast<int>(threadIdx.x) < np ? pid_pre : -1;
-    __syncthreads();
-    if (warp == 0) {
-        const int phys = s_phys[lane];
-        const bool ok = lane < np && phys >= 0 && phys < num_pages;
-        const unsigned okm = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) mbar_arrive_expect_tx(bar, __popc(okm) * (code_bytes + step_bytes));
-        __syncwarp();
-        if (ok) {
-            const uint8_t *src = summ + static_cast<size_t>(phys) * rec;
-            bulk_load(smem_u32(s_summ + lane * stride), src + jb * kCb, code_bytes, bar);
-            bulk_load(smem_u32(s_summ + lane * stride + code_bytes), src + hkv * kCb, step_bytes, bar);
-        }
-        if (lane < np && !ok && blockIdx.z == 0) raise_status(status, kDevBadPage);
-    }
-    if (!mbar_wait(bar, 0) && threadIdx.x == 0) raise_status(status, kDevTimeout);
+    pdl_wait();                               // q and the score buffers follow earlier kernels
+    pdl_trigger();                            // after the wait: see k_select
 
-    if (has_item) {                                          // warp-uniform
-        float acc[2][4];
+    // ---- the block's items ------------------------------------------------------
+    int g0, g1;                               // item range (fewer than 2^21 items)
+    ScoreCursor c0;
+    if constexpr (kPersistent) {
+        const int per = (batch + kScoreThreads - 1) / kScoreThreads;
+        const int rb = min(batch, tid * per), re = min(batch, rb + per);
+        int mine = 0;
+        for (int r = rb; r < re; ++r) mine += score_items_of(__ldg(seq_lens + r), max_pages, n_slices);
+        int x = mine;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-            const uint8_t *src = s_summ + (half * 16 + nt * 8 + (lane >> 2)) * stride + jl * kCb + t * (kCb / 4);
-            if constexpr (kBits == 8) {
-                const uint4 x0 = *reinterpret_cast<const uint4 *>(src);
-                const uint4 x1 = *reinterpret_cast<const uint4 *>(src + 16);
-                const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_16816(acc[nt], aq[ks][0], 0u, aq[ks][1], 0u, q8_pair(w[ks]), q8_pair(w[ks] >> 16));
-            } else {
-                const uint2 x = *reinterpret_cast<const uint2 *>(src);
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_wsum[warp] = x;
+        __syncthreads();
+        int run = x - mine;
+        for (int w = 0; w < warp; ++w) run += s_wsum[w];
+        for (int r = rb; r < re; ++r) {
+            s_pref[r] = run;
+            run += score_items_of(__ldg(seq_lens + r), max_pages, n_slices);
+        }
+        if (tid == kScoreThreads - 1) s_pref[batch] = run;
+        __syncthreads();
+        const long long W = s_pref[batch];
+        g0 = static_cast<int>(blockIdx.x * W / gridDim.x);
+        g1 = static_cast<int>((blockIdx.x + 1) * W / gridDim.x);
+        if (g0 < g1) c0 = score_cursor_at(g0, s_pref, batch, n_slices);
+    } else {
+        __syncthreads();                      // barriers initialised
+        g0 = 0;
+        g1 = 1;
+        c0.chunk = blockIdx.x % n_chunks;
+        c0.slice = (blockIdx.x / n_chunks) % n_slices;
+        c0.r = blockIdx.x / (n_chunks * n_slices);
+        c0.nck = n_chunks;
+    }
+    if (g0 >= g1) return;                     // block-uniform
+
+    if (warp == kScoreConsumers) {
+        // ---- producer ----------------------------------------------------------
+        ScoreCursor c = c0;
+        int L = __ldg(seq_lens + c.r);
+        int phys = c.chunk * kScoreChunk + lane < max_pages
+                       ? __ldg(page_table + static_cast<size_t>(c.r) * max_pages + c.chunk * kScoreChunk + lane)
+                       : -1;
+        for (int g = g0; g < g1; ++g) {
+            // next item's page ids and length, requested before this item's copies
+            ScoreCursor n = c;
+            int L_n = L, phys_n = -1;
+            if (g + 1 < g1) {
+                score_cursor_next(n, s_pref, batch, n_slices);
+                if (n.r != c.r) L_n = __ldg(seq_lens + n.r);
+                if (n.chunk * kScoreChunk + lane < max_pages)
+                    phys_n = __ldg(page_table + static_cast<size_t>(n.r) * max_pages + n.chunk * kScoreChunk + lane);
+            }
+            const int Lc = L < 0 ? 0 : (L > max_pages * kPageSize ? max_pages * kPageSize : L);
+            const int np = min(kScoreChunk, Lc / kPageSize - c.chunk * kScoreChunk);
+            if (np <= 0) break;               // single wave: past the request's full pages
+            const bool ok = lane < np && phys >= 0 && phys < num_pages;
+            const uint32_t okm = __ballot_sync(0xffffffffu, ok);
+            if (lane < np && !ok && c.slice == 0) raise_status(status, kDevBadPage);
+            const int it = g - g0;
+            const int stage = it % stages;
+            const uint32_t use = static_cast<uint32_t>(it / stages);
+            if (use > 0 && !mbar_wait(smem_u32(&s_empty[stage]), (use - 1) & 1u) && lane == 0)
+                raise_status(status, kDevTimeout);
+            const uint32_t full = smem_u32(&s_full[stage]);
+            if (lane == 0) {
+                s_ok[stage] = okm;
+                mbar_arrive_expect_tx(full, __popc(okm) * copy_bytes);
+            }
+            __syncwarp();
+            if (ok) {
+                bulk_load(smem_u32(s_score + (static_cast<uint32_t>(stage) * kScoreChunk + lane) * stride),
+                          summ + static_cast<size_t>(phys) * rec + static_cast<size_t>(c.slice) * copy_bytes,
+                          copy_bytes, full);
+            }
+            c = n;
+            L = L_n;
+            phys = phys_n;
+        }
+        return;
+    }
+
+    // ---- consumers -------------------------------------------------------------
+    const int hrow = (lane >> 2) & 3;
+    const int t = lane & 3;
+    const bool has_item = warp < nh * 2;      // warp-uniform
+    const int jl = warp >> 1, half = warp & 1;
+    ScoreCursor c = c0;
+    // query fragments of the current (request, slice); consecutive items of a
+    // block mostly share them, so they are fetched (and, for low-bit
+    // summaries, scaled and packed to fp16) only when (request, slice) changes
+    uint32_t qw[16];
+    float down = 1.f, half_qsum = 0.f;
+    int q_r = -1, q_slice = -1;
+    for (int g = g0; g < g1; ++g) {
+        const int jb = c.slice * nh;
+        if (has_item && (c.r != q_r || c.slice != q_slice)) {
+            q_r = c.r;
+            q_slice = c.slice;
+            const uint16_t *qrow = q + (static_cast<size_t>(c.r) * hq + (jb + jl) * kGroup + hrow) * kHeadDim;
+            if constexpr (!kLow) {
+                const uint16_t *qa = qrow + 2 * t;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t b = ((ks < 4 ? x.x : x.y) >> (8 * (ks & 3))) & 0xFFu;
-                    mma_bf16_16816(acc[nt], aq[ks][0], 0u, aq[ks][1], 0u, q2_pair(b), q2_pair(b >> 4));
+                    qw[2 * ks] = __ldg(reinterpret_cast<const uint32_t *>(qa + ks * 16));
+                    qw[2 * ks + 1] = __ldg(reinterpret_cast<const uint32_t *>(qa + ks * 16 + 8));
+                }
+            } else {
+                // the lane's 32 query elements 32t .. 32t+31 as bf16 pairs
+                const uint4 *qv4 = reinterpret_cast<const uint4 *>(qrow + 32 * t);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = __ldg(qv4 + i);
+                    qw[4 * i] = v.x;
+                    qw[4 * i + 1] = v.y;
+                    qw[4 * i + 2] = v.z;
+                    qw[4 * i + 3] = v.w;
+                }
+                float qmax = 0.f, qsum = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float lo = bf16_lo(qw[i]), hi = bf16_hi(qw[i]);
+                    qmax = fmaxf(qmax, fmaxf(fabsf(lo), fabsf(hi)));
+                    qsum += lo + hi;
+                }
+                qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+                qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+                qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+                int k = 0;
+                if (qmax > 0.f)
+                    k = min(max(14 - (static_cast<int>((__float_as_uint(qmax) >> 23) & 0xFFu) - 127), -126), 126);
+                const float up = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+                down = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);
+                half_qsum = 0.5f * qsum;
+                // fp16 query fragments, packed in place.  Q8: qw[2s], qw[2s+1]
+                // hold elements 4s + {0,1}, {2,3} (k-step s).  Q2: k-step s
+                // takes elements {s, s+8} and {16+s, 24+s}, built from the
+                // pairs (2j, 2j+1) and (8+2j, 9+2j): even s sits in qw[s/2] and
+                // qw[8 + s/2], odd s in qw[4 + s/2] and qw[12 + s/2].
+                if constexpr (kBits == 8) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) qw[i] = pack_f16x2(bf16_lo(qw[i]) * up, bf16_hi(qw[i]) * up);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int o = 0; o < 16; o += 8) {
+                            const uint32_t x = qw[o + j], y = qw[o + 4 + j];
+                            qw[o + j] = pack_f16x2(bf16_lo(x) * up, bf16_lo(y) * up);
+                            qw[o + 4 + j] = pack_f16x2(bf16_hi(x) * up, bf16_hi(y) * up);
+                        }
+                    }
                 }
             }
         }
-        if (lane < 16) {
+        if constexpr (!kPersistent) {         // single wave: is this item inside the request?
+            int L = __ldg(seq_lens + c.r);
+            L = L < 0 ? 0 : (L > max_pages * kPageSize ? max_pages * kPageSize : L);
+            if (c.chunk * kScoreChunk >= L / kPageSize) return;     // block-uniform
+        }
+        const int it = g - g0;
+        const int stage = it % stages;
+        const uint32_t use = static_cast<uint32_t>(it / stages);
+        if (!mbar_wait(smem_u32(&s_full[stage]), use & 1u) && tid == 0) raise_status(status, kDevTimeout);
+        const uint32_t okm = s_ok[stage];
+        const uint8_t *base = s_score + static_cast<uint32_t>(stage) * kScoreChunk * stride;
+        if (has_item) {
+            float acc[2][4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int pl = half * 16 + nt * 8 + 2 * t;
-                const int hl = jl * kGroup + hrow;
-                const float st0 = reinterpret_cast<const float *>(s_summ + pl * stride + code_bytes)[jb + jl];
-                const float st1 = reinterpret_cast<const float *>(s_summ + (pl + 1) * stride + code_bytes)[jb + jl];
-                float s0 = acc[nt][0] * st0 * scale_log2, s1 = acc[nt][1] * st1 * scale_log2;
-                if (pl >= np || s_phys[pl] < 0 || s_phys[pl] >= num_pages) s0 = -INFINITY;
-                if (pl + 1 >= np || s_phys[pl + 1] < 0 || s_phys[pl + 1] >= num_pages) s1 = -INFINITY;
-                *reinterpret_cast<float2 *>(&s_s[hl * kScoreChunk + pl]) = make_float2(s0, s1);
+            for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            if constexpr (!kLow) {
+                // ldmatrix rows: (pages 0-7, dims +0), (0-7, +8), (8-15, +0), (8-15, +8)
+                const int prow = half * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const uint32_t rbase = smem_u32(base) + prow * stride + jl * kCb + (((lane >> 3) & 1) << 4);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(rbase + ks * 32, b0, b1, b2, b3);
+                    mma_bf16_16816(acc[0], qw[2 * ks], 0u, qw[2 * ks + 1], 0u, b0, b1);
+                    mma_bf16_16816(acc[1], qw[2 * ks], 0u, qw[2 * ks + 1], 0u, b2, b3);
+                }
+            } else {
+                auto a0 = [&](int ks) { return kBits == 8 ? qw[2 * ks] : qw[(ks & 1) * 4 + (ks >> 1)]; };
+                auto a1 = [&](int ks) { return kBits == 8 ? qw[2 * ks + 1] : qw[8 + (ks & 1) * 4 + (ks >> 1)]; };
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint8_t *src = base + (half * 16 + nt * 8 + (lane >> 2)) * stride + jl * kCb + t * (kCb / 4);
+                    if constexpr (kBits == 8) {
+                        const uint4 x0 = *reinterpret_cast<const uint4 *>(src);
+                        const uint4 x1 = *reinterpret_cast<const uint4 *>(src + 16);
+                        const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t u = w[ks] ^ 0x80808080u;
+                            mma_f16_16816(acc[nt], a0(ks), 0u, a1(ks), 0u, q8_pair(u, 0x5140u),
+                                          q8_pair(u, 0x5342u));
+                        }
+                    } else {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(src);
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks)
+                            mma_f16_16816(acc[nt], a0(ks), 0u, a1(ks), 0u, q2_pair(x.x >> (2 * ks)),
+                                          q2_pair(x.y >> (2 * ks)));
+                    }
+                }
+            }
+            if (lane < 16) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int pl = half * 16 + nt * 8 + 2 * t;
+                    const int hl = jl * kGroup + hrow;
+                    float s0, s1;
+                    if constexpr (kLow) {
+                        const float st0 = reinterpret_cast<const float *>(base + pl * stride + code_bytes)[jl];
+                        const float st1 = reinterpret_cast<const float *>(base + (pl + 1) * stride + code_bytes)[jl];
+                        s0 = fmaf(acc[nt][0], down, half_qsum) * st0 * scale_log2;
+                        s1 = fmaf(acc[nt][1], down, half_qsum) * st1 * scale_log2;
+                    } else {
+                        s0 = acc[nt][0] * scale_log2;
+                        s1 = acc[nt][1] * scale_log2;
+                    }
+                    if (!((okm >> pl) & 1u)) s0 = -INFINITY;
+                    if (!((okm >> (pl + 1)) & 1u)) s1 = -INFINITY;
+                    *reinterpret_cast<float2 *>(&s_s[hl * kScoreChunk + pl]) = make_float2(s0, s1);
+                }
             }
         }
+        score_consumer_bar();                 // the stage is read and the logits are complete
+        if (tid == 0) mbar_arrive(smem_u32(&s_empty[stage]));
+        score_chunk_stats(s_s, nh, jb, c.r, c.chunk, c.chunk * kScoreChunk, hq, ld, ldc, weights, chunks);
+        score_consumer_bar();                 // s_s is free again
+        if (g + 1 < g1) score_cursor_next(c, s_pref, batch, n_slices);
     }
-    __syncthreads();
-    score_chunk_stats(s_s, nh, jb, r, chunk, p0, hq, ld, ldc, weights, chunks);
 }
 
 // ---------------------------------------------------------------------------
@@ -898,34 +1054,67 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
 }
 
 // ---------------------------------------------------------------------------
+template <int kFmt>
+cudaError_t launch_score_fmt(const void *q, const void *summ, const int32_t *page_table,
+                             const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
+                             long long num_pages, float scale_log2, float *weights, float *chunks,
+                             uint32_t *status, cudaStream_t stream)
+{
+    // stages of the persistent ring: the low-bit formats take a deeper ring
+    // in about the shared memory of bf16's two stages
+    constexpr int kStagesMax = kFmt == kSummBf16 ? 2 : (kFmt == kSummQ8 ? 3 : kScoreMaxStages);
+    static_assert(kStagesMax <= kScoreMaxStages, "stage ring");
+    const int nh = hkv < kScoreHeads ? hkv : kScoreHeads;
+    const long long n_items = static_cast<long long>(batch) * (hkv / nh) * ((max_pages + kScoreChunk - 1) / kScoreChunk);
+    const size_t stage_bytes = static_cast<size_t>(kScoreChunk) * score_stride(kFmt, nh, hkv);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // single wave: one block per item with one stage, when every item fits
+    // (resident blocks cached per (device, Hkv): they never change in a context)
+    static std::atomic<int> single_seen[64], single_fit[64][4];
+    const int hk = hkv == 1 ? 0 : (hkv == 2 ? 1 : (hkv == 4 ? 2 : 3));
+    int fit = dev < 64 ? single_fit[dev][hk].load(std::memory_order_relaxed) : 0;
+    if (fit == 0) {
+        if ((e = raise_smem_limit(k_score<kFmt, false>, stage_bytes, single_seen)) != cudaSuccess) return e;
+        int per_sm = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_score<kFmt, false>, kScoreThreads,
+                                                               stage_bytes)) != cudaSuccess)
+            return e;
+        fit = sms * (per_sm > 0 ? per_sm : 1);
+        if (dev < 64) single_fit[dev][hk].store(fit, std::memory_order_relaxed);
+    }
+    if (n_items <= fit)
+        return launch_pdl(k_score<kFmt, false>, dim3(static_cast<unsigned>(n_items)), dim3(kScoreThreads),
+                          stage_bytes, stream, static_cast<const uint16_t *>(q),
+                          static_cast<const uint8_t *>(summ), page_table, seq_lens, batch, hq, hkv,
+                          max_pages, weights_ld(max_pages), num_pages, scale_log2, weights, chunks,
+                          chunks_ld(max_pages), 1, status);
+    // persistent: resident blocks with the ring and the plan's prefix array
+    static std::atomic<int> ring_seen[64];
+    const size_t smem = kStagesMax * stage_bytes + align_up(static_cast<size_t>(batch + 1) * 4, 16);
+    if ((e = raise_smem_limit(k_score<kFmt, true>, smem, ring_seen)) != cudaSuccess) return e;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_score<kFmt, true>, kScoreThreads,
+                                                           smem)) != cudaSuccess)
+        return e;
+    const int blocks = sms * (per_sm > 0 ? per_sm : 1);
+    return launch_pdl(k_score<kFmt, true>, dim3(static_cast<unsigned>(blocks)), dim3(kScoreThreads), smem,
+                      stream, static_cast<const uint16_t *>(q), static_cast<const uint8_t *>(summ),
+                      page_table, seq_lens, batch, hq, hkv, max_pages, weights_ld(max_pages),
+                      num_pages, scale_log2, weights, chunks, chunks_ld(max_pages), kStagesMax, status);
+}
+
 cudaError_t launch_score(const void *q, const void *summ, int fmt, const int32_t *page_table,
                          const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
                          long long num_pages, float scale_log2, float *weights, float *chunks,
                          uint32_t *status, cudaStream_t stream)
 {
-    const int n_chunks = (max_pages + kScoreChunk - 1) / kScoreChunk;
-    const int nh = hkv < kScoreHeads ? hkv : kScoreHeads;
-    dim3 grid(n_chunks, batch, hkv / nh);
-    if (fmt == kSummQ8 || fmt == kSummQ2) {
-        const int bits = summ_bits(fmt);
-        const size_t smem = static_cast<size_t>(kScoreChunk) * score_lowbit_stride(bits, nh, hkv);
-        auto kernel = fmt == kSummQ8 ? k_score_lowbit<8> : k_score_lowbit<2>;
-        static std::atomic<int> seen8[64], seen2[64];
-        cudaError_t e = raise_smem_limit(kernel, smem, fmt == kSummQ8 ? seen8 : seen2);
-        if (e != cudaSuccess) return e;
-        return launch_pdl(kernel, grid, dim3(kScoreThreads), smem, stream,
-                          static_cast<const uint16_t *>(q), static_cast<const uint8_t *>(summ),
-                          page_table, seq_lens, hq, hkv, max_pages, weights_ld(max_pages), num_pages,
-                          scale_log2, weights, chunks, chunks_ld(max_pages), status);
-    }
-    const size_t smem = static_cast<size_t>(kScoreChunk) * (nh * kHeadDim * 2 + 16);
-    static std::atomic<int> seen[64];
-    cudaError_t e = raise_smem_limit(k_score, smem, seen);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k_score, grid, dim3(kScoreThreads), smem, stream,
-                      static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(summ),
-                      page_table, seq_lens, hq, hkv, max_pages, weights_ld(max_pages), num_pages,
-                      scale_log2, weights, chunks, chunks_ld(max_pages), status);
+    auto launch = fmt == kSummQ8 ? launch_score_fmt<kSummQ8>
+                                 : (fmt == kSummQ2 ? launch_score_fmt<kSummQ2> : launch_score_fmt<kSummBf16>);
+    return launch(q, summ, page_table, seq_lens, batch, hq, hkv, max_pages, num_pages, scale_log2,
+                  weights, chunks, status, stream);
 }
 
 cudaError_t launch_select(const float *weights, const float *chunks, const int32_t *page_table,

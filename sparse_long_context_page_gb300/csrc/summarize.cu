@@ -62,8 +62,8 @@ __device__ __forceinline__ void token_sums(const uint32_t *src, double &lo, doub
 
 // Write the low-bit summary of KV head j of one page into its record `rec`
 // from this thread's two fp64 means (dimensions 2*tid, 2*tid+1).  Called by
-// all 64 threads of the block (it synchronises them); head 0's block also
-// zeroes the record's padding.
+// all 64 threads of the block (it synchronises them); the block of the first
+// head of each head group also zeroes that group's padding.
 template <int kBits>
 __device__ void store_lowbit(double lo, double hi, uint8_t *rec, int j, int hkv)
 {
@@ -89,21 +89,21 @@ __device__ void store_lowbit(double lo, double hi, uint8_t *rec, int j, int hkv)
         c0 = static_cast<int>(fmin(fmax(floor(lo / static_cast<double>(step)), -kHalf), kHalf - 1.0));
         c1 = static_cast<int>(fmin(fmax(floor(hi / static_cast<double>(step)), -kHalf), kHalf - 1.0));
     }
+    const int gh = lowbit_group_heads(hkv), jj = j % gh;
+    uint8_t *grp = rec + (j / gh) * lowbit_group_bytes(kBits, hkv);
     if constexpr (kBits == 8) {
-        *reinterpret_cast<uint16_t *>(rec + j * kCb + 2 * tid) =
+        *reinterpret_cast<uint16_t *>(grp + jj * kCb + 2 * tid) =
             static_cast<uint16_t>((c0 & 0xFF) | ((c1 & 0xFF) << 8));
     } else {
         // element i sits in bits 2*(i%4) of byte i/4: this thread's pair is
         // one nibble, the low nibble for even tid
         const uint32_t nib = static_cast<uint32_t>(c0 + 2) | (static_cast<uint32_t>(c1 + 2) << 2);
         const uint32_t up = __shfl_down_sync(0xffffffffu, nib, 1);
-        if ((tid & 1) == 0) rec[j * kCb + (tid >> 1)] = static_cast<uint8_t>(nib | (up << 4));
+        if ((tid & 1) == 0) grp[jj * kCb + (tid >> 1)] = static_cast<uint8_t>(nib | (up << 4));
     }
-    if (tid == 0) *reinterpret_cast<float *>(rec + hkv * kCb + 4 * j) = step;
-    if (j == 0) {
-        const int pad0 = hkv * kCb + 4 * hkv, pad1 = hkv * kCb + lowbit_step_bytes(hkv);
-        if (pad0 + 4 * tid < pad1) *reinterpret_cast<uint32_t *>(rec + pad0 + 4 * tid) = 0u;
-    }
+    if (tid == 0) *reinterpret_cast<float *>(grp + gh * kCb + 4 * jj) = step;
+    if (jj == 0 && tid < kSummGroup - gh)                   // padding words after the steps
+        *reinterpret_cast<uint32_t *>(grp + gh * kCb + 4 * (gh + tid)) = 0u;
 }
 
 // One block per (listed page, KV head); 64 threads, two dimensions each.

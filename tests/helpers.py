@@ -194,18 +194,23 @@ def check_rule_list(ud: UnitData, gpu_phys: np.ndarray, rule: int, param: float)
 
 def pack_lowbit(codes: np.ndarray, steps: np.ndarray, bits: int, rec_bytes: int) -> np.ndarray:
     """Oracle codes [P][Hkv][d] and steps [P][Hkv] laid out as the library's
-    per-page records (include/moira.h): codes per KV head (one int8 each for
-    8 bits; element i at bits 2*(i%4) of byte i/4, as code + 2, for 2 bits),
-    then the fp32 steps, then zero padding to rec_bytes."""
+    per-page records (include/moira.h): KV heads in groups of min(Hkv, 4);
+    per group the heads' codes (one int8 each for 8 bits; element i at bits
+    2*(i%4) of byte i/4, as code + 2, for 2 bits), then their fp32 steps,
+    then zero padding to 16 bytes past the codes."""
     P, Hkv, d = codes.shape
-    out = np.zeros((P, rec_bytes), np.uint8)
+    gh = min(Hkv, 4)
+    cb = d * bits // 8
     if bits == 8:
-        cb = d
-        out[:, :Hkv * cb] = codes.reshape(P, Hkv * d).view(np.uint8)
+        packed = codes.view(np.uint8)                                   # [P][Hkv][cb]
     else:
-        cb = d // 4
         u = (codes.astype(np.int16) + 2).astype(np.uint8).reshape(P, Hkv, cb, 4)
         packed = u[..., 0] | (u[..., 1] << 2) | (u[..., 2] << 4) | (u[..., 3] << 6)
-        out[:, :Hkv * cb] = packed.reshape(P, Hkv * cb)
-    out[:, Hkv * cb:Hkv * cb + 4 * Hkv] = np.ascontiguousarray(steps, np.float32).view(np.uint8).reshape(P, 4 * Hkv)
+    gbytes = gh * cb + 16
+    out = np.zeros((P, rec_bytes), np.uint8)
+    st = np.ascontiguousarray(steps, np.float32).view(np.uint8).reshape(P, Hkv, 4)
+    for g in range(Hkv // gh):
+        o = g * gbytes
+        out[:, o:o + gh * cb] = packed[:, g * gh:(g + 1) * gh].reshape(P, gh * cb)
+        out[:, o + gh * cb:o + gh * cb + 4 * gh] = st[:, g * gh:(g + 1) * gh].reshape(P, 4 * gh)
     return out
