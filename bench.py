@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of a dense launch (65,536 entries: dram__bytes_read.sum + dram__bytes_write.sum
 # divided by the entries).  The digest names the kernel sources the capture was
 # taken on; once they change the figure is withheld (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "36d717376a3883752fde3882e72679ad80a5c258ddd6bff28b6e66e09e5621bb",
-                  "dram_bytes_per_entry": (537306368 + 3222016) / 65536}
+ATTEND_TRAFFIC = {"sources_sha256": "86b00d5f730080b18df7fe3b1ba1ebd81a21f54e1b514ecf456d17484d3b98d1",
+                  "dram_bytes_per_entry": (537293568 + 3277824) / 65536}
 
 
 def attend_sources_digest() -> str:
@@ -399,6 +399,8 @@ def run_ours(args):
     peak, peak_src = hbm_peak()
     t0 = time.time()
     over = {"layers": args.layers} if args.layers else {}
+    if args.batch:
+        over["batch"] = args.batch
     w = W.make_workload(args.workload, seed=args.seed, device=f"cuda:{local}", **over)
     st = DecodeState(w)
     st.summarize()
@@ -595,6 +597,8 @@ def main():
                     help="skip the comparisons: top-k / top-delta at equal pages, and the summary formats")
     ap.add_argument("--layers", type=int, default=0,
                     help="fewer layers than the workload's (small profiling cases only)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="fewer requests than the workload's (small profiling cases only)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)          # timing rule: at least 3 warm-up steps
     if args.impl == "reference":
