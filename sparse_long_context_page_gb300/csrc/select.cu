@@ -574,18 +574,16 @@ struct SelectShared {
     float red2[kSelWarps];
     float mmax[kGroup];
     float zinv[kGroup];
-    unsigned long long bar;
     uint32_t xmax;                          // largest mass pattern (top-delta)
 };
 
-// Dynamic shared memory of k_select: the group's weights, its chunk
-// statistics, per-chunk factors and the mass bit patterns.
-// Every row starts on a 16-byte boundary (bulk-copy destinations must).
+// Dynamic shared memory of k_select: per-chunk factors and the mass bit
+// patterns (the weights and chunk statistics are read from L2, where k_score
+// has just written them).
 __host__ __device__ inline size_t select_smem_bytes(int max_pages, int ldc)
 {
     const size_t wld = static_cast<size_t>(weights_ld(max_pages));
-    return sizeof(float) * kGroup * wld + sizeof(float) * kGroup * static_cast<size_t>(ldc) +
-           sizeof(float4) * static_cast<size_t>(ldc / 2) + sizeof(uint32_t) * wld;
+    return sizeof(float4) * static_cast<size_t>(ldc / 2) + sizeof(uint32_t) * wld;
 }
 
 __global__ void __launch_bounds__(kSelThreads) k_select(
@@ -597,11 +595,8 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
 {
     extern __shared__ __align__(16) float s_dyn[];
     __shared__ SelectShared sh;
-    const int wld = ld;                                            // 32-page padded rows
-    float *s_w = s_dyn;                                            // [G][wld] page weights
-    float *s_c = s_w + kGroup * wld;                               // [G][ldc] (max, sum) pairs
-    float4 *s_f = reinterpret_cast<float4 *>(s_c + kGroup * ldc);  // [ldc/2] per-chunk factors
-    uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_f + ldc / 2);   // [wld] mass bits
+    float4 *s_f = reinterpret_cast<float4 *>(s_dyn);               // [ldc/2] per-chunk factors
+    uint32_t *s_bits = reinterpret_cast<uint32_t *>(s_f + ldc / 2);   // [ld] mass bits
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // Before the wait: reads of the caller's inputs (page table, lengths) and
@@ -614,7 +609,6 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     const int r = u / hkv, j = u % hkv;
     const int32_t *row = page_table + static_cast<size_t>(r) * max_pages;
     int32_t *out = lists + static_cast<size_t>(u) * max_pages;
-    const uint32_t bar = smem_u32(&sh.bar);
     int L = seq_lens[r];
     // page ids of this thread's pages (page k*1024 + tid) in flight early
     int32_t pref[kSelStripes];
@@ -630,10 +624,6 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         L = L < 0 ? 0 : max_pages * kPageSize;
     }
     const int F = L / kPageSize, T = (L % kPageSize) != 0;
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        mbar_fence_init();
-    }
     for (int b = tid; b < kL1Bins; b += kSelThreads) sh.h1[b] = 0u;
     if (tid == 0) {
         sh.found = 0;
@@ -659,20 +649,18 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     const int nch = (F + kScoreChunk - 1) / kScoreChunk;
     const int nstripes = (F + kSelThreads - 1) / kSelThreads;
 
-    // 1. the group's weights and chunk statistics by bulk copies
-    __syncthreads();                          // barrier initialised, histogram cleared
-    if (warp == 0) {
-        const uint32_t wbytes = static_cast<uint32_t>((F + 3) & ~3) * 4;
-        const uint32_t cbytes = static_cast<uint32_t>((2 * nch + 3) & ~3) * 4;
-        if (lane == 0) mbar_arrive_expect_tx(bar, kGroup * (wbytes + cbytes));
-        __syncwarp();
-        if (lane < kGroup) {
-            const size_t hrow_i = static_cast<size_t>(r) * hq + j * kGroup + lane;
-            bulk_load(smem_u32(s_w + lane * wld), weights + hrow_i * ld, wbytes, bar);
-            bulk_load(smem_u32(s_c + lane * ldc), chunks + hrow_i * ldc, cbytes, bar);
-        }
+    // 1. the group's weight rows and chunk statistics are in L2 (k_score
+    //    wrote them): the first pass of weights is requested now, so that its
+    //    latency overlaps the normalisers
+    const float *wrow = weights + (static_cast<size_t>(r) * hq + j * kGroup) * ld;
+    float4 wpre[kGroup];
+    {
+        const int p = tid * 4;
+#pragma unroll
+        for (int h = 0; h < kGroup; ++h)
+            wpre[h] = p < F ? __ldg(reinterpret_cast<const float4 *>(wrow + h * ld + p))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (!mbar_wait(bar, 0) && tid == 0) raise_status(status, kDevTimeout);
 
     // 2. normalisers of the group's heads.  Thread -> (head tid/256, chunk
     //    tid%256): M = max of the chunk maxima, e_c = 2^(M_c - M) once per
@@ -681,8 +669,10 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         const int hg = tid >> 8, ci = tid & 255;
         float cm = -INFINITY, cz = 0.f;
         if (ci < nch) {
-            cm = s_c[hg * ldc + 2 * ci];
-            cz = s_c[hg * ldc + 2 * ci + 1];
+            const float2 cs = __ldg(reinterpret_cast<const float2 *>(
+                chunks + (static_cast<size_t>(r) * hq + j * kGroup + hg) * ldc + 2 * ci));
+            cm = cs.x;
+            cz = cs.y;
         }
         float mx = cm;
 #pragma unroll
@@ -708,17 +698,26 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
 
     // 3. masses (natural page order, no exponentials) and the level-1
     //    histogram; thread t takes 4 consecutive pages per pass (one chunk
-    //    factor, 16-byte shared-memory loads and stores)
+    //    factor, 16-byte loads and stores).  k_score writes whole 32-page
+    //    chunks, so the 4 weights at p < F are all written.
 #pragma unroll
     for (int k = 0; k < kSelStripes / 4; ++k) {
         const int p = (k * kSelThreads + tid) * 4;
         uint32_t xs[4] = {0u, 0u, 0u, 0u};
-        if (p < F) {                        // weights are loaded up to F rounded up to 4
+        if (p < F) {
             const float4 f = s_f[p / kScoreChunk];
-            const float4 w0 = *reinterpret_cast<const float4 *>(s_w + p);
-            const float4 w1 = *reinterpret_cast<const float4 *>(s_w + wld + p);
-            const float4 w2 = *reinterpret_cast<const float4 *>(s_w + 2 * wld + p);
-            const float4 w3 = *reinterpret_cast<const float4 *>(s_w + 3 * wld + p);
+            float4 w0, w1, w2, w3;
+            if (k == 0) {
+                w0 = wpre[0];
+                w1 = wpre[1];
+                w2 = wpre[2];
+                w3 = wpre[3];
+            } else {
+                w0 = __ldg(reinterpret_cast<const float4 *>(wrow + p));
+                w1 = __ldg(reinterpret_cast<const float4 *>(wrow + ld + p));
+                w2 = __ldg(reinterpret_cast<const float4 *>(wrow + 2 * ld + p));
+                w3 = __ldg(reinterpret_cast<const float4 *>(wrow + 3 * ld + p));
+            }
             const float m[4] = {w0.x * f.x + w1.x * f.y + w2.x * f.z + w3.x * f.w,
                                 w0.y * f.x + w1.y * f.y + w2.y * f.z + w3.y * f.w,
                                 w0.z * f.x + w1.z * f.y + w2.z * f.z + w3.z * f.w,
