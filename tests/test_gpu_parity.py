@@ -372,3 +372,42 @@ def test_a_wait_that_runs_out_is_reported_and_the_context_stays_usable():
     assert 0.04 < took < 5.0, took
     _check_layer(w, st, 0, float(np.float32(0.9)))        # select + attend still correct
     assert st.device_status() == 0
+
+
+def test_maximum_unit_count():
+    """4096 (request, KV head) units, the most one call takes: 512 requests of
+    1-400 tokens (ragged, with tails and with requests shorter than a page).
+    Every list is well formed and kept within its request; a sample of units
+    is checked against the oracle, lists and outputs."""
+    rng = np.random.default_rng(77)
+    ctx = tuple(int(x) for x in rng.integers(1, 400, size=512))
+    w, st = _state("llama8b_32k", seed=77, layers=1, batch=512, context=ctx)
+    assert w.spec.batch * w.spec.kv_heads == mb.MAX_UNITS
+    g = float(np.float32(0.9))
+    lists = torch.full_like(st.lists, -7)
+    lengths = torch.zeros((w.spec.batch, w.spec.kv_heads), dtype=torch.int32, device="cuda")
+    st.select_layer(0, g, lists, lengths)
+    out = torch.zeros_like(st.out[0])
+    st.attend_layer(0, lists, lengths, out)
+    torch.cuda.synchronize()
+    assert st.device_status() == 0
+    lh, nh, oh = lists.cpu().numpy(), lengths.cpu().numpy(), out.cpu().numpy()
+    seq = w.seq_lens
+    for r in range(w.spec.batch):
+        n_pages = (int(seq[r]) + 15) // 16
+        row = set(int(p) for p in w.page_table[r, :n_pages])
+        for j in range(w.spec.kv_heads):
+            n = int(nh[r, j])
+            assert 1 <= n <= n_pages, (r, j, n, n_pages)
+            assert set(int(p) for p in lh[r, j, :n]) <= row
+            if seq[r] % 16:
+                assert lh[r, j, n - 1] == w.page_table[r, n_pages - 1]
+    G = w.group
+    for _ in range(48):
+        r, j = int(rng.integers(w.spec.batch)), int(rng.integers(w.spec.kv_heads))
+        ud = H.UnitData(w, 0, r, j)
+        gl = lh[r, j, :nh[r, j]]
+        why = H.check_list(ud, gl, g)
+        assert why is None, f"r{r} j{j}: {why}"
+        ma, rl = H.out_errors(oh[r, j * G:(j + 1) * G], ud.attend(ud.to_logical(gl)))
+        assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"r{r} j{j}: {ma:.3g} {rl:.3g}"
