@@ -62,6 +62,7 @@ __host__ __device__ inline size_t attend_smem_bytes(int units)
            sizeof(int) * static_cast<size_t>(units + 1);
 }
 
+constexpr int kLenCache = 4;              // list lengths per thread kept in registers by the plan scan
 constexpr int kMergeSpan = 12;            // blocks per first-level merge group
 constexpr int kMergeBatch = 12;           // partials loaded together in a merge
 
@@ -236,14 +237,23 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
         const int ub = min(units, tid * per), ue = min(units, ub + per);
         int mine = 0;
         bool bad = false;
-        for (int u = ub; u < ue; ++u) {
+        // the first kLenCache lengths stay in registers for the second pass
+        // (one global round trip fewer before the first page at small batch)
+        auto length_of = [&](int u) {
             int len = a.lengths[u];
             if (len < 0 || len > a.max_pages) {
                 bad = true;
                 len = len < 0 ? 0 : a.max_pages;
             }
-            mine += len;
+            return len;
+        };
+        int lv[kLenCache];
+#pragma unroll
+        for (int i = 0; i < kLenCache; ++i) {
+            lv[i] = ub + i < ue ? length_of(ub + i) : 0;
+            mine += lv[i];
         }
+        for (int u = ub + kLenCache; u < ue; ++u) mine += length_of(u);
         if (bad) raise_status(a.status, kDevBadLen);
         int x = mine;
 #pragma unroll
@@ -257,9 +267,14 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
         int off = 0;
         for (int w = 0; w < warp; ++w) off += s_wsum[w];
         int run = off + x - mine;
-        for (int u = ub; u < ue; ++u) {
+#pragma unroll
+        for (int i = 0; i < kLenCache; ++i) {
+            if (ub + i < ue) s_off[ub + i] = run;
+            run += lv[i];
+        }
+        for (int u = ub + kLenCache; u < ue; ++u) {
             s_off[u] = run;
-            int len = a.lengths[u];
+            const int len = a.lengths[u];
             run += len < 0 ? 0 : (len > a.max_pages ? a.max_pages : len);
         }
         if (tid == kAttThreads - 1) s_off[units] = run;
