@@ -10,10 +10,13 @@
 //   [b*W/n, (b+1)*W/n) of the lists laid end to end and splits its range at
 //   list boundaries into segments.  A segment's partial goes to slot b + u
 //   (u = list index), which is unique.  Partials are merged by
-//   log-sum-exp in two levels: the last block to finish in each group of 12
-//   consecutive blocks of a list merges the group, and the last group to
-//   finish writes the output (arrival counters, self-resetting); a list held
-//   by one block, or by one group, is written by that block or group merge.
+//   log-sum-exp.  A list on at most 47 blocks (31 with the 8-slot ring) is
+//   one group: the last block to finish copies all its partials into its own
+//   stage ring, idle by then, with one bulk copy and merges them there.
+//   Longer lists merge in two levels: the last block to finish in each group
+//   of 12 consecutive blocks merges the group, and the last group to finish
+//   writes the output.  Arrival counters reset themselves; a list held by one
+//   block is written by that block.
 //
 // Data path per block (1 producer warp + 4 consumer warps, 2 blocks per SM):
 //   the producer looks up a batch of 32 list entries while it issues the
@@ -53,6 +56,7 @@ struct AttendSmem {
     int2 meta[NS];            // (unit, valid tokens; 0 = skip)
     int flag;
     int pad[3];
+    unsigned long long mrg;   // one-level merge: the bulk copy of a list's partials
 };
 
 template <int NS>
@@ -65,6 +69,10 @@ __host__ __device__ inline size_t attend_smem_bytes(int units)
 constexpr int kLenCache = 4;              // list lengths per thread kept in registers by the plan scan
 constexpr int kMergeSpan = 12;            // blocks per first-level merge group
 constexpr int kMergeBatch = 12;           // partials loaded together in a merge
+// A list spread over at most this many blocks merges in one level: its last
+// block copies all its partials into its stage ring (idle by then).
+template <int NS>
+constexpr int flat_merge_max() { return NS * kSlotBytes / (kPartFloats * 4); }
 
 // Online log-sum-exp merge of `count` partials stored at slots first,
 // first + stride, ... for this thread's head h and dims d0..d0+3: returns the
@@ -131,21 +139,57 @@ __device__ __forceinline__ float *out_row(const AttendArgs &a, int u, int h, int
 
 // How list u is spread over the blocks: blocks bfirst..blast hold its pages;
 // block b's merge group starts at gfirst and has gn members; the list has
-// ngroups groups.
+// ngroups groups.  A list on at most flat_max blocks is one group.
 struct ListSplit {
     int bfirst, blast, gfirst, gn, ngroups;
 };
 
-__device__ __forceinline__ ListSplit list_split(const int *s_off, int u, int b, long long W, long long n)
+__device__ __forceinline__ ListSplit list_split(const int *s_off, int u, int b, long long W, long long n,
+                                                int flat_max)
 {
     ListSplit ls;
     ls.bfirst = block_of(s_off[u], W, n);
     ls.blast = block_of(static_cast<long long>(s_off[u + 1]) - 1, W, n);
+    if (ls.blast - ls.bfirst + 1 <= flat_max) {
+        ls.gfirst = ls.bfirst;
+        ls.gn = ls.blast - ls.bfirst + 1;
+        ls.ngroups = 1;
+        return ls;
+    }
     ls.gfirst = ls.bfirst + (b - ls.bfirst) / kMergeSpan * kMergeSpan;
     ls.gn = min(kMergeSpan, ls.blast - ls.gfirst + 1);
     ls.ngroups = (ls.blast - ls.bfirst) / kMergeSpan + 1;
     return ls;
 }
+
+// Merge of `count` partials that sit contiguously in shared memory, for this
+// thread's head h and dims d0..d0+3 (two passes: the maximum, then the sums).
+__device__ __forceinline__ void merge_partials_smem(const float *pp, int count, int h, int d0, float &Mout,
+                                                    float &Lout, float4 &Oout)
+{
+    float mb = -INFINITY;
+    for (int k = 0; k < count; ++k) mb = fmaxf(mb, pp[k * kPartFloats + h]);
+    const float ms = mb == -INFINITY ? 0.f : mb;
+    float la = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < count; ++k) {
+        const float *q = pp + k * kPartFloats;
+        const float e = exp2f(q[h] - ms);
+        const float4 o = *reinterpret_cast<const float4 *>(q + 2 * kGroup + h * kHeadDim + d0);
+        acc.x += e * o.x; acc.y += e * o.y; acc.z += e * o.z; acc.w += e * o.w;
+        la += e * q[kGroup + h];
+    }
+    Mout = mb;
+    Lout = la;
+    Oout = acc;
+}
+
+// Where a merge may land its copy of the partials: the block's stage ring.
+struct MergeRing {
+    uint8_t *ring;
+    uint32_t bar;
+    uint32_t phase;
+};
 
 // Merges after this block's partial of a shared list u is published; prev is
 // the value thread 0's arrival atomic on the group counter returned (unused
@@ -153,7 +197,7 @@ __device__ __forceinline__ ListSplit list_split(const int *s_off, int u, int b, 
 // (into the output when the list has one group); the last group to arrive
 // merges the groups into the output.  Called by all consumer threads.
 __device__ __forceinline__ void resolve_list(const AttendArgs &a, int &flag, int u, const ListSplit ls,
-                                          uint32_t prev, int h, int d0)
+                                          uint32_t prev, int h, int d0, MergeRing &mr)
 {
     const int tid = threadIdx.x;
     int mine = 1;
@@ -165,7 +209,26 @@ __device__ __forceinline__ void resolve_list(const AttendArgs &a, int &flag, int
         if (mine) {
             float gm, gl;
             float4 go;
-            merge_partials(a.partials, ls.gfirst + u, 1, ls.gn, h, d0, gm, gl, go);
+            if (ls.gn > kMergeBatch) {
+                // one bulk copy of the group's partials (consecutive slots) into
+                // the idle ring instead of several rounds of L2 loads.  The
+                // acquire above made the other blocks' partials visible to this
+                // thread; the proxy fences hand them, and the ring's last
+                // generic reads, over to the asynchronous copy.
+                const uint32_t bytes = static_cast<uint32_t>(ls.gn) * kPartFloats * 4;
+                if (tid == 0) {
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive_expect_tx(mr.bar, bytes);
+                    bulk_load(smem_u32(mr.ring), a.partials + static_cast<size_t>(ls.gfirst + u) * kPartFloats,
+                              bytes, mr.bar);
+                }
+                if (!mbar_wait(mr.bar, mr.phase) && tid == 0) raise_status(a.status, kDevTimeout);
+                mr.phase ^= 1u;
+                merge_partials_smem(reinterpret_cast<const float *>(mr.ring), ls.gn, h, d0, gm, gl, go);
+            } else {
+                merge_partials(a.partials, ls.gfirst + u, 1, ls.gn, h, d0, gm, gl, go);
+            }
             if (ls.ngroups == 1) {                       // the only group: write the output
                 const float inv = gl > 0.f ? 1.f / gl : 0.f;
                 *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
@@ -222,6 +285,7 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
             mbar_init(smem_u32(&sm.full[s]), 1);
             mbar_init(smem_u32(&sm.empty[s]), 1);
         }
+        mbar_init(smem_u32(&sm.mrg), 1);
         mbar_fence_init();
     }
     if (warp == kConsumerWarps && lane == 0) {
@@ -372,6 +436,7 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
     const float c = a.scale_log2;
     // this thread's (head, 4 dims) in the block result and the merges
     const int h = tid >> 5, d0 = (tid & 31) * 4;
+    MergeRing mring{stage, smem_u32(&sm.mrg), 0u};
 
     // q fragments of list v (A operand rows 0-7 = heads 0-3 twice, rows 8-15 zero)
     uint32_t aq[8][2];
@@ -552,7 +617,7 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
             o.x += e * v.x; o.y += e * v.y; o.z += e * v.z; o.w += e * v.w;
             Lsum += e * sm.cl[w][h];
         }
-        const ListSplit ls = list_split(s_off, u, b, W, n);
+        const ListSplit ls = list_split(s_off, u, b, W, n, flat_merge_max<kSlots>());
         if (ls.bfirst == ls.blast) {
             const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
             *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
@@ -574,7 +639,7 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
                 pend_u = u;
                 pend_prev = prev;
             } else {
-                resolve_list(a, sm.flag, u, ls, prev, h, d0);
+                resolve_list(a, sm.flag, u, ls, prev, h, d0, mring);
             }
         }
         consumer_bar();                    // sm.co / cm / cl are reused by the next segment
@@ -582,7 +647,8 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
         u = un;
     }
     if (pend_u >= 0)
-        resolve_list(a, sm.flag, pend_u, list_split(s_off, pend_u, b, W, n), pend_prev, h, d0);
+        resolve_list(a, sm.flag, pend_u, list_split(s_off, pend_u, b, W, n, flat_merge_max<kSlots>()), pend_prev,
+                     h, d0, mring);
 }
 
 int attend_blocks_per_sm() { return kBlocksPerSm; }
