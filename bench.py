@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of a dense launch (65,536 entries: dram__bytes_read.sum + dram__bytes_write.sum
 # divided by the entries).  The digest names the kernel sources the capture was
 # taken on; once they change the figure is withheld (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "ad56ad8d37f38b3f59d84d0dd1b4d9208784b2c13f37ba7e636592d92a435a4c",
-                  "dram_bytes_per_entry": (537296896 + 2730752) / 65536}
+ATTEND_TRAFFIC = {"sources_sha256": "3747ac3ec8e2c017fc9f7af8f443f9a16a4d9e0323b70579ff7373e5edf929bf",
+                  "dram_bytes_per_entry": (537295616 + 2990592) / 65536}
 
 
 def attend_sources_digest() -> str:

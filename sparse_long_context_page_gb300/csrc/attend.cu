@@ -72,7 +72,7 @@ constexpr int kMergeBatch = 12;           // partials loaded together in a merge
 // A list spread over at most this many blocks merges in one level: its last
 // block copies all its partials into its stage ring (idle by then).
 template <int NS>
-constexpr int flat_merge_max() { return NS * kSlotBytes / (kPartFloats * 4); }
+__host__ __device__ constexpr int flat_merge_max() { return NS * kSlotBytes / (kPartFloats * 4); }
 
 // Online log-sum-exp merge of `count` partials stored at slots first,
 // first + stride, ... for this thread's head h and dims d0..d0+3: returns the

@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
 
     if (warp == kScoreConsumers) {
         // ---- producer ----------------------------------------------------------
+        const uint64_t pol = l2_evict_first();    // summaries are read once per step
         ScoreCursor c = c0;
         int L = __ldg(seq_lens + c.r);
         int phys = c.chunk * kScoreChunk + lane < max_pages
@@ -321,9 +322,9 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
             }
             __syncwarp();
             if (ok) {
-                bulk_load(smem_u32(s_score + (static_cast<uint32_t>(stage) * kScoreChunk + lane) * stride),
-                          summ + static_cast<size_t>(phys) * rec + static_cast<size_t>(c.slice) * copy_bytes,
-                          copy_bytes, full);
+                bulk_load_hint(smem_u32(s_score + (static_cast<uint32_t>(stage) * kScoreChunk + lane) * stride),
+                               summ + static_cast<size_t>(phys) * rec + static_cast<size_t>(c.slice) * copy_bytes,
+                               copy_bytes, full, pol);
             }
             c = n;
             L = L_n;
