@@ -73,7 +73,7 @@ typedef enum moira_status {
 #define MOIRA_HEAD_DIM 128               /* d */
 #define MOIRA_PAGE_SIZE 16               /* S, tokens per page */
 #define MOIRA_GROUP 4                    /* G = Hq / Hkv */
-#define MOIRA_MAX_PAGES_PER_SEQ 8192     /* max_pages: 128k tokens per request */
+#define MOIRA_MAX_PAGES_PER_SEQ 16384    /* max_pages: 256k tokens per request */
 #define MOIRA_MAX_UNITS 4096             /* batch * num_kv_heads */
 
 /* Model / cache geometry.  This build requires head_dim == 128,

@@ -25,7 +25,7 @@ STATUS = {0: "MOIRA_OK", 1: "MOIRA_EINVAL", 2: "MOIRA_EWORKSPACE", 3: "MOIRA_ECU
           4: "MOIRA_EUNSUPPORTED"}
 DEV_BADPAGE, DEV_BADLEN, DEV_TIMEOUT = 0x1, 0x2, 0x4
 HEAD_DIM, PAGE_SIZE, GROUP = 128, 16, 4
-MAX_PAGES_PER_SEQ, MAX_UNITS = 8192, 4096
+MAX_PAGES_PER_SEQ, MAX_UNITS = 16384, 4096
 
 # every symbol include/moira.h declares
 EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summaries",

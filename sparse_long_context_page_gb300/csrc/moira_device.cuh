@@ -12,7 +12,7 @@ namespace moira {
 constexpr int kHeadDim = 128;           // d
 constexpr int kPageSize = 16;           // S
 constexpr int kGroup = 4;               // G = Hq / Hkv
-constexpr int kMaxPagesPerSeq = 8192;       // 8 stripes of 1024 pages per selection thread block
+constexpr int kMaxPagesPerSeq = 16384;      // 256k tokens: 16 stripes of 1024 pages per selection block
 constexpr int kMaxUnits = 4096;
 
 constexpr uint32_t kDevBadPage = 0x1u;

@@ -492,8 +492,10 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
 // ---------------------------------------------------------------------------
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelStripes = kMaxPagesPerSeq / kSelThreads;   // stripes of 1024 pages
-static_assert(kSelStripes % 4 == 0, "masses: 4 pages per thread per pass");
+// Stripes of 1024 pages: 8 up to 8192 pages per request, 16 up to 16384
+// (the kernel is instantiated for both; registers hold one value per stripe).
+constexpr int kSelStripesMax = kMaxPagesPerSeq / kSelThreads;
+static_assert(kSelStripesMax % 4 == 0, "masses: 4 pages per thread per pass");
 // Level-1 bins: the fp32 bit pattern >> 16 (exponent + 7 fraction bits, 128
 // bins per octave) for masses in [2^-32, 2); bin 0 gathers everything below.
 constexpr uint32_t kKeyLo = 95u << 7;
@@ -556,7 +558,7 @@ __device__ unsigned long long sel_excl_scan(unsigned long long v, unsigned long 
 constexpr int kCand = 2048;                 // crossing-bin pages refined by one warp
 constexpr int kPairMax = 256;               // crossing-bin pages resolved pairwise
 static_assert(kPairMax * 4 <= kSelThreads, "pairwise path: at least 4 threads per candidate");
-static_assert(kMaxPagesPerSeq / kScoreChunk <= 256, "normalisers: one thread per chunk and head");
+static_assert(kMaxPagesPerSeq / kScoreChunk <= 2 * 256, "normalisers: at most two chunks per thread and head");
 
 struct SelectShared {
     uint32_t h1[kL1Bins];
@@ -567,7 +569,7 @@ struct SelectShared {
     int ncand;
     unsigned long long scan[32];
     unsigned long long above;
-    uint32_t cnt[kSelStripes * kSelWarps];              // (stripe, warp): gt | eq << 16
+    uint32_t cnt[kSelStripesMax * kSelWarps];           // (stripe, warp): gt | eq << 16
     uint32_t cnt_total;
     uint32_t lo, hi;
     int found;
@@ -587,6 +589,7 @@ __host__ __device__ inline size_t select_smem_bytes(int max_pages, int ldc)
     return sizeof(float4) * static_cast<size_t>(ldc / 2) + sizeof(uint32_t) * wld;
 }
 
+template <int kSelStripes>
 __global__ void __launch_bounds__(kSelThreads) k_select(
     const float *__restrict__ weights, const float *__restrict__ chunks,
     const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int hq, int hkv,
@@ -663,19 +666,27 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
                             : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    // 2. normalisers of the group's heads.  Thread -> (head tid/256, chunk
-    //    tid%256): M = max of the chunk maxima, e_c = 2^(M_c - M) once per
-    //    chunk, Z = sum_c e_c Z_c; the chunk factor is e_c / (G Z).
+    // 2. normalisers of the group's heads.  Thread -> (head tid/256, chunks
+    //    tid%256 + 256 i): M = max of the chunk maxima, e_c = 2^(M_c - M) once
+    //    per chunk, Z = sum_c e_c Z_c; the chunk factor is e_c / (G Z).
     {
+        constexpr int kCpt = kSelStripes / 8;         // chunks per thread and head: 1 or 2
         const int hg = tid >> 8, ci = tid & 255;
-        float cm = -INFINITY, cz = 0.f;
-        if (ci < nch) {
-            const float2 cs = __ldg(reinterpret_cast<const float2 *>(
-                chunks + (static_cast<size_t>(r) * hq + j * kGroup + hg) * ldc + 2 * ci));
-            cm = cs.x;
-            cz = cs.y;
+        const float *crow = chunks + (static_cast<size_t>(r) * hq + j * kGroup + hg) * ldc;
+        float cm[kCpt], cz[kCpt];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kCpt; ++i) {
+            cm[i] = -INFINITY;
+            cz[i] = 0.f;
+            const int c = ci + 256 * i;
+            if (c < nch) {
+                const float2 cs = __ldg(reinterpret_cast<const float2 *>(crow + 2 * c));
+                cm[i] = cs.x;
+                cz[i] = cs.y;
+            }
+            mx = fmaxf(mx, cm[i]);
         }
-        float mx = cm;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (lane == 0) sh.red[warp] = mx;
@@ -683,8 +694,12 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < 8; ++w) M = fmaxf(M, sh.red[hg * 8 + w]);
-        const float e = (cm == -INFINITY) ? 0.f : exp2f(cm - M);
-        float z = cz * e;
+        float e[kCpt], z = 0.f;
+#pragma unroll
+        for (int i = 0; i < kCpt; ++i) {
+            e[i] = (cm[i] == -INFINITY) ? 0.f : exp2f(cm[i] - M);
+            z += cz[i] * e[i];
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         if (lane == 0) sh.red2[warp] = z;
@@ -693,7 +708,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
 #pragma unroll
         for (int w = 0; w < 8; ++w) Z += sh.red2[hg * 8 + w];
         const float zinv = Z > 0.f ? 1.f / (kGroup * Z) : 0.f;
-        if (ci < nch) reinterpret_cast<float *>(s_f)[4 * ci + hg] = e * zinv;
+#pragma unroll
+        for (int i = 0; i < kCpt; ++i)
+            if (ci + 256 * i < nch) reinterpret_cast<float *>(s_f)[4 * (ci + 256 * i) + hg] = e[i] * zinv;
     }
     __syncthreads();
 
@@ -1006,11 +1023,11 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         }
     }
     __syncthreads();
-    if (warp == 0) {                          // lane l: entries 8l .. 8l+7
-        uint32_t v[8], run = 0u;
+    if (warp == 0) {                          // lane l: entries S*l .. S*l+S-1 (S stripes)
+        uint32_t v[kSelStripes], run = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane * 8 + i;
+        for (int i = 0; i < kSelStripes; ++i) {
+            const int e = lane * kSelStripes + i;
             const uint32_t c = e < nstripes * kSelWarps ? sh.cnt[e] : 0u;
             v[i] = run;
             run += c;
@@ -1023,12 +1040,12 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
         }
         const uint32_t base = x - run;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (lane * 8 + i < nstripes * kSelWarps) sh.cnt[lane * 8 + i] = base + v[i];
+        for (int i = 0; i < kSelStripes; ++i)
+            if (lane * kSelStripes + i < nstripes * kSelWarps) sh.cnt[lane * kSelStripes + i] = base + v[i];
         if (lane == 31) sh.cnt_total = x;
     }
     __syncthreads();
-    static_assert(kSelStripes * kSelWarps <= 256, "one warp scans the compaction counts");
+    static_assert(kSelStripes * kSelWarps == 32 * kSelStripes, "one warp scans the compaction counts");
     bool badp = false;
 #pragma unroll
     for (int k = 0; k < kSelStripes; ++k) {
@@ -1125,12 +1142,14 @@ cudaError_t launch_select(const float *weights, const float *chunks, const int32
 {
     const int ldc = chunks_ld(max_pages);
     const size_t smem = dense ? 0 : select_smem_bytes(max_pages, ldc);
+    const bool wide = max_pages > 8 * kSelThreads;            // 16 stripes of 1024 pages
+    auto kernel = wide ? k_select<16> : k_select<8>;
     if (!dense) {
-        static std::atomic<int> seen[64];
-        cudaError_t e = raise_smem_limit(k_select, smem, seen);
+        static std::atomic<int> seen8[64], seen16[64];
+        cudaError_t e = raise_smem_limit(kernel, smem, wide ? seen16 : seen8);
         if (e != cudaSuccess) return e;
     }
-    return launch_pdl(k_select, dim3(batch * hkv), dim3(kSelThreads), smem, stream, weights, chunks,
+    return launch_pdl(kernel, dim3(batch * hkv), dim3(kSelThreads), smem, stream, weights, chunks,
                       page_table, seq_lens, hq, hkv, max_pages, weights_ld(max_pages), ldc,
                       num_pages, rule, target, delta, dense ? 1 : 0, lists, lengths, status);
 }

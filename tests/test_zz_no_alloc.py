@@ -68,7 +68,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     lib = mb.load_library()
     w = W.make_workload("tiny", seed=1, device="cuda")
     st = DecodeState(w)
-    # 32 requests x 8 query heads x 8192 pages x 4 B of page weights = 8 MiB > 4 MiB
+    # 32 requests x 8 query heads x MAX_PAGES_PER_SEQ pages x 4 B of page weights > 4 MiB
     nb = 32
     big = nb * 8 * mb.MAX_PAGES_PER_SEQ * 4
     assert big > SCRATCH_BYTES
