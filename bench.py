@@ -44,8 +44,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of a dense launch (65,536 entries: dram__bytes_read.sum + dram__bytes_write.sum
 # divided by the entries).  The digest names the kernel sources the capture was
 # taken on; once they change the figure is withheld (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "3747ac3ec8e2c017fc9f7af8f443f9a16a4d9e0323b70579ff7373e5edf929bf",
-                  "dram_bytes_per_entry": (537295616 + 2990592) / 65536}
+ATTEND_TRAFFIC = {"sources_sha256": "5ff57dc927270af2ecc3f21e3d619453836047eafe184a55448b9db1a690f8a2",
+                  "dram_bytes_per_entry": (537294848 + 2964992) / 65536}
 
 
 def attend_sources_digest() -> str:
@@ -151,15 +151,17 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- bytes
 
-def step_bytes(w, lengths: np.ndarray, gamma: float):
-    """Algorithmic bytes of one step: summaries of every full page (gamma < 1),
-    K and V of the listed tokens, q in and fp32 out.  lengths: [L][B][Hkv]."""
+def step_bytes(w, lengths: np.ndarray, gamma: float, summ_page_bytes: int | None = None):
+    """Algorithmic bytes of one step: summaries of every full page (gamma < 1;
+    bf16 rows unless a record size per page is given), K and V of the listed
+    tokens, q in and fp32 out.  lengths: [L][B][Hkv]."""
     sp = w.spec
     d, S = sp.head_dim, sp.page_size
     L = w.seq_lens.astype(np.int64)
     F, T = L // S, (L % S != 0).astype(np.int64)
     tail_tok = L % S
-    per_layer_summ = int(F.sum()) * sp.kv_heads * d * 2 if gamma < 1.0 else 0
+    page_summ = sp.kv_heads * d * 2 if summ_page_bytes is None else summ_page_bytes
+    per_layer_summ = int(F.sum()) * page_summ if gamma < 1.0 else 0
     lens = lengths.astype(np.int64)                                   # [L][B][Hkv]
     tokens = (lens - T[None, :, None]) * S + (T * tail_tok)[None, :, None]
     kv = tokens * d * 2 * 2                                           # K + V bf16
@@ -205,7 +207,7 @@ def workload_config(args, w, head):
     return {"workload": f"{args.workload}: {sp.batch} request(s) x {int(w.seq_lens.max())} "
                         f"tokens, {sp.layers} layers, {sp.q_heads} q / {sp.kv_heads} kv heads, "
                         f"d=128, 16-token pages",
-            "gamma": round(head, 4), "seed": args.seed,
+            "gamma": round(head, 4), "seed": args.seed, "summaries": args.summaries,
             "l2": "inputs larger than L2 (each step reads >5 GB of K/V)",
             "graph": f"whole {sp.layers}-layer step in one CUDA graph, replayed"}
 
@@ -402,8 +404,10 @@ def run_ours(args):
     if args.batch:
         over["batch"] = args.batch
     w = W.make_workload(args.workload, seed=args.seed, device=f"cuda:{local}", **over)
-    st = DecodeState(w)
+    fmt = {"bf16": moira.SUMM_BF16, "q8": moira.SUMM_Q8, "q2": moira.SUMM_Q2}[args.summaries]
+    st = DecodeState(w, fmt=fmt)
     st.summarize()
+    spb = moira.summary_page_bytes(st.shape, fmt)
     torch.cuda.synchronize()
     log(f"[bench] workload {args.workload} generated in {time.time() - t0:.1f}s, "
         f"P={w.num_phys_pages} pages, KV {2 * w.k_pool.numel() * 2 / 2**30:.1f} GiB")
@@ -418,7 +422,7 @@ def run_ours(args):
         clk = clocks.stop(window) if clocks else None
         ms = max_over_ranks(ms, world)
         lengths = st.lengths.cpu().numpy()
-        per_layer, total, frac, parts = step_bytes(w, lengths, gm)
+        per_layer, total, frac, parts = step_bytes(w, lengths, gm, spb)
         results[gm] = dict(ms=ms, bytes=total, frac=frac, parts=parts, per_layer=per_layer,
                            lengths=lengths, clocks=clk)
         log(f"[bench] gamma={gm:.4f}: {ms * 1e3:.1f} us/step, {total / ms / 1e6:.0f} GB/s, "
@@ -429,7 +433,7 @@ def run_ours(args):
     # dominant kernel: attention, average in-graph launch duration at the headline gamma
     sel_ms, att_ms = time_parts(st, head, max(3, args.steps // 2), args.warmup)
     lengths = st.lengths.cpu().numpy()
-    per_layer, _, _, _ = step_bytes(w, lengths, head)
+    per_layer, _, _, _ = step_bytes(w, lengths, head, spb)
     summ_layer = results[head]["parts"]["summaries"] / sp.layers
     att_bytes = per_layer - summ_layer                    # K/V of kept tokens + q + out
     att_gbs = float(att_bytes.mean() / (att_ms * 1e6))
@@ -446,37 +450,41 @@ def run_ours(args):
     formats = compare_summaries(w, head, args) if not args.no_rules else None
 
     # end to end: host q in, host out back, through moira_decode_step_host
-    q_host = w.q.cpu().pin_memory()
-    out_host = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
-    q_dev, out_dev = torch.empty_like(w.q), torch.empty_like(st.out)
+    # (bf16 summaries; the low-bit formats are a profiling option here)
+    e2e_ms = eager_ms = None
+    q_host = out_host = None
+    if fmt == moira.SUMM_BF16:
+        q_host = w.q.cpu().pin_memory()
+        out_host = torch.empty(st.out.shape, dtype=torch.float32).pin_memory()
+        q_dev, out_dev = torch.empty_like(w.q), torch.empty_like(st.out)
 
-    def host_step():
-        moira.decode_step_host(st.shape, q_host, q_dev, w.k_pool, w.v_pool, st.summ, st.page_table,
-                               st.seq_lens, head, st.sm_scale, st.lists, st.lengths, out_dev,
-                               out_host, st.ws)
+        def host_step():
+            moira.decode_step_host(st.shape, q_host, q_dev, w.k_pool, w.v_pool, st.summ, st.page_table,
+                                   st.seq_lens, head, st.sm_scale, st.lists, st.lengths, out_dev,
+                                   out_host, st.ws)
 
-    # eager: the host enqueues the copies and the 3 x layers launches every step
-    for _ in range(args.warmup):
-        host_step()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        host_step()
-    e1.record()
-    torch.cuda.synchronize()
-    eager_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
-    # the same public call captured once (H2D copy of q from pinned memory, the
-    # step, D2H copy of out) and replayed: how a serving loop runs it
-    g_host = capture_fn(host_step)
-    e2e_ms, _ = time_graph(g_host, args.steps, args.warmup, world)
-    e2e_ms = max_over_ranks(e2e_ms, world)
-    del g_host
+        # eager: the host enqueues the copies and the 3 x layers launches every step
+        for _ in range(args.warmup):
+            host_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            host_step()
+        e1.record()
+        torch.cuda.synchronize()
+        eager_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+        # the same public call captured once (H2D copy of q from pinned memory, the
+        # step, D2H copy of out) and replayed: how a serving loop runs it
+        g_host = capture_fn(host_step)
+        e2e_ms, _ = time_graph(g_host, args.steps, args.warmup, world)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        del g_host
 
     # CPU baseline: the oracle on a bounded sample of the same step (rank 0 only)
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and fmt == moira.SUMM_BF16:
         n = max(1, min(sp.layers, args.cpu_layers))
         sample = list(range(n))
         secs, used = time_oracle(w, sample, head)
@@ -526,12 +534,12 @@ def run_ours(args):
                                      "null: no ncu capture of the current k_attend sources"),
                      "entries_per_launch": round(entries, 1),
                      "bytes_per_launch": int(att_bytes.mean())},
-        "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "us/step",
-                "h2d_bytes_per_step": int(q_host.numel() * 2),
-                "d2h_bytes_per_step": int(out_host.numel() * 4),
-                "how": "moira_decode_step_host (q copied in from pinned host memory, out copied back) "
-                       "captured in a CUDA graph and replayed; CUDA events",
-                "eager_value": round(eager_ms * 1e3, 2)},
+        "e2e": ({"value": round(e2e_ms * 1e3, 2), "unit": "us/step",
+                 "h2d_bytes_per_step": int(q_host.numel() * 2),
+                 "d2h_bytes_per_step": int(out_host.numel() * 4),
+                 "how": "moira_decode_step_host (q copied in from pinned host memory, out copied back) "
+                        "captured in a CUDA graph and replayed; CUDA events",
+                 "eager_value": round(eager_ms * 1e3, 2)} if e2e_ms is not None else None),
         "gpu_launches": args.steps * launches_per_step,
         "clocks": hd["clocks"],
         "cpu_baseline": cpu,
@@ -597,6 +605,9 @@ def main():
                     help="skip the comparisons: top-k / top-delta at equal pages, and the summary formats")
     ap.add_argument("--layers", type=int, default=0,
                     help="fewer layers than the workload's (small profiling cases only)")
+    ap.add_argument("--summaries", default="bf16", choices=["bf16", "q8", "q2"],
+                    help="page-summary format of the measured step (bf16 is the headline; the "
+                         "low-bit formats are for profiling: no e2e or CPU legs)")
     ap.add_argument("--batch", type=int, default=0,
                     help="fewer requests than the workload's (small profiling cases only)")
     args = ap.parse_args()
