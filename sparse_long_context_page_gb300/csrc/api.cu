@@ -103,7 +103,7 @@ moira_status select_impl(const moira_shape *shape, int32_t fmt, const void *q, c
                          const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
                          int32_t max_pages, int32_t rule, float param, float sm_scale,
                          int32_t *lists, int32_t *lengths, void *ws, size_t ws_bytes,
-                         cudaStream_t stream)
+                         bool early, cudaStream_t stream)
 {
     static_assert(MOIRA_RULE_COVERAGE == kRuleCoverage && MOIRA_RULE_TOPK == kRuleTopK &&
                       MOIRA_RULE_TOPDELTA == kRuleTopDelta,
@@ -129,7 +129,7 @@ moira_status select_impl(const moira_shape *shape, int32_t fmt, const void *q, c
         const float scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
         cudaError_t e = launch_score(q, summ, fmt, page_table, seq_lens, batch, shape->num_q_heads,
                                      shape->num_kv_heads, max_pages, shape->num_phys_pages,
-                                     scale_log2, scores, chunks, status, stream);
+                                     scale_log2, scores, chunks, early, status, stream);
         if (e != cudaSuccess) return MOIRA_ECUDA;
     }
     return cuda_status(launch_select(scores, chunks, page_table, seq_lens, batch,
@@ -276,7 +276,7 @@ moira_status moira_select_ex(const moira_shape *shape, int32_t format, const voi
     if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
     if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
     return select_impl(shape, format, q, summ, page_table, seq_lens, batch, max_pages, rule, param,
-                       sm_scale, lists, lengths, workspace, ws_bytes,
+                       sm_scale, lists, lengths, workspace, ws_bytes, false,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -354,7 +354,7 @@ moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int3
     for (int l = 0; l < num_layers; ++l) {
         st = select_impl(shape, format, q + l * q_layer, sp + l * sm_layer, page_table, seq_lens,
                          batch, max_pages, rule, param, sm_scale, lists,
-                         lengths_all + l * len_layer, workspace, ws_bytes, s);
+                         lengths_all + l * len_layer, workspace, ws_bytes, l > 0, s);
         if (st != MOIRA_OK) return st;
         st = attend_impl(shape, q + l * q_layer, kp + l * kv_layer, vp + l * kv_layer, lists,
                          lengths_all + l * len_layer, seq_lens, batch, max_pages, sm_scale,

@@ -19,10 +19,13 @@ cudaError_t launch_append(const void *k_new, const void *v_new, void *k_pool, vo
                           int batch, int hkv, int max_pages, long long num_pages, int fmt,
                           cudaStream_t stream);
 
+// `early`: the launch directly follows a kernel of this library that writes
+// neither page_table nor seq_lens (the previous layer's attention inside one
+// decode step); the kernel then reads them before its dependency wait.
 cudaError_t launch_score(const void *q, const void *summ, int fmt, const int32_t *page_table,
                          const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
                          long long num_pages, float scale_log2, float *scores, float *chunks,
-                         uint32_t *status, cudaStream_t stream);
+                         bool early, uint32_t *status, cudaStream_t stream);
 
 // Page rules of the selection (the values of the public moira_rule).
 constexpr int kRuleCoverage = 0;          // target = ceil(gamma * 2^31)

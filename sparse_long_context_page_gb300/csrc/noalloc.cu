@@ -101,8 +101,8 @@ extern "C" moira_status moira_select_noalloc(const moira_shape *shape, const voi
     if (!dense) {
         const float scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
         if (launch_score(q, summ, kSummBf16, page_table, seq_lens, batch, hq, shape->num_kv_heads,
-                         max_pages, shape->num_phys_pages, scale_log2, scores, chunks, status,
-                         s) != cudaSuccess)
+                         max_pages, shape->num_phys_pages, scale_log2, scores, chunks, false,
+                         status, s) != cudaSuccess)
             return MOIRA_ECUDA;
     }
     if (launch_select(scores, chunks, page_table, seq_lens, batch, hq, shape->num_kv_heads,

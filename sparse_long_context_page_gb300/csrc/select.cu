@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
     const uint16_t *__restrict__ q, const uint8_t *__restrict__ summ,
     const int32_t *__restrict__ page_table, const int32_t *__restrict__ seq_lens, int batch, int hq,
     int hkv, int max_pages, int ld, long long num_pages, float scale_log2,
-    float *__restrict__ weights, float *__restrict__ chunks, int ldc, int stages, uint32_t *status)
+    float *__restrict__ weights, float *__restrict__ chunks, int ldc, int stages, int early,
+    uint32_t *status)
 {
     constexpr bool kLow = kFmt != kSummBf16;
     constexpr int kBits = summ_bits(kFmt);
@@ -244,8 +245,16 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
         }
         mbar_fence_init();
     }
-    pdl_wait();                               // q and the score buffers follow earlier kernels
-    pdl_trigger();                            // after the wait: see k_select
+    // q, the summaries and the score buffers follow earlier kernels, so they
+    // are touched only after the wait.  With `early`, the launch follows a
+    // kernel of this library in the same step (which never writes the page
+    // table or the lengths), and the plan and the first page ids are read
+    // before it.  Every thread triggers its dependents after its own wait:
+    // k_select relies on that.
+    if (!early) {
+        pdl_wait();
+        pdl_trigger();
+    }
 
     // ---- the block's items ------------------------------------------------------
     int g0, g1;                               // item range (fewer than 2^21 items)
@@ -294,6 +303,10 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
         int phys = c.chunk * kScoreChunk + lane < max_pages
                        ? __ldg(page_table + static_cast<size_t>(c.r) * max_pages + c.chunk * kScoreChunk + lane)
                        : -1;
+        if (early) {
+            pdl_wait();
+            pdl_trigger();
+        }
         for (int g = g0; g < g1; ++g) {
             // next item's page ids and length, requested before this item's copies
             ScoreCursor n = c;
@@ -334,6 +347,10 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
     }
 
     // ---- consumers -------------------------------------------------------------
+    if (early) {
+        pdl_wait();
+        pdl_trigger();
+    }
     const int hrow = (lane >> 2) & 3;
     const int t = lane & 3;
     const bool has_item = warp < nh * 2;      // warp-uniform
@@ -1075,7 +1092,7 @@ template <int kFmt>
 cudaError_t launch_score_fmt(const void *q, const void *summ, const int32_t *page_table,
                              const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
                              long long num_pages, float scale_log2, float *weights, float *chunks,
-                             uint32_t *status, cudaStream_t stream)
+                             bool early, uint32_t *status, cudaStream_t stream)
 {
     // stages of the persistent ring: the low-bit formats take a deeper ring
     // in about the shared memory of bf16's two stages
@@ -1107,7 +1124,7 @@ cudaError_t launch_score_fmt(const void *q, const void *summ, const int32_t *pag
                           stage_bytes, stream, static_cast<const uint16_t *>(q),
                           static_cast<const uint8_t *>(summ), page_table, seq_lens, batch, hq, hkv,
                           max_pages, weights_ld(max_pages), num_pages, scale_log2, weights, chunks,
-                          chunks_ld(max_pages), 1, status);
+                          chunks_ld(max_pages), 1, early ? 1 : 0, status);
     // persistent: resident blocks with the ring and the plan's prefix array
     static std::atomic<int> ring_seen[64];
     const size_t smem = kStagesMax * stage_bytes + align_up(static_cast<size_t>(batch + 1) * 4, 16);
@@ -1120,18 +1137,19 @@ cudaError_t launch_score_fmt(const void *q, const void *summ, const int32_t *pag
     return launch_pdl(k_score<kFmt, true>, dim3(static_cast<unsigned>(blocks)), dim3(kScoreThreads), smem,
                       stream, static_cast<const uint16_t *>(q), static_cast<const uint8_t *>(summ),
                       page_table, seq_lens, batch, hq, hkv, max_pages, weights_ld(max_pages),
-                      num_pages, scale_log2, weights, chunks, chunks_ld(max_pages), kStagesMax, status);
+                      num_pages, scale_log2, weights, chunks, chunks_ld(max_pages), kStagesMax,
+                      early ? 1 : 0, status);
 }
 
 cudaError_t launch_score(const void *q, const void *summ, int fmt, const int32_t *page_table,
                          const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
                          long long num_pages, float scale_log2, float *weights, float *chunks,
-                         uint32_t *status, cudaStream_t stream)
+                         bool early, uint32_t *status, cudaStream_t stream)
 {
     auto launch = fmt == kSummQ8 ? launch_score_fmt<kSummQ8>
                                  : (fmt == kSummQ2 ? launch_score_fmt<kSummQ2> : launch_score_fmt<kSummBf16>);
     return launch(q, summ, page_table, seq_lens, batch, hq, hkv, max_pages, num_pages, scale_log2,
-                  weights, chunks, status, stream);
+                  weights, chunks, early, status, stream);
 }
 
 cudaError_t launch_select(const float *weights, const float *chunks, const int32_t *page_table,
