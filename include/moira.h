@@ -276,7 +276,10 @@ moira_status moira_attend(const moira_shape *shape, const void *q, const void *k
  *   summ_all   : bf16 [L][P][Hkv][d]
  *   lists      : int32 [batch][Hkv][max_pages]  scratch, reused per layer
  *   lengths_all: int32 [L][batch][Hkv] out (every layer's list lengths)
- *   out_all    : fp32 [L][batch][Hq][d] out */
+ *   out_all    : fp32 [L][batch][Hq][d] out
+ * page_table and seq_lens must not change until the step's work is done:
+ * from layer 1 on, the score kernel reads them while the previous layer's
+ * attention is still finishing. */
 moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, const void *q_all,
                                const void *k_pool_all, const void *v_pool_all,
                                const void *summ_all, const int32_t *page_table,
