@@ -223,6 +223,44 @@ def test_host_buffers_step_matches_device_step():
     assert torch.equal(out_host, ref.cpu())
 
 
+@pytest.mark.parametrize("fmt", [mb.SUMM_BF16, mb.SUMM_Q8])
+@pytest.mark.parametrize("persistent", [False, True])
+def test_decode_step_matches_per_layer_calls(fmt, persistent):
+    """From layer 1 on, the decode step lets the score kernel read the page
+    table and the lengths before its dependency wait; the per-layer calls
+    wait first.  Both must give the same lengths and outputs, bit for bit,
+    under both launch shapes of the score kernel."""
+    if persistent:
+        over = dict(batch=3, context=(16 * 700 + 9, 16 * 1500 + 3, 16 * 300))
+        max_pages = 8192                   # 3 x 2 x 256 items: more than one wave
+    else:
+        over = dict(batch=1, context=(16 * 900 + 5,))
+        max_pages = None
+    w = W.make_workload("llama8b_32k", seed=50, device="cuda", layers=4, **over)
+    st = DecodeState(w, max_pages=max_pages, fmt=fmt)
+    st.summarize()
+    gamma = float(np.float32(0.99))
+    st.step(gamma)
+    torch.cuda.synchronize()
+    assert st.device_status() == 0
+    out_s, len_s, last_lists = st.out.clone(), st.lengths.clone(), st.lists.clone()
+    for l in range(w.spec.layers):
+        lists = torch.full_like(st.lists, -1)
+        lengths = torch.zeros_like(st.lengths[l])
+        st.select_layer(l, gamma, lists, lengths)
+        out = torch.zeros_like(st.out[l])
+        st.attend_layer(l, lists, lengths, out)
+        torch.cuda.synchronize()
+        assert torch.equal(lengths, len_s[l]), f"layer {l}: list lengths differ"
+        assert torch.equal(out, out_s[l]), f"layer {l}: outputs differ"
+    n = lengths.cpu().numpy()
+    lh, ls = lists.cpu().numpy(), last_lists.cpu().numpy()
+    for r in range(w.spec.batch):
+        for j in range(w.spec.kv_heads):
+            assert np.array_equal(lh[r, j, :n[r, j]], ls[r, j, :n[r, j]])
+    assert st.device_status() == 0
+
+
 # ------------------------------------------------------------------ full sizes, sampled units
 
 FULL = [("llama8b_32k", 0.99), ("llama8b_128k", 0.99), ("llama8b_128k", 0.98),
