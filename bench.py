@@ -403,6 +403,9 @@ def run_ours(args):
     over = {"layers": args.layers} if args.layers else {}
     if args.batch:
         over["batch"] = args.batch
+        ctx = W.spec(args.workload).context
+        if len(ctx) > 1:                      # per-request lengths: the first `batch` of them
+            over["context"] = tuple(ctx[:args.batch])
     w = W.make_workload(args.workload, seed=args.seed, device=f"cuda:{local}", **over)
     fmt = {"bf16": moira.SUMM_BF16, "q8": moira.SUMM_Q8, "q2": moira.SUMM_Q2}[args.summaries]
     st = DecodeState(w, fmt=fmt)
