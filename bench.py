@@ -40,12 +40,16 @@ METRIC = "µs/decode-attn step & achieved HBM GB/s at 128k ctx, γ=0.99 vs γ=1 
 FALLBACK_HBM_GBS = 6800.0
 
 # DRAM bytes (read + write) that k_attend moves per list entry, i.e. per kept
-# (page, KV head) with its 4 KB of K and 4 KB of V, from a one-pass ncu capture
-# of a dense launch (65,536 entries: dram__bytes_read.sum + dram__bytes_write.sum
-# divided by the entries).  The digest names the kernel sources the capture was
-# taken on; once they change the figure is withheld (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "5ff57dc927270af2ecc3f21e3d619453836047eafe184a55448b9db1a690f8a2",
-                  "dram_bytes_per_entry": (537294848 + 2964992) / 65536}
+# (page, KV head) with its 4 KB of K and 4 KB of V, from one-pass ncu captures
+# of dense launches (dram__bytes_read.sum + dram__bytes_write.sum divided by the
+# entries), one per block shape of the kernel: below 64 lists (llama8b_128k,
+# 8 lists, 65,536 entries) and from 64 lists on (serving_ragged cut to 8
+# requests, 64 lists, 184,984 entries).  The digest names the kernel sources
+# the captures were taken on; once they change the figure is withheld
+# (traffic = null).
+ATTEND_TRAFFIC = {"sources_sha256": "PENDING",
+                  "many_lists_from": 64,
+                  "dram_bytes_per_entry": {"few_lists": None, "many_lists": None}}
 
 
 def attend_sources_digest() -> str:
@@ -442,9 +446,11 @@ def run_ours(args):
     att_gbs = float(att_bytes.mean() / (att_ms * 1e6))
     entries = float(lengths.reshape(sp.layers, -1).sum(axis=1).mean())     # list entries per launch
     digest = attend_sources_digest()
+    shape = "many_lists" if sp.batch * sp.kv_heads >= ATTEND_TRAFFIC["many_lists_from"] else "few_lists"
+    per_entry = ATTEND_TRAFFIC["dram_bytes_per_entry"][shape]
     traffic = None
-    if ATTEND_TRAFFIC["dram_bytes_per_entry"] and ATTEND_TRAFFIC["sources_sha256"] == digest:
-        traffic = int(round(ATTEND_TRAFFIC["dram_bytes_per_entry"] * entries))
+    if per_entry and ATTEND_TRAFFIC["sources_sha256"] == digest:
+        traffic = int(round(per_entry * entries))
 
     # the same step under the fixed-budget and relative-threshold rules, tuned
     # to read the same pages as coverage at the headline gamma; quality is the
@@ -535,7 +541,8 @@ def run_ours(args):
         "roofline": {"kernel": "k_attend", "bound": "hbm", "achieved": round(att_gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(att_gbs / peak, 4),
                      "peak_source": peak_src, "traffic": traffic,
-                     "traffic_how": ("ncu DRAM bytes per list entry of a dense launch x entries per launch"
+                     "traffic_how": (f"ncu DRAM bytes per list entry of a dense launch of the same block "
+                                     f"shape ({shape.replace('_', ' ')}) x entries per launch"
                                      if traffic is not None else
                                      "null: no ncu capture of the current k_attend sources"),
                      "entries_per_launch": round(entries, 1),

@@ -10,7 +10,7 @@
 //   [b*W/n, (b+1)*W/n) of the lists laid end to end and splits its range at
 //   list boundaries into segments.  A segment's partial goes to slot b + u
 //   (u = list index), which is unique.  Partials are merged by
-//   log-sum-exp.  A list on at most 47 blocks (31 with the 8-slot ring) is
+//   log-sum-exp.  A list on at most 47 blocks (39 with the 10-slot ring) is
 //   one group: the last block to finish copies all its partials into its own
 //   stage ring, idle by then, with one bulk copy and merges them there.
 //   Longer lists merge in two levels: the last block to finish in each group
@@ -18,13 +18,15 @@
 //   writes the output.  Arrival counters reset themselves; a list held by one
 //   block is written by that block.
 //
-// Data path per block (1 producer warp + 4 consumer warps, 2 blocks per SM):
+// Data path per block (1 producer warp + 4 consumer warps and a 12-slot ring
+// below 64 lists, 5 consumer warps and a 10-slot ring from 64 lists on; 2
+// blocks per SM either way):
 //   the producer looks up a batch of 32 list entries while it issues the
 //   previous batch, and issues 2-D TMA tensor loads of each kept page's K and
 //   V blocks (16 tokens x 128 dims bf16 = 4 KB each, two 128-byte-swizzled
-//   boxes per block) into a 12-slot (8 for very large batches) ring tracked
-//   by mbarriers, i.e. up to 192 KB in flight per SM; consumer warp w takes
-//   pages w, w+4, ... of the block's range.  The G = 4 query heads of
+//   boxes per block) into the ring, tracked by mbarriers (up to 192 or 160 KB
+//   per SM); with NW consumer warps, warp w takes pages w, w+NW, ... of the
+//   block's range, so each ring slot has one consumer.  The G = 4 query heads of
 //   the KV head share every page load:
 //     S^T[h][t] = q_h . k_t   : mma.m16n8k16, A = q (rows 0-3 and 4-7 both
 //                               hold the 4 heads), B = K^T via ldmatrix
@@ -38,19 +40,23 @@
 
 namespace moira {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kAttThreads = (kConsumerWarps + 1) * 32;
 constexpr int kSlotBytes = 2 * kPageSize * kHeadDim * 2;          // K + V block, 8 KB
 constexpr int kHalfBox = kPageSize * 64 * 2;                        // 16 rows x 128 B
 constexpr int kBlocksPerSm = 2;
-constexpr int kDeepSlots = 12, kShallowSlots = 8;
-constexpr int kDeepMaxUnits = 1024;       // s_off of the deep ring must leave room for 2 blocks/SM
+// Two block shapes, both 2 per SM.  Few lists (a small batch, each list
+// spread over many blocks, merges on the critical path): 4 consumer warps and
+// a 12-slot ring, whose one-level merge reaches lists on 47 blocks.  Many
+// lists (short merges; the consumer warps set the rate): 5 consumer warps and
+// a 10-slot ring.  The slot count is a multiple of the consumer warps.
+constexpr int kFewSlots = 12, kFewWarps = 4;
+constexpr int kManySlots = 10, kManyWarps = 5;
+constexpr int kManyUnits = 64;            // lists per launch from which the second shape runs
 
-template <int NS>
+template <int NS, int NW>
 struct AttendSmem {
-    float co[kConsumerWarps][kGroup][kHeadDim];
-    float cm[kConsumerWarps][kGroup];
-    float cl[kConsumerWarps][kGroup];
+    float co[NW][kGroup][kHeadDim];
+    float cm[NW][kGroup];
+    float cl[NW][kGroup];
     unsigned long long full[NS];
     unsigned long long empty[NS];
     int2 meta[NS];            // (unit, valid tokens; 0 = skip)
@@ -59,10 +65,10 @@ struct AttendSmem {
     unsigned long long mrg;   // one-level merge: the bulk copy of a list's partials
 };
 
-template <int NS>
+template <int NS, int NW>
 __host__ __device__ inline size_t attend_smem_bytes(int units)
 {
-    return 1024 + static_cast<size_t>(NS) * kSlotBytes + sizeof(AttendSmem<NS>) +
+    return 1024 + static_cast<size_t>(NS) * kSlotBytes + sizeof(AttendSmem<NS, NW>) +
            sizeof(int) * static_cast<size_t>(units + 1);
 }
 
@@ -126,9 +132,10 @@ __device__ __forceinline__ int block_of(long long g, long long W, long long n)
 }
 
 // Named barrier of the 4 consumer warps (the producer warp never joins it).
+template <int NW>
 __device__ __forceinline__ void consumer_bar()
 {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
 }
 
 __device__ __forceinline__ float *out_row(const AttendArgs &a, int u, int h, int d0)
@@ -195,17 +202,20 @@ struct MergeRing {
 // the value thread 0's arrival atomic on the group counter returned (unused
 // for a group of one).  The last block to arrive in a group merges the group
 // (into the output when the list has one group); the last group to arrive
-// merges the groups into the output.  Called by all consumer threads.
+// merges the groups into the output.  Called by all NW consumer warps; only
+// the first 4 (one per (head, 4 dims)) write.
+template <int NW>
 __device__ __forceinline__ void resolve_list(const AttendArgs &a, int &flag, int u, const ListSplit ls,
                                           uint32_t prev, int h, int d0, MergeRing &mr)
 {
     const int tid = threadIdx.x;
+    const bool hw = NW == kGroup || tid < kGroup * 32;   // always true with 4 consumer warps
     int mine = 1;
     if (ls.gn > 1) {
         if (tid == 0) flag = (prev == static_cast<uint32_t>(ls.gn - 1)) ? 1 : 0;
-        consumer_bar();
+        consumer_bar<NW>();
         mine = *const_cast<volatile int *>(&flag);
-        consumer_bar();                                  // every thread has read flag
+        consumer_bar<NW>();                                  // every thread has read flag
         if (mine) {
             float gm, gl;
             float4 go;
@@ -231,13 +241,14 @@ __device__ __forceinline__ void resolve_list(const AttendArgs &a, int &flag, int
             }
             if (ls.ngroups == 1) {                       // the only group: write the output
                 const float inv = gl > 0.f ? 1.f / gl : 0.f;
-                *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
-                    make_float4(go.x * inv, go.y * inv, go.z * inv, go.w * inv);
+                if (hw)
+                    *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
+                        make_float4(go.x * inv, go.y * inv, go.z * inv, go.w * inv);
             } else {
-                consumer_bar();                          // the group's first slot is read
+                consumer_bar<NW>();                          // the group's first slot is read
                 float *gp = a.partials + static_cast<size_t>(ls.gfirst + u) * kPartFloats;
-                *reinterpret_cast<float4 *>(gp + 2 * kGroup + h * kHeadDim + d0) = go;
-                if ((tid & 31) == 0) {
+                if (hw) *reinterpret_cast<float4 *>(gp + 2 * kGroup + h * kHeadDim + d0) = go;
+                if (hw && (tid & 31) == 0) {
                     gp[h] = gm;
                     gp[kGroup + h] = gl;
                 }
@@ -246,35 +257,45 @@ __device__ __forceinline__ void resolve_list(const AttendArgs &a, int &flag, int
         }
     }
     if (mine && ls.ngroups > 1) {
-        consumer_bar();                                  // group partial written
+        consumer_bar<NW>();                                  // group partial written
         if (tid == 0) {
             const uint32_t p2 = atomic_add_acq_rel_gpu(&a.counters[u], 1u);
             flag = (p2 == static_cast<uint32_t>(ls.ngroups - 1)) ? 1 : 0;
         }
-        consumer_bar();
+        consumer_bar<NW>();
         const int last = *const_cast<volatile int *>(&flag);
         if (last) {
             float fm, fl;
             float4 fo;
             merge_partials(a.partials, ls.bfirst + u, kMergeSpan, ls.ngroups, h, d0, fm, fl, fo);
             const float inv = fl > 0.f ? 1.f / fl : 0.f;
-            *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
-                make_float4(fo.x * inv, fo.y * inv, fo.z * inv, fo.w * inv);
+            if (hw)
+                *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
+                    make_float4(fo.x * inv, fo.y * inv, fo.z * inv, fo.w * inv);
             if (tid == 0) a.counters[u] = 0u;            // ready for the next launch
         }
     }
-    consumer_bar();                                      // flag is free again
+    consumer_bar<NW>();                                      // flag is free again
 }
 
-template <int kSlots>
-__global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
+template <int kSlots, int kConsumerWarps>
+__global__ void __launch_bounds__((kConsumerWarps + 1) * 32, kBlocksPerSm)
     k_attend(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
              const AttendArgs a)
 {
+    // Consumer warp w takes the pages whose range index is w modulo the warp
+    // count, so with a slot count that is a multiple of it every slot belongs
+    // to one warp, which waits on its rounds in order.  Otherwise a warp that
+    // runs ahead could wait on a slot's parity one round early and match the
+    // round before.
+    static_assert(kSlots % kConsumerWarps == 0, "every ring slot belongs to one consumer warp");
+    static_assert(kConsumerWarps >= kGroup, "the first 4 consumer warps own the (head, dims) slices");
+    constexpr int kAttThreads = (kConsumerWarps + 1) * 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *stage = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    AttendSmem<kSlots> &sm = *reinterpret_cast<AttendSmem<kSlots> *>(stage + kSlots * kSlotBytes);
+    AttendSmem<kSlots, kConsumerWarps> &sm =
+        *reinterpret_cast<AttendSmem<kSlots, kConsumerWarps> *>(stage + kSlots * kSlotBytes);
     int *s_off = reinterpret_cast<int *>(&sm + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -435,7 +456,9 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
     const bool lo_lane = lane >= 16;      // holds the bf16 residual column of P
     const float c = a.scale_log2;
     // this thread's (head, 4 dims) in the block result and the merges
-    const int h = tid >> 5, d0 = (tid & 31) * 4;
+    // (a fifth consumer warp reads head 0's slice and writes nothing)
+    const bool hw = kConsumerWarps == kGroup || tid < kGroup * 32;
+    const int h = hw ? tid >> 5 : 0, d0 = (tid & 31) * 4;
     MergeRing mring{stage, smem_u32(&sm.mrg), 0u};
 
     // q fragments of list v (A operand rows 0-7 = heads 0-3 twice, rows 8-15 zero)
@@ -601,7 +624,7 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
             sm.cm[warp][lane >> 2] = m_run;
             sm.cl[warp][lane >> 2] = lsum;
         }
-        consumer_bar();
+        consumer_bar<kConsumerWarps>();
 
         // ---- block result: thread -> (head, 4 dims) ----
         float M = -INFINITY;
@@ -620,57 +643,59 @@ __global__ void __launch_bounds__(kAttThreads, kBlocksPerSm)
         const ListSplit ls = list_split(s_off, u, b, W, n, flat_merge_max<kSlots>());
         if (ls.bfirst == ls.blast) {
             const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-            *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
-                make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            if (hw)
+                *reinterpret_cast<float4 *>(out_row(a, u, h, d0)) =
+                    make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
         } else {
             // this block's partial of list u -> slot b + u, then its arrival
             float *part = a.partials + static_cast<size_t>(b + u) * kPartFloats;
-            *reinterpret_cast<float4 *>(part + 2 * kGroup + h * kHeadDim + d0) = o;
-            if ((tid & 31) == 0) {
+            if (hw) *reinterpret_cast<float4 *>(part + 2 * kGroup + h * kHeadDim + d0) = o;
+            if (hw && (tid & 31) == 0) {
                 part[h] = M;
                 part[kGroup + h] = Lsum;
             }
             // the CTA barrier makes every thread's partial visible to thread 0,
             // whose acq_rel atomic publishes it and acquires the others
-            consumer_bar();
+            consumer_bar<kConsumerWarps>();
             uint32_t prev = 0u;
             if (ls.gn > 1 && tid == 0) prev = atomic_add_acq_rel_gpu(&a.gcounters[ls.gfirst + u], 1u);
             if (more) {                    // first segment: resolved after the last one
                 pend_u = u;
                 pend_prev = prev;
             } else {
-                resolve_list(a, sm.flag, u, ls, prev, h, d0, mring);
+                resolve_list<kConsumerWarps>(a, sm.flag, u, ls, prev, h, d0, mring);
             }
         }
-        consumer_bar();                    // sm.co / cm / cl are reused by the next segment
+        consumer_bar<kConsumerWarps>();    // sm.co / cm / cl are reused by the next segment
         if (!more) break;
         u = un;
     }
     if (pend_u >= 0)
-        resolve_list(a, sm.flag, pend_u, list_split(s_off, pend_u, b, W, n, flat_merge_max<kSlots>()), pend_prev,
-                     h, d0, mring);
+        resolve_list<kConsumerWarps>(a, sm.flag, pend_u,
+                                     list_split(s_off, pend_u, b, W, n, flat_merge_max<kSlots>()),
+                                     pend_prev, h, d0, mring);
 }
 
 int attend_blocks_per_sm() { return kBlocksPerSm; }
 
-template <int NS>
-static cudaError_t launch_attend_ns(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
-                                    const AttendArgs &args, int blocks, cudaStream_t stream)
+template <int NS, int NW>
+static cudaError_t launch_attend_shape(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                       const AttendArgs &args, int blocks, cudaStream_t stream)
 {
-    const size_t smem = attend_smem_bytes<NS>(args.units);
+    const size_t smem = attend_smem_bytes<NS, NW>(args.units);
     static std::atomic<int> seen[64];
-    cudaError_t e = raise_smem_limit(k_attend<NS>, smem, seen);
+    cudaError_t e = raise_smem_limit(k_attend<NS, NW>, smem, seen);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k_attend<NS>, dim3(blocks), dim3(kAttThreads), smem, stream, tmap_k, tmap_v,
-                      args);
+    return launch_pdl(k_attend<NS, NW>, dim3(blocks), dim3((NW + 1) * 32), smem, stream, tmap_k,
+                      tmap_v, args);
 }
 
 cudaError_t launch_attend(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           const AttendArgs &args, int blocks, cudaStream_t stream)
 {
-    if (args.units <= kDeepMaxUnits)
-        return launch_attend_ns<kDeepSlots>(tmap_k, tmap_v, args, blocks, stream);
-    return launch_attend_ns<kShallowSlots>(tmap_k, tmap_v, args, blocks, stream);
+    if (args.units < kManyUnits)
+        return launch_attend_shape<kFewSlots, kFewWarps>(tmap_k, tmap_v, args, blocks, stream);
+    return launch_attend_shape<kManySlots, kManyWarps>(tmap_k, tmap_v, args, blocks, stream);
 }
 
 }  // namespace moira

@@ -104,9 +104,13 @@ def test_select_edge_lengths():
         _check_layer(w, st, 0, float(np.float32(gamma)))
 
 
-def test_attend_random_lists_isolated():
-    """Attention alone on seeded random lists (neither side's selection)."""
-    w = W.make_workload("serving_ragged", seed=21, device="cuda", batch=5, layers=1)
+@pytest.mark.parametrize("batch", [5, 8, 12])
+def test_attend_random_lists_isolated(batch):
+    """Attention alone on seeded random lists (neither side's selection).
+    40 lists run the attention kernel's small-batch shape (4 consumer warps,
+    12-slot ring); 64 (the switch-over) and 96 run the many-list shape (5
+    consumer warps, 10-slot ring), long lists included."""
+    w = W.make_workload("serving_ragged", seed=21, device="cuda", batch=batch, layers=1)
     st = DecodeState(w)
     G = w.group
     for trial, frac in enumerate([(0.0, 1.0), (0.0, 0.02), (0.9, 1.0)]):
