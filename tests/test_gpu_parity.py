@@ -130,31 +130,47 @@ def test_attend_random_lists_isolated(batch):
                 assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"{frac} r{r} j{j}: {ma:.3g} {rl:.3g}"
 
 
-def test_attend_empty_and_single_lists():
-    w = W.make_workload("tiny", seed=2, device="cuda", batch=3, context=(16 * 40, 16 * 40 + 3, 16 * 40))
+@pytest.mark.parametrize("batch", [3, 32])
+def test_attend_empty_and_single_lists(batch):
+    """Empty lists give zeros; one full page, the tail page alone and a whole
+    context give the oracle's attention.  Every list keeps the contract: a
+    request's partial tail page, when it has one and the list is not empty,
+    is the list's last entry.  3 requests (6 lists) run the attention
+    kernel's small-batch shape, 32 requests (64 lists) its many-list shape."""
+    ctx = tuple(16 * 40 + (3 if r % 3 == 1 else 0) for r in range(batch))
+    w = W.make_workload("tiny", seed=2, device="cuda", batch=batch, context=ctx)
     st = DecodeState(w)
-    B, Hkv = 3, 2
+    B, Hkv = batch, w.spec.kv_heads
     phys = np.full((B, Hkv, w.max_pages), -1, np.int32)
     lengths = np.zeros((B, Hkv), np.int32)
     logical = [[np.zeros(0, np.int32) for _ in range(Hkv)] for _ in range(B)]
-    logical[0][1] = np.array([7], np.int32)                         # one full page
-    logical[1][0] = np.array([40], np.int32)                        # the tail page alone (3 tokens)
-    logical[2][1] = np.arange(40, dtype=np.int32)                   # everything
     for r in range(B):
+        F, T = ctx[r] // 16, int(ctx[r] % 16 != 0)
         for j in range(Hkv):
+            kind = (r * Hkv + j) % 4
+            if kind == 1:      # one full page, and the tail, which the contract puts last
+                logical[r][j] = np.array([7, F] if T else [7], np.int32)
+            elif kind == 2:    # the tail page alone (3 tokens), or the last full page
+                logical[r][j] = np.array([F if T else F - 1], np.int32)
+            elif kind == 3:    # everything
+                logical[r][j] = np.arange(F + T, dtype=np.int32)
             lst = logical[r][j]
             phys[r, j, :len(lst)] = w.page_table[r, lst]
             lengths[r, j] = len(lst)
     out = torch.full_like(st.out[0], 7.0)
     st.attend_layer(0, torch.from_numpy(phys).cuda(), torch.from_numpy(lengths).cuda(), out)
     torch.cuda.synchronize()
+    assert st.device_status() == 0
     oh = out.cpu().numpy()
+    G = w.group
     for r in range(B):
         for j in range(Hkv):
+            if len(logical[r][j]) == 0:
+                assert np.all(oh[r, j * G:(j + 1) * G] == 0.0), f"r{r} j{j}: empty list not zero"
+                continue
             ref = H.UnitData(w, 0, r, j).attend(logical[r][j])
-            ma, rl = H.out_errors(oh[r, j * 4:(j + 1) * 4], ref)
-            assert ma <= H.MAX_ABS and rl <= H.REL_L2
-    assert np.all(oh[0, 0:4] == 0.0)                                # empty list -> zeros
+            ma, rl = H.out_errors(oh[r, j * G:(j + 1) * G], ref)
+            assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"r{r} j{j}: {ma:.3g} {rl:.3g}"
 
 
 # ------------------------------------------------------------------ graph, status, determinism
