@@ -131,7 +131,7 @@ __device__ __forceinline__ int block_of(long long g, long long W, long long n)
     return static_cast<int>(((g + 1) * n - 1) / W);
 }
 
-// Named barrier of the 4 consumer warps (the producer warp never joins it).
+// Named barrier of the NW consumer warps (the producer warp never joins it).
 template <int NW>
 __device__ __forceinline__ void consumer_bar()
 {
