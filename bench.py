@@ -47,10 +47,10 @@ FALLBACK_HBM_GBS = 6800.0
 # requests, 64 lists, 184,984 entries).  The digest names the kernel sources
 # the captures were taken on; once they change the figure is withheld
 # (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "9f65ee9eec44119e4cbf9b49dac00645617b155f6eaeec3f5ce649d497b01c81",
+ATTEND_TRAFFIC = {"sources_sha256": "d07f992bee27fd0cdae6f10959b65ff46177aa59f62afdf42389c87e34572831",
                   "many_lists_from": 64,
-                  "dram_bytes_per_entry": {"few_lists": (537305088 + 3194624) / 65536,
-                                           "many_lists": (1516674048 + 3329536) / 184984}}
+                  "dram_bytes_per_entry": {"few_lists": (537294336 + 3244544) / 65536,
+                                           "many_lists": (1516678912 + 3335936) / 184984}}
 
 
 def attend_sources_digest() -> str:
