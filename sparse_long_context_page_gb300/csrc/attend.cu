@@ -420,10 +420,20 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, kBlocksPerSm)
                         const uint32_t dst = smem_u32(stage + slot * kSlotBytes);
                         const int row = (cp * a.hkv + cu % a.hkv) * kPageSize;
                         mbar_arrive_expect_tx(full, kSlotBytes);
-                        tma_load_2d(dst, &tmap_k, 0, row, full);
-                        tma_load_2d(dst + kHalfBox, &tmap_k, 64, row, full);
-                        tma_load_2d(dst + 2 * kHalfBox, &tmap_v, 0, row, full);
-                        tma_load_2d(dst + 3 * kHalfBox, &tmap_v, 64, row, full);
+                        if constexpr (kConsumerWarps == kFewWarps) {
+                            // small batches: K/V are read once and must not push the
+                            // merge partials and list data out of L2
+                            const uint64_t pol = l2_evict_first();
+                            tma_load_2d_hint(dst, &tmap_k, 0, row, full, pol);
+                            tma_load_2d_hint(dst + kHalfBox, &tmap_k, 64, row, full, pol);
+                            tma_load_2d_hint(dst + 2 * kHalfBox, &tmap_v, 0, row, full, pol);
+                            tma_load_2d_hint(dst + 3 * kHalfBox, &tmap_v, 64, row, full, pol);
+                        } else {
+                            tma_load_2d(dst, &tmap_k, 0, row, full);
+                            tma_load_2d(dst + kHalfBox, &tmap_k, 64, row, full);
+                            tma_load_2d(dst + 2 * kHalfBox, &tmap_v, 0, row, full);
+                            tma_load_2d(dst + 3 * kHalfBox, &tmap_v, 64, row, full);
+                        }
                     } else {
                         mbar_arrive(full);
                     }
