@@ -45,3 +45,16 @@ def test_step_bytes_low_bit_records():
     w = _workload()
     _, _, _, parts = bench.step_bytes(w, LENGTHS, 0.99, summ_page_bytes=288)
     assert parts["summaries"] == 4 * 288        # one record per full page
+
+
+def test_traffic_shape_threshold_matches_the_kernel():
+    """The benchmark picks the DRAM-traffic figure of the attention kernel's
+    block shape by the number of lists; its switch-over must be the kernel's."""
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(bench.__file__), "sparse_long_context_page_gb300", "csrc",
+                            "attend.cu")).read()
+    m = re.search(r"constexpr int kManyUnits = (\d+);", src)
+    assert m, "kManyUnits not found in attend.cu"
+    assert int(m.group(1)) == bench.ATTEND_TRAFFIC["many_lists_from"]
+    assert set(bench.ATTEND_TRAFFIC["dram_bytes_per_entry"]) == {"few_lists", "many_lists"}
