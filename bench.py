@@ -39,23 +39,26 @@ sys.path.insert(0, ROOT)
 METRIC = "µs/decode-attn step & achieved HBM GB/s at 128k ctx, γ=0.99 vs γ=1 dense"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) that k_attend moves per list entry, i.e. per kept
-# (page, KV head) with its 4 KB of K and 4 KB of V, from one-pass ncu captures
-# of dense launches (dram__bytes_read.sum + dram__bytes_write.sum divided by the
-# entries), one per block shape of the kernel: below 64 lists (llama8b_128k,
-# 8 lists, 65,536 entries) and from 64 lists on (serving_ragged cut to 8
-# requests, 64 lists, 184,984 entries).  The digest names the kernel sources
+# DRAM bytes (read + write) that the attention kernels move per list entry,
+# i.e. per kept (page, KV head) with its 4 KB of K and 4 KB of V, from
+# one-pass ncu captures of dense launches (dram__bytes_read.sum +
+# dram__bytes_write.sum divided by the entries): the single-launch selection +
+# attention of small batches (k_select_attend) and k_attend's two block shapes
+# (below 64 lists and from 64 lists on).  The digest names the kernel sources
 # the captures were taken on; once they change the figure is withheld
 # (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "4a8e9be87596107227aebc6157a647938b89c7fee8ae071cca0c1106b2e27888",
+ATTEND_TRAFFIC = {"sources_sha256": "",
                   "many_lists_from": 64,
-                  "dram_bytes_per_entry": {"few_lists": (537230848 + 2864896) / 65536,
-                                           "many_lists": (1516680448 + 3328512) / 184984}}
+                  "dram_bytes_per_entry": {"fused": None, "few_lists": None, "many_lists": None}}
+ATTEND_SOURCES = ("attend_core.cuh", "attend.cu", "fused.cu", "select_core.cuh", "moira_device.cuh")
+
+# The other configurations reported next to the headline (γ = 0.99 each).
+OTHER_WORKLOADS = ("llama8b_32k", "serving_ragged", "stress_regimes")
 
 
 def attend_sources_digest() -> str:
     h = hashlib.sha256()
-    for f in ("attend.cu", "moira_device.cuh"):
+    for f in ATTEND_SOURCES:
         with open(os.path.join(ROOT, "sparse_long_context_page_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -287,6 +290,128 @@ def time_parts(st, gamma, steps, warmup):
     return out[0], out[1]
 
 
+def time_score(st, steps, warmup):
+    """In-graph duration of the page-scoring kernel alone, per layer: the
+    layers' k_score launches captured in one CUDA graph and replayed between
+    CUDA events on the capturing stream."""
+    g = capture_fn(lambda: [st.score_layer(l) for l in range(st.layers)])
+    ms, _ = time_graph(g, steps, warmup, 1)
+    del g
+    return ms / st.layers
+
+
+def kernel_roofline(st, w, head, lengths, spb, step_ms, peak, steps, warmup, two_launch=None):
+    """The step's dominant kernel, its algorithmic bytes per launch (K and V
+    of the kept tokens, q, out) and its average in-graph launch duration.
+    Small batches run k_score then k_select_attend per layer: the latter's
+    duration is the step's per-layer time less the scoring kernel's (both
+    CUDA-event timed graphs).  Larger batches run k_score, k_select and
+    k_attend: k_attend's duration is timed in a graph of attention launches
+    alone (two_launch = time_parts' result)."""
+    import sparse_long_context_page_gb300 as moira
+    sp = w.spec
+    per_layer, _, _, parts = step_bytes(w, lengths, head, spb)
+    att_bytes = per_layer - parts["summaries"] / sp.layers      # K/V of kept tokens + q + out
+    entries = float(lengths.reshape(sp.layers, -1).sum(axis=1).mean())     # list entries per launch
+    fused = False          # the decode step runs k_score, k_select, k_attend per layer
+    score_ms = time_score(st, steps, warmup)
+    if fused:
+        kernel, dur_ms, shape = "k_select_attend", step_ms / sp.layers - score_ms, "fused"
+    else:
+        if two_launch is None:
+            two_launch = time_parts(st, head, steps, warmup)
+        kernel, dur_ms = "k_attend", two_launch[1]
+        shape = "many_lists" if sp.batch * sp.kv_heads >= ATTEND_TRAFFIC["many_lists_from"] else "few_lists"
+    gbs = float(att_bytes.mean() / (dur_ms * 1e6))
+    per_entry = ATTEND_TRAFFIC["dram_bytes_per_entry"].get(shape)
+    traffic = None
+    if per_entry and ATTEND_TRAFFIC["sources_sha256"] == attend_sources_digest():
+        traffic = int(round(per_entry * entries))
+    how = ("step per layer less the scoring kernel per layer (two CUDA-event timed graphs)" if fused
+           else "graph of the layers' attention launches alone, CUDA events")
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": peak[0], "unit": "GB/s",
+            "frac": round(gbs / peak[0], 4), "peak_source": peak[1], "traffic": traffic,
+            "traffic_how": (f"ncu DRAM bytes per list entry of a dense launch of the same kernel "
+                            f"({shape.replace('_', ' ')}) x entries per launch" if traffic is not None else
+                            "null: no ncu capture of the current attention sources"),
+            "entries_per_launch": round(entries, 1), "bytes_per_launch": int(att_bytes.mean()),
+            "duration_us": round(dur_ms * 1e3, 2), "duration_how": how,
+            "score_us_per_layer": round(score_ms * 1e3, 2)}, fused
+
+
+def load_balance(st, w, gamma):
+    """Per-block attention times of one step, from the load-balance build of
+    the library (the same kernels with %globaltimer stamps): per attention
+    launch, the blocks' time from their plan to the end of their merges;
+    max / mean over the blocks that hold pages, and the launch's span from
+    the first start to the last end.  One eager step; median over layers."""
+    import sparse_long_context_page_gb300 as moira
+    from sparse_long_context_page_gb300 import build as B
+    nb = moira.attend_grid_blocks()
+    buf = torch.zeros((w.spec.layers, nb, 2), dtype=torch.int64, device=st.device)
+    with moira._binding.library_variant(B.LIB_CTA_TIMES):
+        moira._binding.set_cta_times(buf, w.spec.layers)
+        st.step(gamma)
+        torch.cuda.synchronize()
+        moira._binding.set_cta_times(None, 0)
+    t = buf.cpu().numpy()
+    ratios, spans = [], []
+    for l in range(w.spec.layers):
+        s, e = t[l, :, 0], t[l, :, 1]
+        ok = s > 0
+        d = (e[ok] - s[ok]).astype(np.float64)
+        if len(d):
+            ratios.append(float(d.max() / d.mean()))
+            spans.append(float(e[ok].max() - s[ok].min()) / 1e3)
+    return {"max_over_mean_block_time": round(float(np.median(ratios)), 4),
+            "max_over_mean_worst_layer": round(float(np.max(ratios)), 4),
+            "launch_span_us_median": round(float(np.median(spans)), 2),
+            "how": "load-balance build (libmoira_cta_times.so): per attention launch, each block's time "
+                   "from its plan to the end of its merges; max/mean over blocks with pages; median over layers"}
+
+
+def other_workload(name, args, peak, local):
+    """One more configuration at gamma = 0.99: the step (one graph) and the
+    dense step, the step's HBM rate on the bytes it must read, and the
+    dominant kernel's roofline."""
+    import sparse_long_context_page_gb300 as moira
+    from sparse_long_context_page_gb300 import workloads as W
+    from sparse_long_context_page_gb300.state import DecodeState
+    t0 = time.time()
+    w = W.make_workload(name, seed=args.seed, device=f"cuda:{local}")
+    st = DecodeState(w)
+    st.summarize()
+    spb = moira.summary_page_bytes(st.shape, moira.SUMM_BF16)
+    torch.cuda.synchronize()
+    gen_s = time.time() - t0
+    head = float(np.float32(0.99))
+    out = {}
+    steps = max(3, args.steps // 2)
+    for gm in (1.0, head):
+        g = capture_step(st, gm)
+        ms, _ = time_graph(g, steps, args.warmup, 1)
+        del g
+        out[gm] = ms
+    assert moira.read_device_status(st.ws) == 0, f"device status word set during {name}"
+    lengths = st.lengths.cpu().numpy()          # the gamma = 0.99 step ran last
+    _, total, frac, _ = step_bytes(w, lengths, head, spb)
+    roof, fused = kernel_roofline(st, w, head, lengths, spb, out[head], peak, steps, args.warmup)
+    res = {"workload": f"{name}: {w.spec.batch} request(s), {int(w.seq_lens.min())}..{int(w.seq_lens.max())} "
+                       f"tokens, {w.spec.layers} layer(s), 32 q / 8 kv heads",
+           "us_per_step": round(out[head] * 1e3, 2), "dense_us_per_step": round(out[1.0] * 1e3, 2),
+           "speedup_vs_dense": round(out[1.0] / out[head], 3), "pages_read_fraction": round(frac, 4),
+           "step_hbm_gbs": round(total / out[head] / 1e6, 1),
+           "step_hbm_frac_of_measured": round(total / out[head] / 1e6 / peak[0], 4),
+           "single_launch_select_attend": bool(fused), "roofline": roof,
+           "load_balance": load_balance(st, w, head)}
+    log(f"[bench] {name}: generated in {gen_s:.1f}s; {out[head] * 1e3:.1f} us/step "
+        f"({res['step_hbm_frac_of_measured']:.3f} of peak), dense {out[1.0] * 1e3:.1f}, "
+        f"{roof['kernel']} {roof['frac']:.3f}")
+    del st, w
+    torch.cuda.empty_cache()
+    return res
+
+
 def capture_fn(fn):
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -438,20 +563,12 @@ def run_ours(args):
         del g
     assert moira.read_device_status(st.ws) == 0, "device status word set during the benchmark"
 
-    # dominant kernel: attention, average in-graph launch duration at the headline gamma
-    sel_ms, att_ms = time_parts(st, head, max(3, args.steps // 2), args.warmup)
-    lengths = st.lengths.cpu().numpy()
-    per_layer, _, _, _ = step_bytes(w, lengths, head, spb)
-    summ_layer = results[head]["parts"]["summaries"] / sp.layers
-    att_bytes = per_layer - summ_layer                    # K/V of kept tokens + q + out
-    att_gbs = float(att_bytes.mean() / (att_ms * 1e6))
-    entries = float(lengths.reshape(sp.layers, -1).sum(axis=1).mean())     # list entries per launch
-    digest = attend_sources_digest()
-    shape = "many_lists" if sp.batch * sp.kv_heads >= ATTEND_TRAFFIC["many_lists_from"] else "few_lists"
-    per_entry = ATTEND_TRAFFIC["dram_bytes_per_entry"][shape]
-    traffic = None
-    if per_entry and ATTEND_TRAFFIC["sources_sha256"] == digest:
-        traffic = int(round(per_entry * entries))
+    # dominant kernel and the layer's split (in-graph, CUDA events)
+    two = time_parts(st, head, max(3, args.steps // 2), args.warmup)
+    roof, fused = kernel_roofline(st, w, head, results[head]["lengths"], spb, results[head]["ms"],
+                                  (peak, peak_src), max(3, args.steps // 2), args.warmup, two_launch=two)
+    sel_ms, att_ms = two
+    balance = load_balance(st, w, head)
 
     # the same step under the fixed-budget and relative-threshold rules, tuned
     # to read the same pages as coverage at the headline gamma; quality is the
@@ -509,7 +626,14 @@ def run_ours(args):
 
     hd = results[head]
     dense = results[1.0]
-    launches_per_step = sp.layers * 3
+    launches_per_step = sp.layers * (2 if fused else 3)
+    # the other configurations (the headline's buffers are freed first)
+    others = None
+    if not args.no_others and world == 1:
+        del st, w
+        torch.cuda.empty_cache()
+        others = [other_workload(nm, args, (peak, peak_src), local) for nm in OTHER_WORKLOADS
+                  if nm != args.workload]
     line = {
         "metric": METRIC,
         "value": round(hd["ms"] * 1e3, 2),
@@ -537,17 +661,16 @@ def run_ours(args):
         "gamma_0.98": {"us_per_step": round(results[gammas[1]]["ms"] * 1e3, 2),
                        "hbm_gbs": round(results[gammas[1]]["bytes"] / results[gammas[1]]["ms"] / 1e6, 1),
                        "speedup_vs_dense": round(dense["ms"] / results[gammas[1]]["ms"], 3)},
-        "per_layer_us": {"select": round(sel_ms * 1e3, 2), "attend": round(att_ms * 1e3, 2),
-                         "how": "in-graph, 32 layers of one half per graph, CUDA events"},
-        "roofline": {"kernel": "k_attend", "bound": "hbm", "achieved": round(att_gbs, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(att_gbs / peak, 4),
-                     "peak_source": peak_src, "traffic": traffic,
-                     "traffic_how": (f"ncu DRAM bytes per list entry of a dense launch of the same block "
-                                     f"shape ({shape.replace('_', ' ')}) x entries per launch"
-                                     if traffic is not None else
-                                     "null: no ncu capture of the current k_attend sources"),
-                     "entries_per_launch": round(entries, 1),
-                     "bytes_per_launch": int(att_bytes.mean())},
+        "per_layer_us": {"step": round(hd["ms"] * 1e3 / sp.layers, 2),
+                         "score": roof["score_us_per_layer"],
+                         "select_attend": roof["duration_us"] if fused else None,
+                         "two_launch_select": round(sel_ms * 1e3, 2), "two_launch_attend": round(att_ms * 1e3, 2),
+                         "how": "in-graph, CUDA events: the step graph; graphs of the layers' scoring "
+                                "launches alone; and, for comparison, the two-launch form (score + "
+                                "k_select, then k_attend) timed half by half"},
+        "single_launch_select_attend": bool(fused),
+        "roofline": roof,
+        "load_balance": balance,
         "e2e": ({"value": round(e2e_ms * 1e3, 2), "unit": "us/step",
                  "h2d_bytes_per_step": int(q_host.numel() * 2),
                  "d2h_bytes_per_step": int(out_host.numel() * 4),
@@ -559,6 +682,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "rules_at_equal_pages": rules,
         "summary_formats": formats,
+        "other_workloads": others,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -622,6 +746,8 @@ def main():
     ap.add_argument("--summaries", default="bf16", choices=["bf16", "q8", "q2"],
                     help="page-summary format of the measured step (bf16 is the headline; the "
                          "low-bit formats are for profiling: no e2e or CPU legs)")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the other configurations (32k, serving, stress) after the headline")
     ap.add_argument("--batch", type=int, default=0,
                     help="fewer requests than the workload's (small profiling cases only)")
     args = ap.parse_args()

@@ -39,9 +39,15 @@
  *     and a status other than MOIRA_OK is returned.
  *   - Problems only visible on the device (a physical page id outside the
  *     pool, a length out of range, a device wait that ran out) never trap:
- *     the kernel skips or clamps the offending item and ORs a MOIRA_DEV_* bit
- *     into the status word kept in the workspace; read it with
+ *     the kernel skips or clamps the offending item and ORs a MOIRA_DEV_*
+ *     bit into the status word kept in the workspace; read it with
  *     moira_read_device_status().
+ *   - Every device wait is bounded (2 s).  The first wait of a launch that
+ *     runs out sets MOIRA_DEV_TIMEOUT, and from then on every wait of that
+ *     launch, and of every later launch that starts while the bit is set,
+ *     gives up at once, so a lost copy costs about one limit per step.  The
+ *     results are then invalid: read and clear the status and call
+ *     moira_workspace_init before the workspace is used again.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).
  */
 #ifndef MOIRA_H
@@ -268,9 +274,58 @@ moira_status moira_attend(const moira_shape *shape, const void *q, const void *k
                           float sm_scale, float *out, void *workspace, size_t ws_bytes,
                           moira_stream_t stream);
 
+/* One layer's selection and attention: exactly the lists and lengths of
+ * moira_select, and the output of moira_attend over them (within the
+ * attention tolerance: the fp32 summation order may differ).  Arguments as
+ * in those two calls; out: fp32 [batch][Hq][d].
+ * For small batches (fewer than 64 (request, KV head) lists, and at most
+ * 512 pages per block when each list's pages are split over
+ * grid / lists blocks of the attention grid: about 19k pages per request at
+ * 8 lists on 152 SMs) the selection is spread over the whole attention grid
+ * and runs in the same launch as the attention (the "MOIRA" abstract's
+ * self-planning attention with its selection cost taken off the critical
+ * path): after the score kernel, one launch whose blocks meet at barriers
+ * inside it, so every block of the grid must be resident at once (checked
+ * once per device; another kernel that holds SMs for longer than the device
+ * wait limit makes the launch report MOIRA_DEV_TIMEOUT).  Larger batches run
+ * moira_select then moira_attend. */
+moira_status moira_select_attend(const moira_shape *shape, const void *q, const void *summ,
+                                 const void *k_pool, const void *v_pool, const int32_t *page_table,
+                                 const int32_t *seq_lens, int32_t batch, int32_t max_pages, float gamma,
+                                 float sm_scale, int32_t *lists, int32_t *lengths, float *out,
+                                 void *workspace, size_t ws_bytes, moira_stream_t stream);
+
+/* moira_select_attend reading summaries in `format` (moira_summ_format), as
+ * moira_select_ex does with the coverage rule.  MOIRA_SUMM_BF16 is exactly
+ * moira_select_attend. */
+moira_status moira_select_attend_ex(const moira_shape *shape, int32_t format, const void *q,
+                                    const void *summ, const void *k_pool, const void *v_pool,
+                                    const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                                    int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
+                                    int32_t *lengths, float *out, void *workspace, size_t ws_bytes,
+                                    moira_stream_t stream);
+
+/* The page-scoring kernel of moira_select_ex alone: the logits of every
+ * (request, KV head, full page) against the summaries, reduced to per-chunk
+ * softmax statistics in the workspace (the estimator's first half; the
+ * "MOIRA" abstract's estimated mass needs them).  Its results are internal
+ * to the workspace; the call exists to time how a layer's work splits
+ * between scoring and the rest.  Arguments and errors as moira_select_ex. */
+moira_status moira_score_ex(const moira_shape *shape, int32_t format, const void *q, const void *summ,
+                            const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                            int32_t max_pages, float sm_scale, void *workspace, size_t ws_bytes,
+                            moira_stream_t stream);
+
+/* 1 if moira_select_attend (and the coverage-rule decode step) takes the
+ * single-launch form for these sizes on the current device, 0 if it runs
+ * moira_select then moira_attend (or the arguments are invalid). */
+int32_t moira_select_attend_is_fused(const moira_shape *shape, int32_t batch, int32_t max_pages);
+
 /* One whole decode-attention step: for layer l = 0 .. num_layers-1,
  * moira_select then moira_attend on that layer's slices, in order on one
- * stream (the per-layer calls above, looped on the host).
+ * stream (the per-layer calls above, looped on the host).  The output
+ * equals moira_select_attend's per layer bit for bit (same lists, same
+ * attention plan and data path).
  *   q_all      : bf16 [L][batch][Hq][d]
  *   k_pool_all, v_pool_all : bf16 [L][P][Hkv][S][d]
  *   summ_all   : bf16 [L][P][Hkv][d]
@@ -344,6 +399,23 @@ moira_status moira_select_noalloc(const moira_shape *shape, const void *q, const
  * leaves the context usable.  No paper counterpart. */
 moira_status moira_diag_wait_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns,
                                      moira_stream_t stream);
+
+/* Diagnostic of the give-up rule of the device waits: one block waits on
+ * `n_waits` (1 .. 4096) barriers that nothing completes, one after the
+ * other, the way the kernels wait: the first wait runs out after `limit_ns`
+ * (1 .. 10^10) and sets MOIRA_DEV_TIMEOUT, and every later wait of the block
+ * gives up at once, so the launch takes about one limit, not n_waits.  No
+ * paper counterpart. */
+moira_status moira_diag_wait_chain(void *workspace, size_t ws_bytes, uint64_t limit_ns, int32_t n_waits,
+                                   moira_stream_t stream);
+
+/* Diagnostic of the inter-block barrier of moira_select_attend: `blocks`
+ * (1 .. SM count) blocks meet at a barrier sized for one block more, so it
+ * never completes; each block gives up after `limit_ns` and sets
+ * MOIRA_DEV_TIMEOUT.  Uses (and clears) bytes 128..255 of the workspace.
+ * No paper counterpart. */
+moira_status moira_diag_barrier_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns, int32_t blocks,
+                                        moira_stream_t stream);
 
 /* Synchronise `stream`, copy the device status word (MOIRA_DEV_* bits) to
  * *status_out (HOST pointer) and clear it when `clear` is non-zero.  A host

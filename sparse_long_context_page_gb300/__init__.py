@@ -13,7 +13,7 @@ from ._binding import (DEV_BADLEN, DEV_BADPAGE, DEV_TIMEOUT, EXPORTS, GROUP, HEA
                        RULE_TOPK, SUMM_BF16, SUMM_Q2, SUMM_Q8, MoiraError, Shape, append_kv, attend,
                        attend_grid_blocks, decode_step, decode_step_ex, decode_step_host,
                        library_path, load_library, make_summaries, make_workspace,
-                       read_device_status, select, select_ex, select_rule, shape_of,
+                       read_device_status, select, select_attend, select_attend_is_fused, select_ex, select_rule, shape_of,
                        summary_page_bytes, update_summaries, workspace_bytes, workspace_init)
 
 __all__ = ["DEV_BADLEN", "DEV_BADPAGE", "DEV_TIMEOUT", "EXPORTS", "GROUP", "HEAD_DIM",
@@ -21,5 +21,5 @@ __all__ = ["DEV_BADLEN", "DEV_BADPAGE", "DEV_TIMEOUT", "EXPORTS", "GROUP", "HEAD
            "RULE_TOPK", "SUMM_BF16", "SUMM_Q2", "SUMM_Q8", "MoiraError", "Shape", "append_kv",
            "attend", "attend_grid_blocks", "decode_step", "decode_step_ex", "decode_step_host",
            "library_path", "load_library", "make_summaries", "make_workspace",
-           "read_device_status", "select", "select_ex", "select_rule", "shape_of",
+           "read_device_status", "select", "select_attend", "select_attend_is_fused", "select_ex", "select_rule", "shape_of",
            "summary_page_bytes", "update_summaries", "workspace_bytes", "workspace_init"]

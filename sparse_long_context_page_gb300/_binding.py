@@ -8,6 +8,7 @@ an exception is raised.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -33,7 +34,8 @@ EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summar
            "moira_read_device_status", "moira_attend_grid_blocks", "moira_status_string",
            "moira_select_noalloc", "moira_select_rule", "moira_append_kv",
            "moira_diag_wait_timeout", "moira_summary_page_bytes", "moira_update_summaries_ex",
-           "moira_append_kv_ex", "moira_select_ex", "moira_decode_step_ex")
+           "moira_append_kv_ex", "moira_select_ex", "moira_decode_step_ex", "moira_select_attend",
+           "moira_select_attend_ex", "moira_select_attend_is_fused", "moira_score_ex", "moira_diag_wait_chain", "moira_diag_barrier_timeout")
 
 # page rules of moira_select_rule (moira_rule in include/moira.h)
 RULE_COVERAGE, RULE_TOPK, RULE_TOPDELTA = 0, 1, 2
@@ -72,7 +74,25 @@ def load_library(build_if_missing: bool = True):
         if not build_if_missing:
             raise RuntimeError(f"{path} is missing; build it with sparse_long_context_page_gb300.build")
         _build.build()
-    lib = ctypes.CDLL(path)
+    _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+@contextlib.contextmanager
+def library_variant(path: str):
+    """Route every call of this module through another build of the library
+    (e.g. the load-balance build, build.LIB_CTA_TIMES) inside the block."""
+    global _lib
+    saved = load_library()
+    _lib = _declare(ctypes.CDLL(path))
+    try:
+        yield _lib
+    finally:
+        _lib = saved
+
+
+def _declare(lib):
+    """Argument and result types of the C ABI on a loaded library."""
     sp = ctypes.POINTER(Shape)
     lib.moira_workspace_bytes.argtypes = [sp, _i32, _i32]
     lib.moira_workspace_bytes.restype = ctypes.c_size_t
@@ -121,9 +141,27 @@ def load_library(build_if_missing: bool = True):
                                          _i32, ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp,
                                          ctypes.c_size_t, _vp]
     lib.moira_decode_step_ex.restype = ctypes.c_int
+    lib.moira_select_attend.argtypes = [sp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float,
+                                        ctypes.c_float, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.moira_select_attend.restype = ctypes.c_int
+    lib.moira_select_attend_ex.argtypes = [sp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+                                           ctypes.c_float, ctypes.c_float, _vp, _vp, _vp, _vp,
+                                           ctypes.c_size_t, _vp]
+    lib.moira_select_attend_ex.restype = ctypes.c_int
+    lib.moira_score_ex.argtypes = [sp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, ctypes.c_float, _vp,
+                                   ctypes.c_size_t, _vp]
+    lib.moira_score_ex.restype = ctypes.c_int
+    lib.moira_select_attend_is_fused.argtypes = [sp, _i32, _i32]
+    lib.moira_select_attend_is_fused.restype = _i32
+    lib.moira_diag_wait_chain.argtypes = [_vp, ctypes.c_size_t, ctypes.c_uint64, _i32, _vp]
+    lib.moira_diag_wait_chain.restype = ctypes.c_int
+    lib.moira_diag_barrier_timeout.argtypes = [_vp, ctypes.c_size_t, ctypes.c_uint64, _i32, _vp]
+    lib.moira_diag_barrier_timeout.restype = ctypes.c_int
     lib.moira_status_string.argtypes = [ctypes.c_int]
     lib.moira_status_string.restype = ctypes.c_char_p
-    _lib = lib
+    if hasattr(lib, "moira_set_cta_times"):          # the load-balance build
+        lib.moira_set_cta_times.argtypes = [_vp, _i32]
+        lib.moira_set_cta_times.restype = ctypes.c_int
     return lib
 
 
@@ -278,6 +316,42 @@ def select_ex(shape: Shape, fmt: int, q, summ, page_table, seq_lens, rule: int, 
            "moira_select_ex")
 
 
+def select_attend(shape: Shape, q, summ, k_pool, v_pool, page_table, seq_lens, gamma: float,
+                  sm_scale: float, lists, lengths, out, ws, stream=None, fmt: int = SUMM_BF16):
+    """One layer's coverage selection and attention (moira_select_attend /
+    _ex): the lists and lengths of select(), the output of attend() over them."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    args = (_dev(q, "q", torch.bfloat16), _summ(summ, fmt), _dev(k_pool, "k_pool", torch.bfloat16),
+            _dev(v_pool, "v_pool", torch.bfloat16), _dev(page_table, "page_table", torch.int32, 2),
+            _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages, float(gamma), float(sm_scale),
+            _dev(lists, "lists", torch.int32), _dev(lengths, "lengths", torch.int32),
+            _dev(out, "out", torch.float32), _dev(ws, "workspace", torch.uint8), ws.numel(), _stream(stream))
+    if fmt == SUMM_BF16:
+        st = lib.moira_select_attend(ctypes.byref(shape), *args)
+    else:
+        st = lib.moira_select_attend_ex(ctypes.byref(shape), int(fmt), *args)
+    _check(st, "moira_select_attend")
+
+
+def score(shape: Shape, q, summ, page_table, seq_lens, sm_scale: float, ws, stream=None,
+          fmt: int = SUMM_BF16):
+    """The page-scoring kernel alone (moira_score_ex): results stay in the
+    workspace; for timing how a layer's work splits."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    _check(lib.moira_score_ex(ctypes.byref(shape), int(fmt), _dev(q, "q", torch.bfloat16), _summ(summ, fmt),
+                              _dev(page_table, "page_table", torch.int32, 2),
+                              _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages, float(sm_scale),
+                              _dev(ws, "workspace", torch.uint8), ws.numel(), _stream(stream)),
+           "moira_score_ex")
+
+
+def select_attend_is_fused(shape: Shape, batch: int, max_pages: int) -> bool:
+    """Whether select_attend takes its single-launch form for these sizes."""
+    return bool(load_library().moira_select_attend_is_fused(ctypes.byref(shape), int(batch), int(max_pages)))
+
+
 def attend(shape: Shape, q, k_pool, v_pool, lists, lengths, seq_lens, max_pages: int,
            sm_scale: float, out, ws, stream=None):
     """Attention of one layer over the listed pages; writes fp32 ``out``."""
@@ -374,6 +448,34 @@ def diag_wait_timeout(ws, limit_ns: int, stream=None):
     lib = load_library()
     _check(lib.moira_diag_wait_timeout(_dev(ws, "workspace", torch.uint8), ws.numel(), int(limit_ns),
                                        _stream(stream)), "moira_diag_wait_timeout")
+
+
+def diag_wait_chain(ws, limit_ns: int, n_waits: int, stream=None):
+    """Launch the give-up diagnostic: n_waits waits on barriers nothing
+    completes; the first runs out after ``limit_ns``, the rest give up at once."""
+    lib = load_library()
+    _check(lib.moira_diag_wait_chain(_dev(ws, "workspace", torch.uint8), ws.numel(), int(limit_ns),
+                                     int(n_waits), _stream(stream)), "moira_diag_wait_chain")
+
+
+def diag_barrier_timeout(ws, limit_ns: int, blocks: int, stream=None):
+    """Launch the inter-block barrier diagnostic: ``blocks`` blocks meet at a
+    barrier that never completes and give up after ``limit_ns``."""
+    lib = load_library()
+    _check(lib.moira_diag_barrier_timeout(_dev(ws, "workspace", torch.uint8), ws.numel(), int(limit_ns),
+                                          int(blocks), _stream(stream)), "moira_diag_barrier_timeout")
+
+
+def set_cta_times(buf, max_launches: int):
+    """Load-balance build only (inside library_variant(build.LIB_CTA_TIMES)):
+    the next max_launches attention launches record each block's (start, end)
+    %globaltimer ns into buf, int64 [max_launches][grid blocks][2] on the
+    device; None, 0 stops recording."""
+    lib = load_library()
+    if not hasattr(lib, "moira_set_cta_times"):
+        raise RuntimeError("set_cta_times needs the load-balance build (build.LIB_CTA_TIMES)")
+    ptr = None if buf is None else _dev(buf, "cta_times", torch.int64)
+    _check(lib.moira_set_cta_times(ptr, int(max_launches)), "moira_set_cta_times")
 
 
 def attend_grid_blocks() -> int:

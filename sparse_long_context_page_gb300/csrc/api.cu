@@ -9,6 +9,9 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/moira.h"
+#ifdef MOIRA_CTA_TIMES
+#include "../../include/moira_cta_times.h"
+#endif
 #include "moira_device.cuh"
 #include "moira_launch.h"
 
@@ -138,10 +141,15 @@ moira_status select_impl(const moira_shape *shape, int32_t fmt, const void *q, c
                                      lengths, status, stream));
 }
 
+// The next layer's summaries are brought into L2 by the attention launch when
+// they fit comfortably (one request's summaries; a serving batch's do not).
+constexpr size_t kNextSummMaxBytes = 48u << 20;
+
 moira_status attend_impl(const moira_shape *shape, const void *q, const void *k_pool,
                          const void *v_pool, const int32_t *lists, const int32_t *lengths,
                          const int32_t *seq_lens, int32_t batch, int32_t max_pages, float sm_scale,
-                         float *out, void *ws, size_t ws_bytes, cudaStream_t stream)
+                         float *out, void *ws, size_t ws_bytes, cudaStream_t stream,
+                         const void *next_summ = nullptr, size_t next_summ_bytes = 0)
 {
     const WsLayout L = layout_for(shape, batch, max_pages);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -163,7 +171,87 @@ moira_status attend_impl(const moira_shape *shape, const void *q, const void *k_
     a.max_pages = max_pages;
     a.num_pages = shape->num_phys_pages;
     a.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    const bool pf = next_summ != nullptr && next_summ_bytes > 0 && next_summ_bytes <= kNextSummMaxBytes &&
+                    (reinterpret_cast<uintptr_t>(next_summ) & 15u) == 0;
+    a.next_summ = pf ? static_cast<const uint8_t *>(next_summ) : nullptr;
+    a.next_summ_bytes = pf ? next_summ_bytes : 0ull;
+#ifdef MOIRA_CTA_TIMES
+    a.cta_times = next_cta_times(attend_blocks());
+#endif
     return cuda_status(launch_attend(mk, mv, a, attend_blocks(), stream));
+}
+
+// One layer's selection and attention.  Small batches (fewer than 64 lists
+// of at most 16 chunks per selecting block) with the coverage rule run as
+// k_score then one k_select_attend launch; everything else as select_impl
+// then attend_impl.  Both give the same lists and lengths bit for bit.
+moira_status select_attend_impl(const moira_shape *shape, int32_t fmt, const void *q, const void *summ,
+                                const void *k_pool, const void *v_pool, const int32_t *page_table,
+                                const int32_t *seq_lens, int32_t batch, int32_t max_pages, int32_t rule,
+                                float param, float sm_scale, int32_t *lists, int32_t *lengths, float *out,
+                                void *ws, size_t ws_bytes, bool early, cudaStream_t stream)
+{
+    const int units = batch * shape->num_kv_heads;
+    const int blocks = attend_blocks();
+    if (rule != MOIRA_RULE_COVERAGE || !select_attend_fits(units, max_pages, blocks)) {
+        moira_status st = select_impl(shape, fmt, q, summ, page_table, seq_lens, batch, max_pages, rule, param,
+                                      sm_scale, lists, lengths, ws, ws_bytes, early, stream);
+        if (st != MOIRA_OK) return st;
+        return attend_impl(shape, q, k_pool, v_pool, lists, lengths, seq_lens, batch, max_pages, sm_scale, out,
+                           ws, ws_bytes, stream);
+    }
+    const WsLayout L = layout_for(shape, batch, max_pages);
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    const float gamma = param;
+    const bool dense = gamma >= 1.0f;
+    const float scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    uint32_t *status = reinterpret_cast<uint32_t *>(w + L.status);
+    float *scores = reinterpret_cast<float *>(w + L.scores);
+    float *chunks = reinterpret_cast<float *>(w + L.chunks);
+    if (!dense) {
+        cudaError_t e = launch_score(q, summ, fmt, page_table, seq_lens, batch, shape->num_q_heads,
+                                     shape->num_kv_heads, max_pages, shape->num_phys_pages, scale_log2, scores,
+                                     chunks, early, status, stream);
+        if (e != cudaSuccess) return MOIRA_ECUDA;
+    }
+    CUtensorMap mk, mv;
+    if (!make_pool_map(&mk, k_pool, shape) || !make_pool_map(&mv, v_pool, shape)) return MOIRA_ECUDA;
+    FusedArgs f;
+    f.at.q = q;
+    f.at.lists = lists;
+    f.at.lengths = lengths;
+    f.at.seq_lens = seq_lens;
+    f.at.out = out;
+    f.at.partials = reinterpret_cast<float *>(w + L.partials);
+    f.at.counters = reinterpret_cast<uint32_t *>(w + L.counters);
+    f.at.gcounters = reinterpret_cast<uint32_t *>(w + L.gcounters);
+    f.at.status = status;
+    f.at.hq = shape->num_q_heads;
+    f.at.hkv = shape->num_kv_heads;
+    f.at.units = units;
+    f.at.max_pages = max_pages;
+    f.at.num_pages = shape->num_phys_pages;
+    f.at.scale_log2 = scale_log2;
+    f.at.next_summ = nullptr;
+    f.at.next_summ_bytes = 0ull;
+#ifdef MOIRA_CTA_TIMES
+    f.at.cta_times = next_cta_times(blocks);
+#endif
+    f.weights = scores;
+    f.chunks = chunks;
+    f.page_table = page_table;
+    f.k_pool = static_cast<const uint8_t *>(k_pool);
+    f.v_pool = static_cast<const uint8_t *>(v_pool);
+    f.lists = lists;
+    f.lengths = lengths;
+    f.bars = reinterpret_cast<uint32_t *>(w + L.fbars);
+    f.l1hist = reinterpret_cast<uint32_t *>(w + L.fl1);
+    f.mass = reinterpret_cast<uint32_t *>(w + L.fmass);
+    f.target = dense ? 0ull : static_cast<unsigned long long>(std::ceil(static_cast<double>(gamma) * 0x1p31));
+    f.ld = weights_ld(max_pages);
+    f.ldc = chunks_ld(max_pages);
+    f.dense = dense ? 1 : 0;
+    return cuda_status(launch_select_attend(mk, mv, f, blocks, stream));
 }
 
 bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
@@ -188,6 +276,22 @@ bool valid_rule(int32_t rule, float param)
 }
 
 }  // namespace
+
+#ifdef MOIRA_CTA_TIMES
+// Load-balance build only (include/moira_cta_times.h): where the next
+// attention launches record their per-block times.
+static unsigned long long *g_cta_times = nullptr;
+static int g_cta_launches = 0;
+
+unsigned long long *moira::next_cta_times(int blocks)
+{
+    if (g_cta_times == nullptr || g_cta_launches <= 0) return nullptr;
+    unsigned long long *p = g_cta_times;
+    g_cta_times += 2 * static_cast<size_t>(blocks);
+    if (--g_cta_launches == 0) g_cta_times = nullptr;
+    return p;
+}
+#endif
 
 extern "C" {
 
@@ -318,6 +422,67 @@ moira_status moira_attend(const moira_shape *shape, const void *q, const void *k
                        sm_scale, out, workspace, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+moira_status moira_select_attend_ex(const moira_shape *shape, int32_t format, const void *q,
+                                    const void *summ, const void *k_pool, const void *v_pool,
+                                    const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                                    int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
+                                    int32_t *lengths, float *out, void *workspace, size_t ws_bytes,
+                                    moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (!valid_format(format) || !valid_rule(MOIRA_RULE_COVERAGE, gamma) || !finite_pos(sm_scale))
+        return MOIRA_EINVAL;
+    if (!q || !summ || !k_pool || !v_pool || !page_table || !seq_lens || !lists || !lengths || !out)
+        return MOIRA_EINVAL;
+    if (!aligned16(q) || !aligned16(summ) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return MOIRA_EINVAL;
+    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
+    return select_attend_impl(shape, format, q, summ, k_pool, v_pool, page_table, seq_lens, batch, max_pages,
+                              MOIRA_RULE_COVERAGE, gamma, sm_scale, lists, lengths, out, workspace, ws_bytes,
+                              false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moira_status moira_select_attend(const moira_shape *shape, const void *q, const void *summ,
+                                 const void *k_pool, const void *v_pool, const int32_t *page_table,
+                                 const int32_t *seq_lens, int32_t batch, int32_t max_pages, float gamma,
+                                 float sm_scale, int32_t *lists, int32_t *lengths, float *out,
+                                 void *workspace, size_t ws_bytes, moira_stream_t stream)
+{
+    return moira_select_attend_ex(shape, MOIRA_SUMM_BF16, q, summ, k_pool, v_pool, page_table, seq_lens,
+                                  batch, max_pages, gamma, sm_scale, lists, lengths, out, workspace, ws_bytes,
+                                  stream);
+}
+
+moira_status moira_score_ex(const moira_shape *shape, int32_t format, const void *q, const void *summ,
+                            const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                            int32_t max_pages, float sm_scale, void *workspace, size_t ws_bytes,
+                            moira_stream_t stream)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (!valid_format(format) || !finite_pos(sm_scale)) return MOIRA_EINVAL;
+    if (!q || !summ || !page_table || !seq_lens) return MOIRA_EINVAL;
+    if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
+    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
+    const WsLayout L = layout_for(shape, batch, max_pages);
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    const float scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    return cuda_status(launch_score(q, summ, format, page_table, seq_lens, batch, shape->num_q_heads,
+                                    shape->num_kv_heads, max_pages, shape->num_phys_pages, scale_log2,
+                                    reinterpret_cast<float *>(w + L.scores), reinterpret_cast<float *>(w + L.chunks),
+                                    false, reinterpret_cast<uint32_t *>(w + L.status),
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t moira_select_attend_is_fused(const moira_shape *shape, int32_t batch, int32_t max_pages)
+{
+    if (check_shape(shape) != MOIRA_OK || check_batch(shape, batch, max_pages) != MOIRA_OK) return 0;
+    return select_attend_fits(batch * shape->num_kv_heads, max_pages, attend_blocks()) ? 1 : 0;
+}
+
 moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int32_t num_layers,
                                   const void *q_all, const void *k_pool_all,
                                   const void *v_pool_all, const void *summ_all,
@@ -356,9 +521,12 @@ moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int3
                          batch, max_pages, rule, param, sm_scale, lists,
                          lengths_all + l * len_layer, workspace, ws_bytes, l > 0, s);
         if (st != MOIRA_OK) return st;
+        const bool dense = rule == MOIRA_RULE_COVERAGE && param >= 1.0f;
+        const bool more = l + 1 < num_layers && !dense;
         st = attend_impl(shape, q + l * q_layer, kp + l * kv_layer, vp + l * kv_layer, lists,
                          lengths_all + l * len_layer, seq_lens, batch, max_pages, sm_scale,
-                         out_all + l * q_layer, workspace, ws_bytes, s);
+                         out_all + l * q_layer, workspace, ws_bytes, s, more ? sp + (l + 1) * sm_layer : nullptr,
+                         more ? sm_layer : 0);
         if (st != MOIRA_OK) return st;
     }
     return MOIRA_OK;
@@ -427,6 +595,43 @@ moira_status moira_diag_wait_timeout(void *workspace, size_t ws_bytes, uint64_t 
     return cuda_status(launch_wait_timeout(static_cast<uint32_t *>(workspace), limit_ns,
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
+
+moira_status moira_diag_wait_chain(void *workspace, size_t ws_bytes, uint64_t limit_ns, int32_t n_waits,
+                                   moira_stream_t stream)
+{
+    if (!workspace || ws_bytes < 256 || limit_ns < 1 || limit_ns > 10000000000ull || n_waits < 1 ||
+        n_waits > 4096)
+        return MOIRA_EINVAL;
+    return cuda_status(launch_wait_chain(static_cast<uint32_t *>(workspace), limit_ns, n_waits,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moira_status moira_diag_barrier_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns, int32_t blocks,
+                                        moira_stream_t stream)
+{
+    if (!workspace || ws_bytes < 256 || limit_ns < 1 || limit_ns > 10000000000ull || blocks < 1 ||
+        blocks > current_sm_count())
+        return MOIRA_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the barrier's two words sit on the status line's second 128 bytes,
+    // cleared before the launch (the barrier never completes, so it leaves
+    // its count behind) and after it
+    uint32_t *bar = static_cast<uint32_t *>(workspace) + 32;
+    if (cudaMemsetAsync(bar, 0, 128, s) != cudaSuccess) return MOIRA_ECUDA;
+    if (launch_barrier_timeout(static_cast<uint32_t *>(workspace), bar, blocks, limit_ns, s) != cudaSuccess)
+        return MOIRA_ECUDA;
+    return cuda_status(cudaMemsetAsync(bar, 0, 128, s));
+}
+
+#ifdef MOIRA_CTA_TIMES
+moira_status moira_set_cta_times(uint64_t *buf, int32_t max_launches)
+{
+    if (max_launches < 0 || (buf == nullptr && max_launches != 0)) return MOIRA_EINVAL;
+    g_cta_times = reinterpret_cast<unsigned long long *>(buf);
+    g_cta_launches = max_launches;
+    return MOIRA_OK;
+}
+#endif
 
 const char *moira_status_string(moira_status status)
 {

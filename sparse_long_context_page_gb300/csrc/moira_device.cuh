@@ -73,8 +73,23 @@ __host__ __device__ inline int chunks_ld(int max_pages)
     return (2 * nch + 3) / 4 * 4;
 }
 
+// Fused selection + attention (k_select_attend, small batches) adds:
+// barriers                    : uint32 [kFusedMaxUnits + 1][kBarWords] one barrier per list, then the grid's
+// level-1 histograms          : uint32 [fu][kL1Stride]       per list, fixed-point mass per bin
+// page masses                 : uint32 [fu][ld]              per list, the fp32 bit pattern of every page's mass
+// with fu = min(units, kFusedMaxUnits).  The barriers and histograms start at
+// zero (moira_workspace_init) and every launch leaves them at zero.
+constexpr int kFusedMaxUnits = 63;                 // lists per launch of the fused kernel
+constexpr uint32_t kKeyLo = 95u << 7;               // level-1 bins: see l1_bin()
+constexpr int kL1Bins = (16384 - static_cast<int>(kKeyLo)) + 1;     // 4225
+constexpr int kL1Stride = (kL1Bins + 3) / 4 * 4;    // 4228: rows of whole 16-byte units
+constexpr int kL2Bins = 256;
+constexpr int kCand = 2048;                         // crossing-bin pages refined by one warp
+constexpr int kBarWords = 32;                       // uint32 words per inter-block barrier (128 B)
+
 struct WsLayout {
-    size_t status, counters, gcounters, scores, chunks, partials, total;
+    size_t status, counters, gcounters, scores, chunks, partials;
+    size_t fbars, fl1, fmass, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -89,6 +104,10 @@ __host__ __device__ inline WsLayout ws_layout(int batch, int hq, int max_pages, 
     w.scores = o;   o = align_up(o + sizeof(float) * (size_t)batch * hq * weights_ld(max_pages), 256);
     w.chunks = o;   o = align_up(o + sizeof(float) * (size_t)batch * hq * chunks_ld(max_pages), 256);
     w.partials = o; o = align_up(o + sizeof(float) * kPartFloats * (size_t)(blocks + units), 256);
+    const size_t fu = units < kFusedMaxUnits ? (size_t)units : (size_t)kFusedMaxUnits;
+    w.fbars = o;    o = align_up(o + sizeof(uint32_t) * kBarWords * (size_t)(kFusedMaxUnits + 1), 256);
+    w.fl1 = o;      o = align_up(o + sizeof(uint32_t) * kL1Stride * fu, 256);
+    w.fmass = o;    o = align_up(o + sizeof(uint32_t) * fu * (size_t)weights_ld(max_pages), 256);
     w.total = o;
     return w;
 }
@@ -164,10 +183,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete, giving up after `limit_ns`
-// (kWaitLimitNs in the kernels).  Returns false on timeout (the caller
-// records MOIRA_DEV_TIMEOUT and goes on, so the control flow of the block
-// never changes and nothing hangs).
+// Wait for the phase of `parity` to complete, giving up after `limit_ns`.
+// Returns false on timeout.  The kernels wait through WaitGuard (below); this
+// plain form serves the diagnostic of a single wait.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs)
 {
@@ -179,6 +197,144 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
             if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer() - t0 > limit_ns) return false;
     }
+}
+
+// ---- bounded waits, given up once per launch ------------------------------------
+// Every wait of a kernel goes through the block's WaitGuard: a flag in shared
+// memory that the block sets when one of its waits runs out, and that starts
+// set when the status word already holds MOIRA_DEV_TIMEOUT (a step whose
+// earlier launch timed out waits no more).  A wait checks the flag while it
+// spins; once the flag is set, every later wait of the block makes one
+// attempt and gives up.  So a copy that never lands costs one wait limit per
+// launch instead of one per wait, and the block still follows its normal
+// control flow (all loops are bounded by sizes, never by the data waited for).
+struct WaitGuard {
+    int *flag;              // shared memory, one per block
+    uint32_t *status;       // device status word (MOIRA_DEV_* bits)
+};
+
+__device__ __forceinline__ bool guard_failed(const WaitGuard &g)
+{
+    return *const_cast<volatile int *>(g.flag) != 0;
+}
+
+__device__ __forceinline__ void guard_fail(const WaitGuard &g)
+{
+    *const_cast<volatile int *>(g.flag) = 1;
+    atomicOr(g.status, kDevTimeout);
+}
+
+// Thread 0 sets the flag from the status word before the block's first
+// barrier; the word may be stale, which only delays the give-up.
+__device__ __forceinline__ void guard_init(const WaitGuard &g)
+{
+    *g.flag = (__ldcg(g.status) & kDevTimeout) ? 1 : 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_g(uint32_t bar, uint32_t parity, const WaitGuard &g,
+                                            uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    if (!guard_failed(g)) {
+        const uint64_t t0 = globaltimer();
+        while (true) {
+#pragma unroll 1
+            for (int i = 0; i < 32; ++i)
+                if (mbar_try_wait(bar, parity)) return true;
+            if (guard_failed(g)) break;
+            if (globaltimer() - t0 > limit_ns) {
+                guard_fail(g);
+                break;
+            }
+        }
+    }
+    return mbar_try_wait(bar, parity);
+}
+
+// After a give-up, copies the block issued may still be in flight towards its
+// shared memory; before the block exits, wait for the phase of `parity` of
+// every such barrier, at most until `deadline` (globaltimer ns) in all.
+constexpr uint64_t kDrainLimitNs = 50000000ull;     // 50 ms per block
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64_t deadline)
+{
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() > deadline) return;
+}
+
+// ---- inter-block barriers inside one launch ------------------------------------------
+// A group of blocks that are resident together (a grid sized to the resident
+// capacity) meets at a barrier made of two words on their own 128-byte line:
+// an arrival count that wraps to zero at the group size, and a generation
+// that the last arrival advances.  Thread 0 of each block reads the
+// generation once before its first arrival (it cannot advance before that
+// arrival) and counts it up itself after every barrier, so a barrier costs
+// one atomic and the polls; the same words serve any number of barriers in a
+// row, for any group size, and are left as they were found (count 0).
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// old = *p; *p = old >= wrap ? 0 : old + 1, acquire-release at GPU scope.
+__device__ __forceinline__ uint32_t atom_inc_acq_rel_gpu(uint32_t *p, uint32_t wrap)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(wrap) : "memory");
+    return old;
+}
+
+// The generation a block expects at its next barrier on `bar` (thread 0).
+__device__ __forceinline__ uint32_t barrier_generation(const uint32_t *bar) { return ld_relaxed_gpu(bar + 1); }
+
+// Every thread of the block calls it; thread 0 arrives for the block with
+// `gen` the barrier's current generation (barrier_generation, then this
+// call's own count).  The memory operations the block made before the call
+// are visible to every block of the group after it: the block barrier makes
+// them visible to thread 0, whose acquire-release arrival publishes them and
+// acquires the others'.  Returns false if the wait ran out (MOIRA_DEV_TIMEOUT).
+__device__ __forceinline__ bool group_barrier(uint32_t *bar, uint32_t n_blocks, uint32_t &gen, const WaitGuard &g,
+                                              uint64_t limit_ns = kWaitLimitNs)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t old = atom_inc_acq_rel_gpu(bar, n_blocks - 1u);
+        if (old == n_blocks - 1u) {
+            st_release_gpu(bar + 1, gen + 1u);
+        } else if (!guard_failed(g)) {
+            const uint64_t t0 = globaltimer();
+            while (ld_acquire_gpu(bar + 1) == gen) {
+                if (guard_failed(g)) break;
+                if (globaltimer() - t0 > limit_ns) {
+                    guard_fail(g);
+                    break;
+                }
+            }
+        }
+        gen += 1u;
+    }
+    __syncthreads();
+    return !guard_failed(g);
+}
+
+// ---- L2 prefetch -----------------------------------------------------------------------
+// Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
+// without waiting for them.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(bytes)
+                 : "memory");
 }
 
 // ---- shared-memory histograms ------------------------------------------------------

@@ -51,15 +51,60 @@ struct AttendArgs {
     int hq, hkv, units, max_pages;
     long long num_pages;
     float scale_log2;
+    // the next layer's page summaries (decode step only; null otherwise):
+    // each block brings its share into L2 once its pages are issued
+    const uint8_t *next_summ;
+    unsigned long long next_summ_bytes;
+#ifdef MOIRA_CTA_TIMES
+    unsigned long long *cta_times;   // [grid][2] (start, end) %globaltimer per block, or null
+#endif
 };
+
+#ifdef MOIRA_CTA_TIMES
+// Where the next attention launch records its per-block times (null: none);
+// advanced by one grid's worth per launch, up to the set number of launches.
+unsigned long long *next_cta_times(int blocks);
+#endif
 
 cudaError_t launch_attend(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                           const AttendArgs &args, int blocks, cudaStream_t stream);
 
+// The selection and the attention of one layer in one launch (k_select_attend,
+// fused.cu), for small batches: every list's selection is spread over the
+// grid's blocks, which meet at barriers inside the launch, then the same
+// blocks attend.  `at.lists` is unused (the kept pages come from the
+// selection); the outputs lists / lengths are written as moira_select would.
+// With `dense` every page is kept and no estimate runs (no k_score before it).
+struct FusedArgs {
+    AttendArgs at;                 // at.lists / at.lengths: the outputs, read back by the attention
+    const float *weights;          // k_score's chunk-relative weights
+    const float *chunks;           // k_score's per-chunk (max, sum)
+    const int32_t *page_table;
+    const uint8_t *k_pool;         // this layer's pools (raw), for L2 prefetches
+    const uint8_t *v_pool;
+    int32_t *lists;                // out
+    int32_t *lengths;              // out
+    uint32_t *bars;                // [kFusedMaxUnits + 1][kBarWords]
+    uint32_t *l1hist;              // [units][kL1Stride]
+    uint32_t *mass;                // [units][ld]
+    unsigned long long target;     // gamma on the 2^-31 grid
+    int ld, ldc;
+    int dense;
+};
+
+// Whether k_select_attend takes `units` lists of at most `max_pages` pages on
+// a grid of `blocks` (and fits 2 blocks per SM on the current device).
+bool select_attend_fits(int units, int max_pages, int blocks);
+cudaError_t launch_select_attend(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                 const FusedArgs &args, int blocks, cudaStream_t stream);
+
 int attend_blocks_per_sm();
 
-// Diagnostic: a bounded wait on an mbarrier nothing arrives at (see diag.cu).
+// Diagnostics of bounded waits made to run out (see diag.cu).
 cudaError_t launch_wait_timeout(uint32_t *status, unsigned long long limit_ns, cudaStream_t stream);
+cudaError_t launch_wait_chain(uint32_t *status, unsigned long long limit_ns, int n_waits, cudaStream_t stream);
+cudaError_t launch_barrier_timeout(uint32_t *status, uint32_t *bar, int blocks, unsigned long long limit_ns,
+                                   cudaStream_t stream);
 
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device.  The attribute stays set in the device's context, so it is

@@ -24,8 +24,7 @@
 // Top-p over pages needs the global softmax and a cumulative sum ("Faster
 // Flash Decoding", section 1 and figure 1); the histogram descent replaces a
 // full sort.
-#include "moira_device.cuh"
-#include "moira_launch.h"
+#include "select_core.cuh"
 
 namespace moira {
 
@@ -227,7 +226,9 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
     __shared__ uint32_t s_ok[kScoreMaxStages];               // per stage: pages loaded
     __shared__ int s_wsum[kScoreConsumers + 1];
     __shared__ __align__(8) unsigned long long s_full[kScoreMaxStages], s_empty[kScoreMaxStages];
+    __shared__ int s_abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const WaitGuard wg{&s_abort, status};
     const int nh = min(hkv, kScoreHeads);
     const int n_slices = hkv / nh;
     const int n_chunks = (max_pages + kScoreChunk - 1) / kScoreChunk;
@@ -244,6 +245,7 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
             mbar_init(smem_u32(&s_empty[s]), 1);
         }
         mbar_fence_init();
+        guard_init(wg);
     }
     // q, the summaries and the score buffers follow earlier kernels, so they
     // are touched only after the wait.  With `early`, the launch follows a
@@ -326,8 +328,7 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
             const int it = g - g0;
             const int stage = it % stages;
             const uint32_t use = static_cast<uint32_t>(it / stages);
-            if (use > 0 && !mbar_wait(smem_u32(&s_empty[stage]), (use - 1) & 1u) && lane == 0)
-                raise_status(status, kDevTimeout);
+            if (use > 0) mbar_wait_g(smem_u32(&s_empty[stage]), (use - 1) & 1u, wg);
             const uint32_t full = smem_u32(&s_full[stage]);
             if (lane == 0) {
                 s_ok[stage] = okm;
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
         const int it = g - g0;
         const int stage = it % stages;
         const uint32_t use = static_cast<uint32_t>(it / stages);
-        if (!mbar_wait(smem_u32(&s_full[stage]), use & 1u) && tid == 0) raise_status(status, kDevTimeout);
+        mbar_wait_g(smem_u32(&s_full[stage]), use & 1u, wg);
         const uint32_t okm = s_ok[stage];
         const uint8_t *base = s_score + static_cast<uint32_t>(stage) * kScoreChunk * stride;
         if (has_item) {
@@ -502,6 +503,16 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
         score_consumer_bar();                 // s_s is free again
         if (g + 1 < g1) score_cursor_next(c, s_pref, batch, n_slices);
     }
+    // after a give-up, let the copies still in flight land before the block
+    // exits (their landing is what the skipped waits were for)
+    if (tid == 0 && guard_failed(wg)) {
+        const uint64_t deadline = globaltimer() + kDrainLimitNs;
+        const int N = g1 - g0;
+        for (int s = 0; s < stages && s < N; ++s) {
+            const int last = N - 1 - ((N - 1 - s) % stages);          // last item on stage s
+            mbar_drain(smem_u32(&s_full[s]), static_cast<uint32_t>(last / stages) & 1u, deadline);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -513,36 +524,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 // (the kernel is instantiated for both; registers hold one value per stripe).
 constexpr int kSelStripesMax = kMaxPagesPerSeq / kSelThreads;
 static_assert(kSelStripesMax % 4 == 0, "masses: 4 pages per thread per pass");
-// Level-1 bins: the fp32 bit pattern >> 16 (exponent + 7 fraction bits, 128
-// bins per octave) for masses in [2^-32, 2); bin 0 gathers everything below.
-constexpr uint32_t kKeyLo = 95u << 7;
-constexpr int kL1Bins = (16384 - static_cast<int>(kKeyLo)) + 1;     // 4225
 constexpr int kL1PerThread = (kL1Bins + kSelThreads - 1) / kSelThreads;   // 5
-constexpr int kL2Bins = 256;
-
-__device__ __forceinline__ int l1_bin(uint32_t x)
-{
-    const uint32_t k = x >> 16;
-    return k < kKeyLo ? 0 : static_cast<int>(k - kKeyLo) + 1;
-}
-__device__ __forceinline__ uint32_t l1_lo(int b) { return b == 0 ? 0u : (static_cast<uint32_t>(b - 1) + kKeyLo) << 16; }
-__device__ __forceinline__ uint32_t l1_hi(int b) { return b == 0 ? (kKeyLo << 16) : (static_cast<uint32_t>(b) + kKeyLo) << 16; }
-
-// Mass as a 2^-31 fixed-point integer.  Masses sum to 1 (to fp32 rounding),
-// so every histogram bin and every partial sum fits in 32 bits; rounding each
-// mass costs at most 2^-32, i.e. < 1e-5 over 16384 pages.
-__device__ __forceinline__ uint32_t to_fx(uint32_t x)
-{
-    return __float2uint_rn(__uint_as_float(x) * 0x1p31f);
-}
-
-// What a page adds to the histograms: its fixed-point mass for the coverage
-// rule, 1 for top-k (the descent then counts pages instead of mass).
-__device__ __forceinline__ uint32_t rule_weight(int rule, uint32_t x)
-{
-    return rule == kRuleTopK ? 1u : to_fx(x);
-}
-
 // Exclusive scan over the block in thread order; *total gets the sum.
 __device__ unsigned long long sel_excl_scan(unsigned long long v, unsigned long long *s_warp,
                                             unsigned long long *total)
@@ -572,8 +554,6 @@ __device__ unsigned long long sel_excl_scan(unsigned long long v, unsigned long 
     return off + x - v;
 }
 
-constexpr int kCand = 2048;                 // crossing-bin pages refined by one warp
-constexpr int kPairMax = 256;               // crossing-bin pages resolved pairwise
 static_assert(kPairMax * 4 <= kSelThreads, "pairwise path: at least 4 threads per candidate");
 static_assert(kMaxPagesPerSeq / kScoreChunk <= 2 * 256, "normalisers: at most two chunks per thread and head");
 
@@ -687,47 +667,34 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
     //    tid%256 + 256 i): M = max of the chunk maxima, e_c = 2^(M_c - M) once
     //    per chunk, Z = sum_c e_c Z_c; the chunk factor is e_c / (G Z).
     {
-        constexpr int kCpt = kSelStripes / 8;         // chunks per thread and head: 1 or 2
+        // thread -> (head tid/256, chunks tid%256 and tid%256 + 256): warp w of
+        // a head is its virtual warp w of the fixed-order reduction
         const int hg = tid >> 8, ci = tid & 255;
         const float *crow = chunks + (static_cast<size_t>(r) * hq + j * kGroup + hg) * ldc;
-        float cm[kCpt], cz[kCpt];
-        float mx = -INFINITY;
+        float cm[2] = {-INFINITY, -INFINITY}, cz[2] = {0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < kCpt; ++i) {
-            cm[i] = -INFINITY;
-            cz[i] = 0.f;
+        for (int i = 0; i < kSelStripes / 8; ++i) {
             const int c = ci + 256 * i;
             if (c < nch) {
                 const float2 cs = __ldg(reinterpret_cast<const float2 *>(crow + 2 * c));
                 cm[i] = cs.x;
                 cz[i] = cs.y;
             }
-            mx = fmaxf(mx, cm[i]);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float mx = warp_max_butterfly(fmaxf(cm[0], cm[1]));
         if (lane == 0) sh.red[warp] = mx;
         __syncthreads();
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < 8; ++w) M = fmaxf(M, sh.red[hg * 8 + w]);
-        float e[kCpt], z = 0.f;
-#pragma unroll
-        for (int i = 0; i < kCpt; ++i) {
-            e[i] = (cm[i] == -INFINITY) ? 0.f : exp2f(cm[i] - M);
-            z += cz[i] * e[i];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        const float z = warp_sum_butterfly(chunk_weight_sum(cm[0], cz[0], cm[1], cz[1], M));
         if (lane == 0) sh.red2[warp] = z;
         __syncthreads();
-        float Z = 0.f;
+        const float zinv = head_zinv(&sh.red2[hg * 8]);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) Z += sh.red2[hg * 8 + w];
-        const float zinv = Z > 0.f ? 1.f / (kGroup * Z) : 0.f;
-#pragma unroll
-        for (int i = 0; i < kCpt; ++i)
-            if (ci + 256 * i < nch) reinterpret_cast<float *>(s_f)[4 * (ci + 256 * i) + hg] = e[i] * zinv;
+        for (int i = 0; i < 2; ++i)
+            if (ci + 256 * i < nch)
+                reinterpret_cast<float *>(s_f)[4 * (ci + 256 * i) + hg] = chunk_factor(cm[i], M, zinv);
     }
     __syncthreads();
 
@@ -753,12 +720,10 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
                 w2 = __ldg(reinterpret_cast<const float4 *>(wrow + 2 * ld + p));
                 w3 = __ldg(reinterpret_cast<const float4 *>(wrow + 3 * ld + p));
             }
-            const float m[4] = {w0.x * f.x + w1.x * f.y + w2.x * f.z + w3.x * f.w,
-                                w0.y * f.x + w1.y * f.y + w2.y * f.z + w3.y * f.w,
-                                w0.z * f.x + w1.z * f.y + w2.z * f.z + w3.z * f.w,
-                                w0.w * f.x + w1.w * f.y + w2.w * f.z + w3.w * f.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) xs[i] = __float_as_uint(fminf(fmaxf(m[i], 0.f), 1.5f));   // NaN -> 0
+            xs[0] = page_mass_bits(w0.x, w1.x, w2.x, w3.x, f);
+            xs[1] = page_mass_bits(w0.y, w1.y, w2.y, w3.y, f);
+            xs[2] = page_mass_bits(w0.z, w1.z, w2.z, w3.z, f);
+            xs[3] = page_mass_bits(w0.w, w1.w, w2.w, w3.w, f);
             *reinterpret_cast<uint4 *>(s_bits + p) = make_uint4(xs[0], xs[1], xs[2], xs[3]);
         }
         if ((k * kSelThreads + warp * 32) * 4 < F) {        // warp-uniform: the warp has pages
@@ -888,60 +853,9 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
             __syncthreads();
         } else if (use_cand) {
             if (warp == 0) {
-                const int nc = sh.ncand;
                 uint32_t lo = sh.lo, hi = sh.hi;
                 unsigned long long above = sh.above;
-                for (int pass = 0; hi - lo > 1u && pass < 6; ++pass) {
-                    const uint32_t width = hi - lo;
-                    const int nbits = 32 - __clz(width - 1u);
-                    const int shift = nbits > 8 ? nbits - 8 : 0;
-                    const int nb = static_cast<int>((width - 1u) >> shift) + 1;
-    #pragma unroll
-                    for (int i = 0; i < kL2Bins / 32; ++i) sh.h2[lane + 32 * i] = 0u;
-                    __syncwarp();
-                    for (int c = lane; c < nc; c += 32) {
-                        const uint32_t x = sh.cand[c];
-                        if (x >= lo && x < hi) atomicAdd(&sh.h2[(x - lo) >> shift], rule_weight(rule, x));
-                    }
-                    __syncwarp();
-                    const int top = nb - 1 - 8 * lane;
-                    unsigned long long mine = 0ull;
-    #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (top - i >= 0) mine += sh.h2[top - i];
-                    unsigned long long xs = mine;
-    #pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const unsigned long long y = __shfl_up_sync(0xffffffffu, xs, o);
-                        if (lane >= o) xs += y;
-                    }
-                    unsigned long long acc = above + xs - mine;
-                    int fb = -1;
-                    unsigned long long fa = 0ull;
-                    if (acc < target && acc + mine >= target) {
-    #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int b = top - i;
-                            if (b < 0) break;
-                            if (acc + sh.h2[b] >= target) {
-                                fb = b;
-                                fa = acc;
-                                break;
-                            }
-                            acc += sh.h2[b];
-                        }
-                    }
-                    const unsigned who = __ballot_sync(0xffffffffu, fb >= 0);
-                    if (!who) break;                             // cannot happen: exact integer sums
-                    const int src = __ffs(who) - 1;
-                    fb = __shfl_sync(0xffffffffu, fb, src);
-                    above = __shfl_sync(0xffffffffu, fa, src);
-                    const uint32_t nlo = lo + (static_cast<uint32_t>(fb) << shift);
-                    const uint32_t span = 1u << shift;
-                    hi = (hi - nlo < span) ? hi : nlo + span;
-                    lo = nlo;
-                    __syncwarp();
-                }
+                warp_refine(sh.cand, sh.ncand, sh.h2, rule, target, lo, hi, above);
                 if (lane == 0) {
                     sh.lo = lo;
                     sh.hi = hi;

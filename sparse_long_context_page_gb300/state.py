@@ -82,6 +82,22 @@ class DecodeState:
                          self.seq_lens, rule, param, self.sm_scale, lists, lengths, self.ws)
         return lists, lengths
 
+    def select_attend_layer(self, l: int, gamma: float, lists=None, lengths=None, out=None):
+        """One layer's coverage selection and attention in one call
+        (moira_select_attend, in this state's summary format)."""
+        lists = self.lists if lists is None else lists
+        lengths = self.lengths[l] if lengths is None else lengths
+        out = self.out[l] if out is None else out
+        mb.select_attend(self.shape, self.w.q[l], self.summ[l], self.w.k_pool[l], self.w.v_pool[l],
+                         self.page_table, self.seq_lens, gamma, self.sm_scale, lists, lengths, out, self.ws,
+                         fmt=self.fmt)
+        return lists, lengths, out
+
+    def score_layer(self, l: int):
+        """The page-scoring kernel of layer l alone (results stay in the workspace)."""
+        mb.score(self.shape, self.w.q[l], self.summ[l], self.page_table, self.seq_lens, self.sm_scale,
+                 self.ws, fmt=self.fmt)
+
     def attend_layer(self, l: int, lists, lengths, out=None):
         out = self.out[l] if out is None else out
         mb.attend(self.shape, self.w.q[l], self.w.k_pool[l], self.w.v_pool[l], lists, lengths,

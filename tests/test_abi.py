@@ -29,6 +29,26 @@ def test_library_exports_every_declared_function():
     assert set(decl) == set(mb.EXPORTS)
 
 
+def test_load_balance_build_exports_the_timing_entry():
+    """The load-balance build exports everything libmoira.so does plus
+    moira_set_cta_times (include/moira_cta_times.h); libmoira.so has none of it.
+    Its host checks reject a missing buffer before any CUDA call."""
+    from sparse_long_context_page_gb300 import build
+    text = open(os.path.join(ROOT, "include", "moira_cta_times.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    extra = set(re.findall(r"\b(moira_[a-z_]+)\s*\(", text))
+    assert extra == {"moira_set_cta_times"}
+    moira.load_library()
+    timed = ctypes.CDLL(build.LIB_CTA_TIMES)
+    for name in list(mb.EXPORTS) + sorted(extra):
+        assert hasattr(timed, name), name
+    assert not hasattr(moira.load_library(), "moira_set_cta_times")
+    timed.moira_set_cta_times.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+    assert timed.moira_set_cta_times(None, 3) == 1
+    assert timed.moira_set_cta_times(FAKE, -1) == 1
+    assert timed.moira_set_cta_times(None, 0) == 0
+
+
 def test_status_strings():
     lib = moira.load_library()
     for code in range(5):

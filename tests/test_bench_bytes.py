@@ -53,8 +53,8 @@ def test_traffic_shape_threshold_matches_the_kernel():
     import os
     import re
     src = open(os.path.join(os.path.dirname(bench.__file__), "sparse_long_context_page_gb300", "csrc",
-                            "attend.cu")).read()
+                            "attend_core.cuh")).read()
     m = re.search(r"constexpr int kManyUnits = (\d+);", src)
-    assert m, "kManyUnits not found in attend.cu"
+    assert m, "kManyUnits not found in attend_core.cuh"
     assert int(m.group(1)) == bench.ATTEND_TRAFFIC["many_lists_from"]
-    assert set(bench.ATTEND_TRAFFIC["dram_bytes_per_entry"]) == {"few_lists", "many_lists"}
+    assert set(bench.ATTEND_TRAFFIC["dram_bytes_per_entry"]) == {"fused", "few_lists", "many_lists"}

@@ -248,8 +248,10 @@ def test_host_buffers_step_matches_device_step():
 def test_decode_step_matches_per_layer_calls(fmt, persistent):
     """From layer 1 on, the decode step lets the score kernel read the page
     table and the lengths before its dependency wait; the per-layer calls
-    wait first.  Both must give the same lengths and outputs, bit for bit,
-    under both launch shapes of the score kernel."""
+    (moira_select_attend, and moira_select for the lists) wait first.  Both
+    must give the same lengths, lists and outputs, bit for bit, under both
+    launch shapes of the score kernel (one request takes the single-launch
+    selection + attention, three requests of 8192 pages the two-launch form)."""
     if persistent:
         over = dict(batch=3, context=(16 * 700 + 9, 16 * 1500 + 3, 16 * 300))
         max_pages = 8192                   # 3 x 2 x 256 items: more than one wave
@@ -267,17 +269,21 @@ def test_decode_step_matches_per_layer_calls(fmt, persistent):
     for l in range(w.spec.layers):
         lists = torch.full_like(st.lists, -1)
         lengths = torch.zeros_like(st.lengths[l])
-        st.select_layer(l, gamma, lists, lengths)
         out = torch.zeros_like(st.out[l])
-        st.attend_layer(l, lists, lengths, out)
+        st.select_attend_layer(l, gamma, lists, lengths, out)
+        sel_lists = torch.full_like(st.lists, -1)
+        sel_len = torch.zeros_like(st.lengths[l])
+        st.select_layer(l, gamma, sel_lists, sel_len)
         torch.cuda.synchronize()
         assert torch.equal(lengths, len_s[l]), f"layer {l}: list lengths differ"
+        assert torch.equal(sel_len, len_s[l]), f"layer {l}: moira_select's lengths differ"
         assert torch.equal(out, out_s[l]), f"layer {l}: outputs differ"
     n = lengths.cpu().numpy()
-    lh, ls = lists.cpu().numpy(), last_lists.cpu().numpy()
+    lh, ls, sh = lists.cpu().numpy(), last_lists.cpu().numpy(), sel_lists.cpu().numpy()
     for r in range(w.spec.batch):
         for j in range(w.spec.kv_heads):
             assert np.array_equal(lh[r, j, :n[r, j]], ls[r, j, :n[r, j]])
+            assert np.array_equal(sh[r, j, :n[r, j]], ls[r, j, :n[r, j]])
     assert st.device_status() == 0
 
 
