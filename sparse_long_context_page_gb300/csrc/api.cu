@@ -141,15 +141,10 @@ moira_status select_impl(const moira_shape *shape, int32_t fmt, const void *q, c
                                      lengths, status, stream));
 }
 
-// The next layer's summaries are brought into L2 by the attention launch when
-// they fit comfortably (one request's summaries; a serving batch's do not).
-constexpr size_t kNextSummMaxBytes = 48u << 20;
-
 moira_status attend_impl(const moira_shape *shape, const void *q, const void *k_pool,
                          const void *v_pool, const int32_t *lists, const int32_t *lengths,
                          const int32_t *seq_lens, int32_t batch, int32_t max_pages, float sm_scale,
-                         float *out, void *ws, size_t ws_bytes, cudaStream_t stream,
-                         const void *next_summ = nullptr, size_t next_summ_bytes = 0)
+                         float *out, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     const WsLayout L = layout_for(shape, batch, max_pages);
     uint8_t *w = static_cast<uint8_t *>(ws);
@@ -171,10 +166,6 @@ moira_status attend_impl(const moira_shape *shape, const void *q, const void *k_
     a.max_pages = max_pages;
     a.num_pages = shape->num_phys_pages;
     a.scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
-    const bool pf = next_summ != nullptr && next_summ_bytes > 0 && next_summ_bytes <= kNextSummMaxBytes &&
-                    (reinterpret_cast<uintptr_t>(next_summ) & 15u) == 0;
-    a.next_summ = pf ? static_cast<const uint8_t *>(next_summ) : nullptr;
-    a.next_summ_bytes = pf ? next_summ_bytes : 0ull;
 #ifdef MOIRA_CTA_TIMES
     a.cta_times = next_cta_times(attend_blocks());
 #endif
@@ -232,8 +223,6 @@ moira_status select_attend_impl(const moira_shape *shape, int32_t fmt, const voi
     f.at.max_pages = max_pages;
     f.at.num_pages = shape->num_phys_pages;
     f.at.scale_log2 = scale_log2;
-    f.at.next_summ = nullptr;
-    f.at.next_summ_bytes = 0ull;
 #ifdef MOIRA_CTA_TIMES
     f.at.cta_times = next_cta_times(blocks);
 #endif
@@ -521,12 +510,9 @@ moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int3
                          batch, max_pages, rule, param, sm_scale, lists,
                          lengths_all + l * len_layer, workspace, ws_bytes, l > 0, s);
         if (st != MOIRA_OK) return st;
-        const bool dense = rule == MOIRA_RULE_COVERAGE && param >= 1.0f;
-        const bool more = l + 1 < num_layers && !dense;
         st = attend_impl(shape, q + l * q_layer, kp + l * kv_layer, vp + l * kv_layer, lists,
                          lengths_all + l * len_layer, seq_lens, batch, max_pages, sm_scale,
-                         out_all + l * q_layer, workspace, ws_bytes, s, more ? sp + (l + 1) * sm_layer : nullptr,
-                         more ? sm_layer : 0);
+                         out_all + l * q_layer, workspace, ws_bytes, s);
         if (st != MOIRA_OK) return st;
     }
     return MOIRA_OK;

@@ -311,7 +311,6 @@ __device__ __forceinline__ void attend_init(AttendSmem<kSlots, kConsumerWarps> &
 // per ring slot), since one lane issuing page after page could not keep the
 // ring full.
 constexpr int kIssueLanes = 8;
-constexpr int kSummPrefetch = 16384;      // bytes per prefetch of the next layer's summaries
 static_assert(kIssueLanes <= kManySlots && kIssueLanes <= kFewSlots && 32 % kIssueLanes == 0,
               "an issue group never holds two pages of one ring slot");
 template <int kSlots, int kConsumerWarps, class Lookup>
@@ -375,17 +374,6 @@ __device__ __forceinline__ void attend_produce(AttendSmem<kSlots, kConsumerWarps
         cu = nu;
         cn = nn;
         cp = np;
-    }
-    // this block's pages are all requested: while the attention tails off,
-    // bring the block's share of the next layer's summaries into L2 for the
-    // next scoring kernel (16 KB per prefetch, 16-byte aligned pieces)
-    if (a.next_summ != nullptr) {
-        const unsigned long long n16 = a.next_summ_bytes / 16;
-        const unsigned long long lo = n16 * blockIdx.x / gridDim.x * 16;
-        const unsigned long long hi = n16 * (blockIdx.x + 1) / gridDim.x * 16;
-        for (unsigned long long off = lo + static_cast<unsigned long long>(lane) * kSummPrefetch; off < hi;
-             off += 32ull * kSummPrefetch)
-            prefetch_l2(a.next_summ + off, static_cast<uint32_t>(min(hi - off, static_cast<unsigned long long>(kSummPrefetch))));
     }
 }
 

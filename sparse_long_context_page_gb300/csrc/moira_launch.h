@@ -51,10 +51,6 @@ struct AttendArgs {
     int hq, hkv, units, max_pages;
     long long num_pages;
     float scale_log2;
-    // the next layer's page summaries (decode step only; null otherwise):
-    // each block brings its share into L2 once its pages are issued
-    const uint8_t *next_summ;
-    unsigned long long next_summ_bytes;
 #ifdef MOIRA_CTA_TIMES
     unsigned long long *cta_times;   // [grid][2] (start, end) %globaltimer per block, or null
 #endif
