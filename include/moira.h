@@ -56,6 +56,13 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* Only the functions declared here are exported from the library. */
+#if defined(__GNUC__)
+#define MOIRA_API __attribute__((visibility("default")))
+#else
+#define MOIRA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -99,12 +106,12 @@ typedef struct moira_shape {
  * Returns 0 if the arguments are invalid.  One workspace may serve every
  * layer of a step issued in order on one stream; concurrent calls need
  * separate workspaces. */
-size_t moira_workspace_bytes(const moira_shape *shape, int32_t batch, int32_t max_pages);
+MOIRA_API size_t moira_workspace_bytes(const moira_shape *shape, int32_t batch, int32_t max_pages);
 
 /* Zero the workspace (device status word and the self-resetting merge
  * counters must start at zero).  Call once after allocating it.  Enqueues a
  * memset on `stream`; returns MOIRA_ECUDA if that fails. */
-moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream_t stream);
+MOIRA_API moira_status moira_workspace_init(void *workspace, size_t ws_bytes, moira_stream_t stream);
 
 /* Page-summary formats.  The estimator reads one summary per (page, KV head).
  * MOIRA_SUMM_BF16 stores the mean key as bf16 [P][Hkv][d].  The low-bit
@@ -139,7 +146,7 @@ typedef enum {
 /* Bytes of one physical page's summaries (all KV heads) in `format`, i.e.
  * one layer's summary buffer holds num_phys_pages times this.  0 if the shape
  * or the format is invalid. */
-size_t moira_summary_page_bytes(const moira_shape *shape, int32_t format);
+MOIRA_API size_t moira_summary_page_bytes(const moira_shape *shape, int32_t format);
 
 /* Page summaries, made when a page fills (the per-page metadata the "MOIRA"
  * abstract's estimate needs; estimator form: mean vectors, "Faster Flash
@@ -153,14 +160,14 @@ size_t moira_summary_page_bytes(const moira_shape *shape, int32_t format);
  *   phys_pages : int32 [n]             physical page ids; ids outside [0, P)
  *                                      are skipped (MOIRA_DEV_BADPAGE)
  * Not part of the decode step: call it when pages fill or after prefill. */
-moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool, void *summ,
+MOIRA_API moira_status moira_update_summaries(const moira_shape *shape, const void *k_pool, void *summ,
                                     const int32_t *phys_pages, int32_t n, moira_stream_t stream);
 
 /* moira_update_summaries in any summary format (moira_summ_format): `summ`
  * is that layer's summary buffer, num_phys_pages * moira_summary_page_bytes()
  * bytes, 16-byte aligned.  MOIRA_SUMM_BF16 is exactly moira_update_summaries.
  * An unknown format returns MOIRA_EINVAL. */
-moira_status moira_update_summaries_ex(const moira_shape *shape, int32_t format, const void *k_pool,
+MOIRA_API moira_status moira_update_summaries_ex(const moira_shape *shape, int32_t format, const void *k_pool,
                                        void *summ, const int32_t *phys_pages, int32_t n,
                                        moira_stream_t stream);
 
@@ -183,14 +190,14 @@ moira_status moira_update_summaries_ex(const moira_shape *shape, int32_t format,
  * A length beyond max_pages * S or a page id outside [0, P) skips that
  * request (no workspace, so nothing is recorded).  All buffers device,
  * 16-byte aligned. */
-moira_status moira_append_kv(const moira_shape *shape, const void *k_new, const void *v_new,
+MOIRA_API moira_status moira_append_kv(const moira_shape *shape, const void *k_new, const void *v_new,
                              void *k_pool, void *v_pool, void *summ, const int32_t *page_table,
                              const int32_t *seq_lens, int32_t batch, int32_t max_pages,
                              moira_stream_t stream);
 
 /* moira_append_kv with the summaries of filled pages written in `format`
  * (as moira_update_summaries_ex would write them). */
-moira_status moira_append_kv_ex(const moira_shape *shape, int32_t format, const void *k_new,
+MOIRA_API moira_status moira_append_kv_ex(const moira_shape *shape, int32_t format, const void *k_new,
                                 const void *v_new, void *k_pool, void *v_pool, void *summ,
                                 const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
                                 int32_t max_pages, moira_stream_t stream);
@@ -210,7 +217,7 @@ moira_status moira_append_kv_ex(const moira_shape *shape, int32_t format, const 
  *   lengths    : int32 [batch][Hkv] out
  * Equal masses are taken lower logical index first.  If rounding keeps the
  * total estimated mass below gamma, every page is kept. */
-moira_status moira_select(const moira_shape *shape, const void *q, const void *summ,
+MOIRA_API moira_status moira_select(const moira_shape *shape, const void *q, const void *summ,
                           const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
                           int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
                           int32_t *lengths, void *workspace, size_t ws_bytes,
@@ -234,7 +241,7 @@ typedef enum {
  * MOIRA_RULE_COVERAGE with param = gamma is exactly moira_select.  A `param`
  * outside the rule's range returns MOIRA_EINVAL and launches nothing.  The
  * rules let a caller compare selections that read the same number of bytes. */
-moira_status moira_select_rule(const moira_shape *shape, const void *q, const void *summ,
+MOIRA_API moira_status moira_select_rule(const moira_shape *shape, const void *q, const void *summ,
                                const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
                                int32_t max_pages, int32_t rule, float param, float sm_scale,
                                int32_t *lists, int32_t *lengths, void *workspace, size_t ws_bytes,
@@ -244,7 +251,7 @@ moira_status moira_select_rule(const moira_shape *shape, const void *q, const vo
  * estimator takes the summary's value, (code + 1/2) * step for the low-bit
  * formats, in place of the bf16 mean key; everything else is unchanged.
  * MOIRA_SUMM_BF16 is exactly moira_select_rule. */
-moira_status moira_select_ex(const moira_shape *shape, int32_t format, const void *q,
+MOIRA_API moira_status moira_select_ex(const moira_shape *shape, int32_t format, const void *q,
                              const void *summ, const int32_t *page_table, const int32_t *seq_lens,
                              int32_t batch, int32_t max_pages, int32_t rule, float param,
                              float sm_scale, int32_t *lists, int32_t *lengths, void *workspace,
@@ -268,7 +275,7 @@ moira_status moira_select_ex(const moira_shape *shape, int32_t format, const voi
  *   out        : fp32 [batch][Hq][d] out: softmax(sm_scale q K^T) V over the
  *                listed tokens; zero for an empty list
  * Computes in bf16 x bf16 -> fp32 on the tensor cores with fp32 softmax. */
-moira_status moira_attend(const moira_shape *shape, const void *q, const void *k_pool,
+MOIRA_API moira_status moira_attend(const moira_shape *shape, const void *q, const void *k_pool,
                           const void *v_pool, const int32_t *lists, const int32_t *lengths,
                           const int32_t *seq_lens, int32_t batch, int32_t max_pages,
                           float sm_scale, float *out, void *workspace, size_t ws_bytes,
@@ -289,7 +296,7 @@ moira_status moira_attend(const moira_shape *shape, const void *q, const void *k
  * once per device; another kernel that holds SMs for longer than the device
  * wait limit makes the launch report MOIRA_DEV_TIMEOUT).  Larger batches run
  * moira_select then moira_attend. */
-moira_status moira_select_attend(const moira_shape *shape, const void *q, const void *summ,
+MOIRA_API moira_status moira_select_attend(const moira_shape *shape, const void *q, const void *summ,
                                  const void *k_pool, const void *v_pool, const int32_t *page_table,
                                  const int32_t *seq_lens, int32_t batch, int32_t max_pages, float gamma,
                                  float sm_scale, int32_t *lists, int32_t *lengths, float *out,
@@ -298,7 +305,7 @@ moira_status moira_select_attend(const moira_shape *shape, const void *q, const 
 /* moira_select_attend reading summaries in `format` (moira_summ_format), as
  * moira_select_ex does with the coverage rule.  MOIRA_SUMM_BF16 is exactly
  * moira_select_attend. */
-moira_status moira_select_attend_ex(const moira_shape *shape, int32_t format, const void *q,
+MOIRA_API moira_status moira_select_attend_ex(const moira_shape *shape, int32_t format, const void *q,
                                     const void *summ, const void *k_pool, const void *v_pool,
                                     const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
                                     int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
@@ -311,7 +318,7 @@ moira_status moira_select_attend_ex(const moira_shape *shape, int32_t format, co
  * "MOIRA" abstract's estimated mass needs them).  Its results are internal
  * to the workspace; the call exists to time how a layer's work splits
  * between scoring and the rest.  Arguments and errors as moira_select_ex. */
-moira_status moira_score_ex(const moira_shape *shape, int32_t format, const void *q, const void *summ,
+MOIRA_API moira_status moira_score_ex(const moira_shape *shape, int32_t format, const void *q, const void *summ,
                             const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
                             int32_t max_pages, float sm_scale, void *workspace, size_t ws_bytes,
                             moira_stream_t stream);
@@ -319,7 +326,7 @@ moira_status moira_score_ex(const moira_shape *shape, int32_t format, const void
 /* 1 if moira_select_attend (and the coverage-rule decode step) takes the
  * single-launch form for these sizes on the current device, 0 if it runs
  * moira_select then moira_attend (or the arguments are invalid). */
-int32_t moira_select_attend_is_fused(const moira_shape *shape, int32_t batch, int32_t max_pages);
+MOIRA_API int32_t moira_select_attend_is_fused(const moira_shape *shape, int32_t batch, int32_t max_pages);
 
 /* One whole decode-attention step: for layer l = 0 .. num_layers-1,
  * moira_select then moira_attend on that layer's slices, in order on one
@@ -335,7 +342,7 @@ int32_t moira_select_attend_is_fused(const moira_shape *shape, int32_t batch, in
  * page_table and seq_lens must not change until the step's work is done:
  * from layer 1 on, the score kernel reads them while the previous layer's
  * attention is still finishing. */
-moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, const void *q_all,
+MOIRA_API moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, const void *q_all,
                                const void *k_pool_all, const void *v_pool_all,
                                const void *summ_all, const int32_t *page_table,
                                const int32_t *seq_lens, int32_t batch, int32_t max_pages,
@@ -347,7 +354,7 @@ moira_status moira_decode_step(const moira_shape *shape, int32_t num_layers, con
  * moira_select_ex(format, rule, param) then moira_attend.  summ_all holds
  * the layers' summary buffers back to back, num_phys_pages *
  * moira_summary_page_bytes() bytes each. */
-moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int32_t num_layers,
+MOIRA_API moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int32_t num_layers,
                                   const void *q_all, const void *k_pool_all,
                                   const void *v_pool_all, const void *summ_all,
                                   const int32_t *page_table, const int32_t *seq_lens,
@@ -361,7 +368,7 @@ moira_status moira_decode_step_ex(const moira_shape *shape, int32_t format, int3
  * q_dev, the step runs, and out_dev is copied back to out_host (fp32
  * [L][batch][Hq][d]).  Copies are cudaMemcpyAsync on `stream` (pinned host
  * memory makes them asynchronous); the call does not synchronise. */
-moira_status moira_decode_step_host(const moira_shape *shape, int32_t num_layers,
+MOIRA_API moira_status moira_decode_step_host(const moira_shape *shape, int32_t num_layers,
                                     const void *q_host, void *q_dev, const void *k_pool_all,
                                     const void *v_pool_all, const void *summ_all,
                                     const int32_t *page_table, const int32_t *seq_lens,
@@ -386,7 +393,7 @@ moira_status moira_decode_step_host(const moira_shape *shape, int32_t num_layers
  * another stream) race; calls in order on one stream do not.  Device-side
  * range problems are skipped or clamped as in moira_select, but the status
  * word is internal and not reported.  Never calls cudaMalloc or cudaFree. */
-moira_status moira_select_noalloc(const moira_shape *shape, const void *q, const void *summ,
+MOIRA_API moira_status moira_select_noalloc(const moira_shape *shape, const void *q, const void *summ,
                                   const int32_t *page_table, const int32_t *seq_lens,
                                   int32_t batch, int32_t max_pages, float gamma, float sm_scale,
                                   int32_t *lists, int32_t *lengths, moira_stream_t stream);
@@ -397,7 +404,7 @@ moira_status moira_select_noalloc(const moira_shape *shape, const void *q, const
  * MOIRA_DEV_TIMEOUT into the workspace status word.  Lets a caller check that
  * a wait that runs out is reported through moira_read_device_status and
  * leaves the context usable.  No paper counterpart. */
-moira_status moira_diag_wait_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns,
+MOIRA_API moira_status moira_diag_wait_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns,
                                      moira_stream_t stream);
 
 /* Diagnostic of the give-up rule of the device waits: one block waits on
@@ -406,7 +413,7 @@ moira_status moira_diag_wait_timeout(void *workspace, size_t ws_bytes, uint64_t 
  * (1 .. 10^10) and sets MOIRA_DEV_TIMEOUT, and every later wait of the block
  * gives up at once, so the launch takes about one limit, not n_waits.  No
  * paper counterpart. */
-moira_status moira_diag_wait_chain(void *workspace, size_t ws_bytes, uint64_t limit_ns, int32_t n_waits,
+MOIRA_API moira_status moira_diag_wait_chain(void *workspace, size_t ws_bytes, uint64_t limit_ns, int32_t n_waits,
                                    moira_stream_t stream);
 
 /* Diagnostic of the inter-block barrier of moira_select_attend: `blocks`
@@ -414,21 +421,21 @@ moira_status moira_diag_wait_chain(void *workspace, size_t ws_bytes, uint64_t li
  * never completes; each block gives up after `limit_ns` and sets
  * MOIRA_DEV_TIMEOUT.  Uses (and clears) bytes 128..255 of the workspace.
  * No paper counterpart. */
-moira_status moira_diag_barrier_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns, int32_t blocks,
+MOIRA_API moira_status moira_diag_barrier_timeout(void *workspace, size_t ws_bytes, uint64_t limit_ns, int32_t blocks,
                                         moira_stream_t stream);
 
 /* Synchronise `stream`, copy the device status word (MOIRA_DEV_* bits) to
  * *status_out (HOST pointer) and clear it when `clear` is non-zero.  A host
  * call: never issue it while `stream` is being captured. */
-moira_status moira_read_device_status(void *workspace, size_t ws_bytes, uint32_t *status_out,
+MOIRA_API moira_status moira_read_device_status(void *workspace, size_t ws_bytes, uint32_t *status_out,
                                       int32_t clear, moira_stream_t stream);
 
 /* Thread blocks of the attention grid on the current device (a multiple of
  * its SM count); a property used by tests and benchmarks. */
-int32_t moira_attend_grid_blocks(void);
+MOIRA_API int32_t moira_attend_grid_blocks(void);
 
 /* Static description of a status code. */
-const char *moira_status_string(moira_status status);
+MOIRA_API const char *moira_status_string(moira_status status);
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,7 @@ extern "C" {
  * 2 * blocks * max_launches uint64 words owned by the caller; the slices are
  * assigned when the launches are issued (so a captured graph keeps them).
  * NULL with 0 stops recording.  Host call; not thread-safe. */
-moira_status moira_set_cta_times(uint64_t *buf, int32_t max_launches);
+MOIRA_API moira_status moira_set_cta_times(uint64_t *buf, int32_t max_launches);
 
 #ifdef __cplusplus
 }

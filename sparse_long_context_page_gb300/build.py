@@ -51,7 +51,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         return LIB
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
-    flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2",
+    flags = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
                     "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
     if ptxas_info:
         flags += ["-Xptxas", "-v"]

@@ -126,13 +126,21 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, kBlocksPerSm)
 
 int attend_blocks_per_sm() { return kBlocksPerSm; }
 
+// Per-device records of the shared-memory limit set for each block shape.
+// They live at namespace scope with internal linkage: a static local of a
+// function template would be one object shared by every library in the
+// process that instantiates it (the load-balance build loaded next to this
+// one), and the other library's kernels would then skip their own setting.
+namespace {
+std::atomic<int> g_attend_smem_seen[2][64];
+}
+
 template <int NS, int NW>
 static cudaError_t launch_attend_shape(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                                        const AttendArgs &args, int blocks, cudaStream_t stream)
 {
     const size_t smem = attend_smem_bytes<NS, NW>(args.units);
-    static std::atomic<int> seen[64];
-    cudaError_t e = raise_smem_limit(k_attend<NS, NW>, smem, seen);
+    cudaError_t e = raise_smem_limit(k_attend<NS, NW>, smem, g_attend_smem_seen[NW == kFewWarps ? 0 : 1]);
     if (e != cudaSuccess) return e;
     return launch_pdl(k_attend<NS, NW>, dim3(blocks), dim3((NW + 1) * 32), smem, stream, tmap_k,
                       tmap_v, args);

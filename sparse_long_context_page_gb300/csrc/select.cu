@@ -1002,6 +1002,14 @@ __global__ void __launch_bounds__(kSelThreads) k_select(
 }
 
 // ---------------------------------------------------------------------------
+// Per-device records of each score launch shape's shared-memory limit and
+// single-wave capacity, at namespace scope with internal linkage (a static
+// local of the function template below would be shared with any other
+// library in the process that instantiates it).
+namespace {
+std::atomic<int> g_score_single_seen[3][64], g_score_single_fit[3][64][4], g_score_ring_seen[3][64];
+}
+
 template <int kFmt>
 cudaError_t launch_score_fmt(const void *q, const void *summ, const int32_t *page_table,
                              const int32_t *seq_lens, int batch, int hq, int hkv, int max_pages,
@@ -1021,7 +1029,8 @@ cudaError_t launch_score_fmt(const void *q, const void *summ, const int32_t *pag
     if (e != cudaSuccess) return e;
     // single wave: one block per item with one stage, when every item fits
     // (resident blocks cached per (device, Hkv): they never change in a context)
-    static std::atomic<int> single_seen[64], single_fit[64][4];
+    std::atomic<int> *single_seen = g_score_single_seen[kFmt];
+    std::atomic<int>(*single_fit)[4] = g_score_single_fit[kFmt];
     const int hk = hkv == 1 ? 0 : (hkv == 2 ? 1 : (hkv == 4 ? 2 : 3));
     int fit = dev < 64 ? single_fit[dev][hk].load(std::memory_order_relaxed) : 0;
     if (fit == 0) {
@@ -1040,7 +1049,7 @@ cudaError_t launch_score_fmt(const void *q, const void *summ, const int32_t *pag
                           max_pages, weights_ld(max_pages), num_pages, scale_log2, weights, chunks,
                           chunks_ld(max_pages), 1, early ? 1 : 0, status);
     // persistent: resident blocks with the ring and the plan's prefix array
-    static std::atomic<int> ring_seen[64];
+    std::atomic<int> *ring_seen = g_score_ring_seen[kFmt];
     const size_t smem = kStagesMax * stage_bytes + align_up(static_cast<size_t>(batch + 1) * 4, 16);
     if ((e = raise_smem_limit(k_score<kFmt, true>, smem, ring_seen)) != cudaSuccess) return e;
     int per_sm = 0;

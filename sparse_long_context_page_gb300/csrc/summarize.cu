@@ -6,9 +6,11 @@
 // mean vector of the page's keys, one of the block summaries named in
 // "Faster Flash Decoding", section 2 (related work).
 //
-// The 16 keys are summed in fp64 (exact for bf16 inputs of moderate range)
-// and the mean is rounded once to bf16, ties to even.  This runs when a page
-// fills, outside the decode step, so fp64 throughput does not matter here.
+// The mean of the 16 keys is their fp64 sum in token order divided by 16,
+// rounded once to bf16, ties to even.  The sum is formed exactly with 64-bit
+// integer adds of the keys' significands (page_dim_sum), which gives the
+// same bits as the fp64 sum without fp64 adds, whose rate on this GPU is far
+// below what the HBM stream of keys needs.
 //
 // Low-bit formats store the same fp64 mean in 8 or 2 bits per element with
 // the symmetric mid-rise quantiser that "Faster Flash Decoding", section 3.1,
@@ -43,21 +45,6 @@ __device__ __forceinline__ uint32_t f64_to_bf16_rne(double x)
     }
     const double grid = rint(fabs(x) * 0x1p133);                      // in [0, 128]
     return sign | static_cast<uint32_t>(grid);
-}
-
-// fp64 sums over the page's 16 tokens of this thread's two dimensions
-// (2*tid, 2*tid+1), in token order; `src` points at the thread's word of
-// token 0.
-__device__ __forceinline__ void token_sums(const uint32_t *src, double &lo, double &hi)
-{
-    lo = 0.0;
-    hi = 0.0;
-#pragma unroll
-    for (int t = 0; t < kPageSize; ++t) {
-        const uint32_t v = __ldg(src + t * (kHeadDim / 2));
-        lo += static_cast<double>(bf16_lo(v));
-        hi += static_cast<double>(bf16_hi(v));
-    }
 }
 
 // Write the low-bit summary of KV head j of one page into its record `rec`
@@ -106,44 +93,133 @@ __device__ void store_lowbit(double lo, double hi, uint8_t *rec, int j, int hkv)
         *reinterpret_cast<uint32_t *>(grp + gh * kCb + 4 * (gh + tid)) = 0u;
 }
 
-// One block per (listed page, KV head); 64 threads, two dimensions each.
-__global__ void __launch_bounds__(64) k_summarize(const uint32_t *__restrict__ k_pool,
-                                                  uint32_t *__restrict__ summ,
-                                                  const int32_t *__restrict__ phys_pages, int hkv,
-                                                  long long num_pages, uint32_t *status)
+// The fp64 sum, in token order, of one dimension of a page's 16 bf16 keys
+// (bit patterns in the low 16 bits of v[t]), computed exactly:
+//  * a key is sig * 2^(e - 134) with an integer significand sig < 256 (e = the
+//    exponent field, 1 for subnormals).  When the nonzero keys' exponents span
+//    at most 40, every partial sum is an integer multiple of 2^(emin - 134)
+//    below 2^52 in magnitude, so the sequential fp64 sum is exact and equals
+//    the 64-bit integer sum of the significands shifted to the smallest
+//    exponent, which is what is computed (integer adds, not fp64 ones);
+//  * wider spreads, infinities and NaNs take the sequential fp64 sum itself.
+// Either way the result is bit-identical to summing the keys in fp64 in
+// token order starting from +0.
+__device__ __forceinline__ double page_dim_sum(const uint32_t (&v)[kPageSize])
 {
-    const int item = blockIdx.x;
-    const int j = item % hkv;
-    const int idx = item / hkv;
-    const int p = phys_pages[idx];
-    if (p < 0 || p >= num_pages) {
-        if (threadIdx.x == 0 && status != nullptr) raise_status(status, kDevBadPage);
-        return;
+    int emax = -1, emin = 1 << 30;
+    bool special = false;
+#pragma unroll
+    for (int t = 0; t < kPageSize; ++t) {
+        const int e = static_cast<int>((v[t] >> 7) & 0xFFu);
+        special |= e == 0xFF;
+        if (v[t] & 0x7FFFu) {                           // nonzero
+            const int es = e > 0 ? e : 1;
+            emax = max(emax, es);
+            emin = min(emin, es);
+        }
     }
-    const size_t blk = (static_cast<size_t>(p) * hkv + j);
-    double lo, hi;
-    token_sums(k_pool + blk * (kPageSize * kHeadDim / 2) + threadIdx.x, lo, hi);
-    const uint32_t blo = f64_to_bf16_rne(lo * (1.0 / kPageSize));
-    const uint32_t bhi = f64_to_bf16_rne(hi * (1.0 / kPageSize));
-    summ[blk * (kHeadDim / 2) + threadIdx.x] = blo | (bhi << 16);
+    if (emax < 0) return 0.0;                           // every key is +-0: 0 + ... = +0
+    if (special || emax - emin > 40) {
+        double sum = 0.0;
+#pragma unroll
+        for (int t = 0; t < kPageSize; ++t) sum += static_cast<double>(__uint_as_float(v[t] << 16));
+        return sum;
+    }
+    long long acc = 0;
+#pragma unroll
+    for (int t = 0; t < kPageSize; ++t) {
+        const int e = static_cast<int>((v[t] >> 7) & 0xFFu);
+        const long long sig = static_cast<long long>((v[t] & 0x7Fu) | (e > 0 ? 0x80u : 0u));
+        const long long term = sig << max((e > 0 ? e : 1) - emin, 0);     // zeros: sig 0
+        acc += (v[t] & 0x8000u) ? -term : term;
+    }
+    return ldexp(static_cast<double>(acc), emin - 134);
 }
 
-// Low-bit summaries: one block per (listed page, KV head), 64 threads.
+// The low-bit record of KV head j from the warp's 128 fp64 means (lane l holds
+// dimensions 4l .. 4l+3); the same quantiser as store_lowbit.
 template <int kBits>
-__global__ void __launch_bounds__(64) k_summarize_lowbit(const uint32_t *__restrict__ k_pool,
-                                                         uint8_t *__restrict__ summ,
-                                                         const int32_t *__restrict__ phys_pages,
-                                                         int hkv, long long num_pages, int rec_bytes)
+__device__ void store_lowbit_warp(const double (&mean)[4], uint8_t *rec, int j, int hkv)
 {
-    const int item = blockIdx.x;
+    constexpr int kCb = lowbit_code_bytes(kBits);
+    constexpr double kHalf = static_cast<double>(1 << (kBits - 1));
+    const int lane = threadIdx.x & 31;
+    bool bad = false;
+    double a = 0.0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        bad |= !isfinite(mean[i]);
+        a = fmax(a, fabs(mean[i]));
+    }
+    if (bad) a = 0.0;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) a = fmax(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    const float step = any_bad ? 0.f : __double2float_rn(a / (kHalf - 0.5));
+    int c[4] = {0, 0, 0, 0};
+    if (step > 0.f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            c[i] = static_cast<int>(fmin(fmax(floor(mean[i] / static_cast<double>(step)), -kHalf), kHalf - 1.0));
+    }
+    const int gh = lowbit_group_heads(hkv), jj = j % gh;
+    uint8_t *grp = rec + (j / gh) * lowbit_group_bytes(kBits, hkv);
+    if constexpr (kBits == 8) {
+        *reinterpret_cast<uint32_t *>(grp + jj * kCb + 4 * lane) =
+            static_cast<uint32_t>(c[0] & 0xFF) | (static_cast<uint32_t>(c[1] & 0xFF) << 8) |
+            (static_cast<uint32_t>(c[2] & 0xFF) << 16) | (static_cast<uint32_t>(c[3] & 0xFF) << 24);
+    } else {
+        // element i sits in bits 2*(i%4) of byte i/4: the lane's 4 elements are byte `lane`
+        grp[jj * kCb + lane] = static_cast<uint8_t>((c[0] + 2) | ((c[1] + 2) << 2) | ((c[2] + 2) << 4) |
+                                                    ((c[3] + 2) << 6));
+    }
+    if (lane == 0) *reinterpret_cast<float *>(grp + gh * kCb + 4 * jj) = step;
+    if (jj == 0 && lane < kSummGroup - gh)                  // padding words after the steps
+        *reinterpret_cast<uint32_t *>(grp + gh * kCb + 4 * (gh + lane)) = 0u;
+}
+
+// One warp per (listed page, KV head), 8 per block: lane l loads 8 bytes
+// (dimensions 4l .. 4l+3) of each of the 16 token rows, all 16 loads in
+// flight, and forms the 4 means exactly (page_dim_sum).
+constexpr int kSumWarps = 8;
+
+template <int kFmt>
+__global__ void __launch_bounds__(kSumWarps * 32) k_summarize(const uint2 *__restrict__ k_pool,
+                                                               uint8_t *__restrict__ summ,
+                                                               const int32_t *__restrict__ phys_pages, int items,
+                                                               int hkv, long long num_pages, uint32_t *status)
+{
+    const int item = blockIdx.x * kSumWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (item >= items) return;                               // warp-uniform
     const int j = item % hkv;
     const int p = phys_pages[item / hkv];
-    if (p < 0 || p >= num_pages) return;                     // block-uniform
-    double lo, hi;
-    token_sums(k_pool + (static_cast<size_t>(p) * hkv + j) * (kPageSize * kHeadDim / 2) + threadIdx.x,
-               lo, hi);
-    store_lowbit<kBits>(lo * (1.0 / kPageSize), hi * (1.0 / kPageSize),
-                        summ + static_cast<size_t>(p) * rec_bytes, j, hkv);
+    if (p < 0 || p >= num_pages) {
+        if (lane == 0 && status != nullptr) raise_status(status, kDevBadPage);
+        return;
+    }
+    const size_t blk = static_cast<size_t>(p) * hkv + j;
+    const uint2 *src = k_pool + blk * (kPageSize * kHeadDim / 4) + lane;
+    uint2 row[kPageSize];
+#pragma unroll
+    for (int t = 0; t < kPageSize; ++t) row[t] = __ldg(src + t * (kHeadDim / 4));
+    double mean[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t v[kPageSize];
+#pragma unroll
+        for (int t = 0; t < kPageSize; ++t) v[t] = ((i < 2 ? row[t].x : row[t].y) >> (16 * (i & 1))) & 0xFFFFu;
+        mean[i] = page_dim_sum(v) * (1.0 / kPageSize);
+    }
+    if constexpr (kFmt == kSummBf16) {
+        uint2 out;
+        out.x = f64_to_bf16_rne(mean[0]) | (f64_to_bf16_rne(mean[1]) << 16);
+        out.y = f64_to_bf16_rne(mean[2]) | (f64_to_bf16_rne(mean[3]) << 16);
+        reinterpret_cast<uint2 *>(summ)[blk * (kHeadDim / 4) + lane] = out;
+    } else {
+        store_lowbit_warp<summ_bits(kFmt)>(mean, summ + static_cast<size_t>(p) * summ_page_bytes(kFmt, hkv), j,
+                                           hkv);
+    }
 }
 
 // Append one token per request to a paged pool (one block per (request, KV
@@ -151,8 +227,8 @@ __global__ void __launch_bounds__(64) k_summarize_lowbit(const uint32_t *__restr
 // seq_lens[r] - 1: slot (L-1) % S of logical page (L-1) / S.  When that slot
 // is the page's last, the page has just filled and its summary is computed
 // here: the 15 earlier keys are read back from the pool, the new one is
-// still in registers, and the mean is formed and stored as in k_summarize
-// (or k_summarize_lowbit, by `fmt`).
+// still in registers, and the mean is formed (fp64 in token order, which
+// page_dim_sum reproduces exactly) and stored as k_summarize stores it.
 __global__ void __launch_bounds__(64) k_append(const uint32_t *__restrict__ k_new,
                                                const uint32_t *__restrict__ v_new,
                                                uint32_t *__restrict__ k_pool, uint32_t *__restrict__ v_pool,
@@ -214,17 +290,16 @@ cudaError_t launch_summarize(const void *k_pool, void *summ, const int32_t *phys
                              cudaStream_t stream)
 {
     if (n <= 0) return cudaSuccess;
-    const unsigned grid = static_cast<unsigned>(n) * hkv;
-    const uint32_t *kp = static_cast<const uint32_t *>(k_pool);
+    const int items = n * hkv;
+    const unsigned grid = static_cast<unsigned>((items + kSumWarps - 1) / kSumWarps);
+    const uint2 *kp = static_cast<const uint2 *>(k_pool);
+    uint8_t *sm = static_cast<uint8_t *>(summ);
     if (fmt == kSummQ8)
-        k_summarize_lowbit<8><<<grid, 64, 0, stream>>>(kp, static_cast<uint8_t *>(summ), phys_pages,
-                                                       hkv, num_pages, summ_page_bytes(fmt, hkv));
+        k_summarize<kSummQ8><<<grid, kSumWarps * 32, 0, stream>>>(kp, sm, phys_pages, items, hkv, num_pages, status);
     else if (fmt == kSummQ2)
-        k_summarize_lowbit<2><<<grid, 64, 0, stream>>>(kp, static_cast<uint8_t *>(summ), phys_pages,
-                                                       hkv, num_pages, summ_page_bytes(fmt, hkv));
+        k_summarize<kSummQ2><<<grid, kSumWarps * 32, 0, stream>>>(kp, sm, phys_pages, items, hkv, num_pages, status);
     else
-        k_summarize<<<grid, 64, 0, stream>>>(kp, static_cast<uint32_t *>(summ), phys_pages, hkv,
-                                             num_pages, status);
+        k_summarize<kSummBf16><<<grid, kSumWarps * 32, 0, stream>>>(kp, sm, phys_pages, items, hkv, num_pages, status);
     return cudaGetLastError();
 }
 
