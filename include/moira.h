@@ -386,9 +386,11 @@ MOIRA_API moira_status moira_decode_step_host(const moira_shape *shape, int32_t 
  * per-chunk softmax normalisers, about 4*batch*Hq*max_pages bytes) lives in
  * a 4 MiB array compiled into the library, which every GPU that loads the
  * library holds until the process exits; sizes that need more return
- * MOIRA_EUNSUPPORTED and launch nothing.  The first call on a device looks
- * up the array's device address with that device current, so make it before
- * any stream capture.  All calls share the array: calls that overlap on the
+ * MOIRA_EUNSUPPORTED and launch nothing.  Arguments are checked as
+ * moira_select checks them (same codes).  The call runs on the current
+ * device: `stream` must belong to it (else MOIRA_EINVAL, nothing launched).
+ * The first call on a device looks up the array's device address with that
+ * device current, so make it before any stream capture.  All calls share the array: calls that overlap on the
  * GPU (different streams, or a call still running when the next starts on
  * another stream) race; calls in order on one stream do not.  Device-side
  * range problems are skipped or clamped as in moira_select, but the status

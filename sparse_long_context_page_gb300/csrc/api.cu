@@ -12,6 +12,7 @@
 #ifdef MOIRA_CTA_TIMES
 #include "../../include/moira_cta_times.h"
 #endif
+#include "checks.h"
 #include "moira_device.cuh"
 #include "moira_launch.h"
 
@@ -32,29 +33,6 @@ int current_sm_count()
 // The attention grid: every SM holds attend_blocks_per_sm() resident blocks
 // (one wave; each block takes an equal range of the concatenated lists).
 int attend_blocks() { return current_sm_count() * attend_blocks_per_sm(); }
-
-moira_status check_shape(const moira_shape *s)
-{
-    if (!s) return MOIRA_EINVAL;
-    if (s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->head_dim <= 0 || s->page_size <= 0 ||
-        s->num_phys_pages <= 0)
-        return MOIRA_EINVAL;
-    if (s->num_q_heads % s->num_kv_heads != 0) return MOIRA_EINVAL;
-    if (s->head_dim != kHeadDim || s->page_size != kPageSize) return MOIRA_EUNSUPPORTED;
-    if (s->num_q_heads / s->num_kv_heads != kGroup) return MOIRA_EUNSUPPORTED;
-    if (32 % s->num_kv_heads != 0) return MOIRA_EUNSUPPORTED;       // Hkv in {1, 2, 4, 8}
-    // TMA row coordinates are 32-bit: P * Hkv * S rows per layer pool.
-    if (s->num_phys_pages * s->num_kv_heads * kPageSize >= (1LL << 31)) return MOIRA_EUNSUPPORTED;
-    return MOIRA_OK;
-}
-
-moira_status check_batch(const moira_shape *s, int32_t batch, int32_t max_pages)
-{
-    if (batch <= 0 || max_pages <= 0) return MOIRA_EINVAL;
-    if (max_pages > kMaxPagesPerSeq) return MOIRA_EUNSUPPORTED;
-    if (static_cast<long long>(batch) * s->num_kv_heads > kMaxUnits) return MOIRA_EUNSUPPORTED;
-    return MOIRA_OK;
-}
 
 WsLayout layout_for(const moira_shape *s, int32_t batch, int32_t max_pages)
 {
@@ -243,6 +221,12 @@ moira_status select_attend_impl(const moira_shape *shape, int32_t fmt, const voi
     return cuda_status(launch_select_attend(mk, mv, f, blocks, stream));
 }
 
+}  // namespace
+
+// ---------------------------------------------------------------- argument checks (checks.h)
+
+namespace {
+
 bool finite_pos(float x) { return std::isfinite(x) && x > 0.f; }
 
 bool valid_format(int32_t fmt)
@@ -264,7 +248,50 @@ bool valid_rule(int32_t rule, float param)
     }
 }
 
+bool aligned16_ptr(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
 }  // namespace
+
+namespace moira {
+
+moira_status check_shape(const moira_shape *s)
+{
+    if (!s) return MOIRA_EINVAL;
+    if (s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->head_dim <= 0 || s->page_size <= 0 ||
+        s->num_phys_pages <= 0)
+        return MOIRA_EINVAL;
+    if (s->num_q_heads % s->num_kv_heads != 0) return MOIRA_EINVAL;
+    if (s->head_dim != kHeadDim || s->page_size != kPageSize) return MOIRA_EUNSUPPORTED;
+    if (s->num_q_heads / s->num_kv_heads != kGroup) return MOIRA_EUNSUPPORTED;
+    if (32 % s->num_kv_heads != 0) return MOIRA_EUNSUPPORTED;       // Hkv in {1, 2, 4, 8}
+    // TMA row coordinates are 32-bit: P * Hkv * S rows per layer pool.
+    if (s->num_phys_pages * s->num_kv_heads * kPageSize >= (1LL << 31)) return MOIRA_EUNSUPPORTED;
+    return MOIRA_OK;
+}
+
+moira_status check_batch(const moira_shape *s, int32_t batch, int32_t max_pages)
+{
+    if (batch <= 0 || max_pages <= 0) return MOIRA_EINVAL;
+    if (max_pages > kMaxPagesPerSeq) return MOIRA_EUNSUPPORTED;
+    if (static_cast<long long>(batch) * s->num_kv_heads > kMaxUnits) return MOIRA_EUNSUPPORTED;
+    return MOIRA_OK;
+}
+
+moira_status check_select_args(const moira_shape *shape, int32_t fmt, const void *q, const void *summ,
+                               const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                               int32_t max_pages, int32_t rule, float param, float sm_scale,
+                               const int32_t *lists, const int32_t *lengths)
+{
+    moira_status st = check_shape(shape);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
+    if (!valid_format(fmt) || !valid_rule(rule, param) || !finite_pos(sm_scale)) return MOIRA_EINVAL;
+    if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
+    if (!aligned16_ptr(q) || !aligned16_ptr(summ)) return MOIRA_EINVAL;
+    return MOIRA_OK;
+}
+
+}  // namespace moira
 
 #ifdef MOIRA_CTA_TIMES
 // Load-balance build only (include/moira_cta_times.h): where the next
@@ -360,13 +387,9 @@ moira_status moira_select_ex(const moira_shape *shape, int32_t format, const voi
                              float sm_scale, int32_t *lists, int32_t *lengths, void *workspace,
                              size_t ws_bytes, moira_stream_t stream)
 {
-    moira_status st = check_shape(shape);
+    moira_status st = check_select_args(shape, format, q, summ, page_table, seq_lens, batch, max_pages,
+                                        rule, param, sm_scale, lists, lengths);
     if (st != MOIRA_OK) return st;
-    if ((st = check_batch(shape, batch, max_pages)) != MOIRA_OK) return st;
-    if (!valid_format(format) || !valid_rule(rule, param) || !finite_pos(sm_scale))
-        return MOIRA_EINVAL;
-    if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
-    if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
     if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
     return select_impl(shape, format, q, summ, page_table, seq_lens, batch, max_pages, rule, param,
                        sm_scale, lists, lengths, workspace, ws_bytes, false,

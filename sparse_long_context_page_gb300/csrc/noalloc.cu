@@ -16,11 +16,14 @@
 // the last call's contents; the kernels overwrite every scratch element they
 // read, and the status word is cleared on every call.  Two calls that overlap
 // on the GPU (different streams, or one call in flight while another starts)
-// race on the array; calls issued in order on one stream do not.
+// race on the array; calls issued in order on one stream do not.  The
+// arguments are checked exactly as moira_select checks them (checks.h), and
+// the stream must belong to the current device.
 #include <cmath>
 #include <mutex>
 
 #include "../../include/moira.h"
+#include "checks.h"
 #include "moira_device.cuh"
 #include "moira_launch.h"
 
@@ -49,8 +52,6 @@ moira_status scratch_address(void **out)
     return MOIRA_OK;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" moira_status moira_select_noalloc(const moira_shape *shape, const void *q,
@@ -61,21 +62,16 @@ extern "C" moira_status moira_select_noalloc(const moira_shape *shape, const voi
                                              moira_stream_t stream)
 {
     using namespace moira;
-    if (!shape || shape->num_q_heads <= 0 || shape->num_kv_heads <= 0 ||
-        shape->num_phys_pages <= 0 || shape->num_q_heads % shape->num_kv_heads != 0)
-        return MOIRA_EINVAL;
-    if (shape->head_dim != kHeadDim || shape->page_size != kPageSize ||
-        shape->num_q_heads / shape->num_kv_heads != kGroup || 32 % shape->num_kv_heads != 0 ||
-        shape->num_phys_pages * shape->num_kv_heads * kPageSize >= (1LL << 31))
-        return MOIRA_EUNSUPPORTED;
-    if (batch <= 0 || max_pages <= 0) return MOIRA_EINVAL;
-    if (max_pages > kMaxPagesPerSeq ||
-        static_cast<long long>(batch) * shape->num_kv_heads > kMaxUnits)
-        return MOIRA_EUNSUPPORTED;
-    if (!(gamma > 0.f && gamma <= 1.f) || !std::isfinite(sm_scale) || !(sm_scale > 0.f))
-        return MOIRA_EINVAL;
-    if (!q || !summ || !page_table || !seq_lens || !lists || !lengths) return MOIRA_EINVAL;
-    if (!aligned16(q) || !aligned16(summ)) return MOIRA_EINVAL;
+    moira_status st = check_select_args(shape, MOIRA_SUMM_BF16, q, summ, page_table, seq_lens, batch,
+                                        max_pages, MOIRA_RULE_COVERAGE, gamma, sm_scale, lists, lengths);
+    if (st != MOIRA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the scratch address and the launches are the current device's: a
+    // stream of another device is refused rather than launched into
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess)
+        return MOIRA_ECUDA;
+    if (sdev != cur) return MOIRA_EINVAL;
 
     // scratch: status word | page weights [batch][Hq][ld] | chunk (max, sum) [batch][Hq][ldc]
     const int hq = shape->num_q_heads;
@@ -86,13 +82,11 @@ extern "C" moira_status moira_select_noalloc(const moira_shape *shape, const voi
     if (need > kNoAllocBytes) return MOIRA_EUNSUPPORTED;     // beyond the compiled-in scratch
 
     void *base = nullptr;
-    moira_status st = scratch_address(&base);
-    if (st != MOIRA_OK) return st;
+    if ((st = scratch_address(&base)) != MOIRA_OK) return st;
     uint8_t *w = static_cast<uint8_t *>(base);
     uint32_t *status = reinterpret_cast<uint32_t *>(w);
     float *scores = reinterpret_cast<float *>(w + off_scores);
     float *chunks = reinterpret_cast<float *>(w + off_chunks);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     if (cudaMemsetAsync(status, 0, sizeof(uint32_t), s) != cudaSuccess) return MOIRA_ECUDA;
     const bool dense = gamma >= 1.0f;

@@ -8,7 +8,8 @@ once):
     the gamma boundary: its oracle cumulative-mass interval [C_before,
     C_through] meets [gamma - 1e-4, gamma + 1e-4], or its oracle mass equals
     the oracle's cut mass to 1e-6 relative (fp32 vs fp64 reordering of
-    near-equal masses);
+    near-equal masses; the tests count the pages only this second clause
+    excuses and bound them, TIE_ONLY_MAX per test);
   * the CUDA set must still cover gamma under the oracle's masses (to 1e-4);
   * lengths must match exactly unless the oracle's running sum crosses gamma
     within 1e-4 of it, where one page more or less is allowed;
@@ -25,6 +26,7 @@ from oracle import oracle
 
 BAND = 1e-4
 TIE_REL = 1e-6
+TIE_ONLY_MAX = 8          # pages per test that only the equal-mass clause may excuse
 MAX_ABS = 1e-2
 REL_L2 = 1e-3
 
@@ -98,8 +100,10 @@ class UnitData:
         return np.array([inv.get(int(p), -1) for p in phys_list], np.int64)
 
 
-def check_list(ud: UnitData, gpu_phys: np.ndarray, gamma: float) -> str | None:
-    """None if the CUDA list is acceptable against the oracle, else a reason."""
+def check_list(ud: UnitData, gpu_phys: np.ndarray, gamma: float, stats: dict | None = None) -> str | None:
+    """None if the CUDA list is acceptable against the oracle, else a reason.
+    With `stats`, stats["tie_only"] counts the differing pages that only the
+    equal-mass clause (not the gamma band) excuses."""
     lg = ud.to_logical(gpu_phys)
     if np.any(lg < 0):
         return f"unknown physical page ids {gpu_phys[lg < 0][:5]}"
@@ -126,6 +130,8 @@ def check_list(ud: UnitData, gpu_phys: np.ndarray, gamma: float) -> str | None:
         near_tie = abs(mass[p] - m_cut) <= TIE_REL * max(m_cut, 1e-30)
         if not (near_band or near_tie):
             bad.append((p, j, c_before, c_thru, mass[p]))
+        elif near_tie and not near_band and stats is not None:
+            stats["tie_only"] = stats.get("tie_only", 0) + 1
     if bad:
         return f"{len(bad)} pages differ away from the boundary, e.g. {bad[:3]} (k={k})"
     covered = mass[list(full_g)].sum() if full_g else 0.0

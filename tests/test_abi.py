@@ -187,3 +187,28 @@ def test_format_entry_points_reject_bad_arguments_on_host():
     assert lib.moira_decode_step_ex(sp, q8, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64,
                                     mb.RULE_TOPDELTA, 0.0, 0.1, FAKE, FAKE, FAKE, FAKE, 1 << 30,
                                     None) == 1
+
+
+def test_select_noalloc_rejects_what_select_rejects_on_host():
+    """moira_select_noalloc shares moira_select's argument checks: the same
+    bad arguments give the same codes, before any CUDA call."""
+    lib = moira.load_library()
+    ok = moira.Shape.of(32, 8, 1024)
+
+    def noalloc(shape=ok, q=FAKE, summ=FAKE, gamma=0.9, sm=0.088, batch=1, max_pages=64, lists=FAKE):
+        return lib.moira_select_noalloc(ctypes.byref(shape), q, summ, FAKE, FAKE, batch, max_pages, gamma,
+                                        sm, lists, FAKE, None)
+
+    cases = [dict(gamma=0.0), dict(gamma=1.5), dict(gamma=float("nan")), dict(sm=-1.0),
+             dict(sm=float("inf")), dict(q=0), dict(lists=0), dict(q=FAKE + 2), dict(summ=FAKE + 8),
+             dict(batch=0), dict(max_pages=mb.MAX_PAGES_PER_SEQ + 1), dict(batch=mb.MAX_UNITS // 8 + 1),
+             dict(shape=moira.Shape.of(32, 8, 1024, head_dim=64)), dict(shape=moira.Shape.of(16, 8, 1024)),
+             dict(shape=moira.Shape.of(30, 8, 1024)), dict(shape=moira.Shape.of(32, 8, 0)),
+             dict(shape=moira.Shape.of(32, 8, 1 << 25))]
+    for kw in cases:
+        sel = _select(lib, kw.get("shape", ok), gamma=kw.get("gamma", 0.9), sm=kw.get("sm", 0.088),
+                      q=kw.get("q", FAKE), batch=kw.get("batch", 1), max_pages=kw.get("max_pages", 64))
+        got = noalloc(**kw)
+        assert got in (1, 4), (kw, got)
+        if not ({"lists", "summ"} & kw.keys()):
+            assert got == sel, (kw, got, sel)

@@ -26,9 +26,12 @@ def _state(name, seed=0, max_pages=None, **over):
     return w, st
 
 
-def _check_layer(w, st, l, gamma, units=None, check_out=True):
+def _check_layer(w, st, l, gamma, units=None, check_out=True, stats=None):
     """Select + attend one layer on the GPU and compare every (or the given)
-    unit with the oracle.  Returns (units checked, outputs compared)."""
+    unit with the oracle: its list by the comparison rules, and its output
+    with the oracle's attention over the GPU's own list (so a list that
+    differs at the gamma boundary is still checked).  Returns (units
+    checked, outputs compared)."""
     lists = torch.zeros_like(st.lists)
     lengths = torch.zeros((w.spec.batch, w.spec.kv_heads), dtype=torch.int32, device="cuda")
     st.select_layer(l, gamma, lists, lengths)
@@ -43,13 +46,15 @@ def _check_layer(w, st, l, gamma, units=None, check_out=True):
     for (r, j) in units:
         ud = H.UnitData(w, l, r, j)
         gl = lists_h[r, j, :len_h[r, j]]
-        why = H.check_list(ud, gl, gamma)
+        why = H.check_list(ud, gl, gamma, stats)
         assert why is None, f"layer {l} req {r} kv {j} gamma {gamma}: {why}"
-        o_list = ud.select(gamma)[0]
-        if check_out and np.array_equal(ud.to_logical(gl), o_list):
-            ref = ud.attend(o_list)
-            ma, rl = H.out_errors(out_h[r, j * G:(j + 1) * G], ref)
-            assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"l{l} r{r} j{j}: max-abs {ma:.3g} rel-L2 {rl:.3g}"
+        if check_out:
+            lg = ud.to_logical(gl)
+            if len(lg) == 0:
+                assert np.all(out_h[r, j * G:(j + 1) * G] == 0.0), f"l{l} r{r} j{j}: empty list not zero"
+            else:
+                ma, rl = H.out_errors(out_h[r, j * G:(j + 1) * G], ud.attend(lg))
+                assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"l{l} r{r} j{j}: max-abs {ma:.3g} rel-L2 {rl:.3g}"
             n_out += 1
     return len(units), n_out
 
@@ -84,13 +89,11 @@ def test_tiny_select_and_attend(gamma):
 ])
 def test_config_select_and_attend(name, over, gamma):
     w, st = _state(name, seed=11, **over)
-    total_u = total_o = 0
+    stats = {}
     for l in range(w.spec.layers):
-        nu, no = _check_layer(w, st, l, float(np.float32(gamma)))
-        total_u += nu
-        total_o += no
-    # units whose lists differ only at the boundary skip the output check; they must be few
-    assert total_o >= 0.8 * total_u, f"only {total_o}/{total_u} outputs compared"
+        nu, no = _check_layer(w, st, l, float(np.float32(gamma)), stats=stats)
+        assert no == nu
+    assert stats.get("tie_only", 0) <= H.TIE_ONLY_MAX, stats
 
 
 def test_select_edge_lengths():
@@ -313,27 +316,25 @@ def test_full_size_sampled_units(name, gamma):
     assert st.device_status() == 0
     rng = np.random.default_rng(123)
     L, B, Hkv, G = w.spec.layers, w.spec.batch, w.spec.kv_heads, w.group
-    picks = {(int(rng.integers(L)), int(rng.integers(B)), int(rng.integers(Hkv))) for _ in range(10)}
+    picks = sorted({(int(rng.integers(L)), int(rng.integers(B)), int(rng.integers(Hkv))) for _ in range(48)})
     out_h = st.out.cpu().numpy()
     len_h = st.lengths.cpu().numpy()
     lists = torch.zeros_like(st.lists)
-    compared = 0
-    for (l, r, j) in sorted(picks):
+    stats = {}
+    for l in sorted({p[0] for p in picks}):
         lengths = torch.zeros((B, Hkv), dtype=torch.int32, device="cuda")
-        st.select_layer(l, g32, lists, lengths)
+        st.select_layer(l, g32, lists, lengths)        # the step keeps only the last layer's lists
         torch.cuda.synchronize()
-        lh = lengths.cpu().numpy()
-        assert lh[r, j] == len_h[l, r, j]
-        gl = lists[r, j, :lh[r, j]].cpu().numpy()
-        ud = H.UnitData(w, l, r, j)
-        why = H.check_list(ud, gl, g32)
-        assert why is None, f"{name} l{l} r{r} j{j}: {why}"
-        o_list = ud.select(g32)[0]
-        if np.array_equal(ud.to_logical(gl), o_list):
-            ma, rl = H.out_errors(out_h[l, r, j * G:(j + 1) * G], ud.attend(o_list))
+        lh, ph = lengths.cpu().numpy(), lists.cpu().numpy()
+        assert np.array_equal(lh, len_h[l])
+        for (_, r, j) in [p for p in picks if p[0] == l]:
+            gl = ph[r, j, :lh[r, j]]
+            ud = H.UnitData(w, l, r, j)
+            why = H.check_list(ud, gl, g32, stats)
+            assert why is None, f"{name} l{l} r{r} j{j}: {why}"
+            ma, rl = H.out_errors(out_h[l, r, j * G:(j + 1) * G], ud.attend(ud.to_logical(gl)))
             assert ma <= H.MAX_ABS and rl <= H.REL_L2, f"{name} l{l} r{r} j{j}: {ma:.3g} {rl:.3g}"
-            compared += 1
-    assert compared >= len(picks) - 2
+    assert stats.get("tie_only", 0) <= H.TIE_ONLY_MAX, stats
     del st, w
     torch.cuda.empty_cache()
 

@@ -64,6 +64,37 @@ def test_noalloc_select_matches_workspace_select(name, over, gammas):
                         f"{name} gamma {g} call {call}: list ({r},{j}) differs"
 
 
+def test_noalloc_sequence_of_shapes():
+    """Calls of different shapes in a row share the one scratch array: a
+    large call, then a tiny one whose full-page count is not a multiple of 4
+    and whose tail is partial, then the large one again; each gives
+    moira_select's lists and lengths."""
+    lib = mb.load_library()
+    g = float(np.float32(0.99))
+    big = W.make_workload("llama8b_128k", seed=41, device="cuda", layers=1, batch=2)
+    small = W.make_workload(W.spec("llama8b_128k", batch=3, layers=1, context=(16 * 7 + 5, 16 * 13 + 1, 9)),
+                            seed=42, device="cuda")
+    states = []
+    for w in (big, small):
+        st = DecodeState(w)
+        st.summarize()
+        states.append(st)
+    for st in (states[0], states[1], states[0], states[1]):
+        B, Hkv = st.batch, st.w.spec.kv_heads
+        ref_lists = torch.full_like(st.lists, -7)
+        ref_len = torch.zeros((B, Hkv), dtype=torch.int32, device="cuda")
+        st.select_layer(0, g, ref_lists, ref_len)
+        lists = torch.full_like(st.lists, -7)
+        lengths = torch.full((B, Hkv), -1, dtype=torch.int32, device="cuda")
+        assert _noalloc(lib, st, 0, g, lists, lengths) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(lengths, ref_len)
+        lh, rh, n = lists.cpu().numpy(), ref_lists.cpu().numpy(), ref_len.cpu().numpy()
+        for r in range(B):
+            for j in range(Hkv):
+                assert np.array_equal(lh[r, j, :n[r, j]], rh[r, j, :n[r, j]]), (B, r, j)
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     lib = mb.load_library()
     w = W.make_workload("tiny", seed=1, device="cuda")
