@@ -7,10 +7,14 @@
 // "Faster Flash Decoding", section 2 (related work).
 //
 // The mean of the 16 keys is their fp64 sum in token order divided by 16,
-// rounded once to bf16, ties to even.  The sum is formed exactly with 64-bit
-// integer adds of the keys' significands (page_dim_sum), which gives the
-// same bits as the fp64 sum without fp64 adds, whose rate on this GPU is far
-// below what the HBM stream of keys needs.
+// rounded once to bf16, ties to even.  Wherever that sum is exact it is
+// formed without fp64, whose rate on this GPU is far below what the HBM
+// stream of keys needs: in fp32 when the keys' exponents span at most 12
+// (every partial sum then fits 24 bits), else with 64-bit integer adds of
+// the keys' significands when they span at most 40 (page_dim_sum_fixed),
+// rounded to bf16 by integer arithmetic; only wider spreads, infinities and
+// NaNs take fp64 adds in token order.  All three give the bits of the fp64
+// sum.
 //
 // Low-bit formats store the same fp64 mean in 8 or 2 bits per element with
 // the symmetric mid-rise quantiser that "Faster Flash Decoding", section 3.1,
@@ -20,6 +24,8 @@
 // standing for (code + 1/2) * step; no zero level, so signs survive.  A
 // non-finite mean element, a zero mean or a step that rounds to 0 gives
 // step 0 and codes 0.
+#include <cuda_bf16.h>
+
 #include "moira_device.cuh"
 #include "moira_launch.h"
 
@@ -93,18 +99,17 @@ __device__ void store_lowbit(double lo, double hi, uint8_t *rec, int j, int hkv)
         *reinterpret_cast<uint32_t *>(grp + gh * kCb + 4 * (gh + tid)) = 0u;
 }
 
-// The fp64 sum, in token order, of one dimension of a page's 16 bf16 keys
-// (bit patterns in the low 16 bits of v[t]), computed exactly:
+// The exact sum, in token order, of one dimension of a page's 16 bf16 keys
+// (bit patterns in the low 16 bits of v[t]), when their exponents allow it:
 //  * a key is sig * 2^(e - 134) with an integer significand sig < 256 (e = the
 //    exponent field, 1 for subnormals).  When the nonzero keys' exponents span
 //    at most 40, every partial sum is an integer multiple of 2^(emin - 134)
 //    below 2^52 in magnitude, so the sequential fp64 sum is exact and equals
 //    the 64-bit integer sum of the significands shifted to the smallest
-//    exponent, which is what is computed (integer adds, not fp64 ones);
-//  * wider spreads, infinities and NaNs take the sequential fp64 sum itself.
-// Either way the result is bit-identical to summing the keys in fp64 in
-// token order starting from +0.
-__device__ __forceinline__ double page_dim_sum(const uint32_t (&v)[kPageSize])
+//    exponent: returns true with that sum in `acc` and emin in `emin`
+//    (acc == 0 when every key is +-0 or they cancel: the fp64 sum is +0);
+//  * wider spreads, infinities and NaNs return false.
+__device__ __forceinline__ bool page_dim_sum_fixed(const uint32_t (&v)[kPageSize], long long &acc, int &emin_out)
 {
     int emax = -1, emin = 1 << 30;
     bool special = false;
@@ -118,14 +123,10 @@ __device__ __forceinline__ double page_dim_sum(const uint32_t (&v)[kPageSize])
             emin = min(emin, es);
         }
     }
-    if (emax < 0) return 0.0;                           // every key is +-0: 0 + ... = +0
-    if (special || emax - emin > 40) {
-        double sum = 0.0;
-#pragma unroll
-        for (int t = 0; t < kPageSize; ++t) sum += static_cast<double>(__uint_as_float(v[t] << 16));
-        return sum;
-    }
-    long long acc = 0;
+    acc = 0;
+    emin_out = 1;
+    if (emax < 0) return true;                          // every key is +-0: 0 + ... = +0
+    if (special || emax - emin > 40) return false;
 #pragma unroll
     for (int t = 0; t < kPageSize; ++t) {
         const int e = static_cast<int>((v[t] >> 7) & 0xFFu);
@@ -133,7 +134,53 @@ __device__ __forceinline__ double page_dim_sum(const uint32_t (&v)[kPageSize])
         const long long term = sig << max((e > 0 ? e : 1) - emin, 0);     // zeros: sig 0
         acc += (v[t] & 0x8000u) ? -term : term;
     }
-    return ldexp(static_cast<double>(acc), emin - 134);
+    emin_out = emin;
+    return true;
+}
+
+// The fp64 sum of the same keys in token order, starting from +0.
+__device__ __forceinline__ double page_dim_sum_f64(const uint32_t (&v)[kPageSize])
+{
+    double sum = 0.0;
+#pragma unroll
+    for (int t = 0; t < kPageSize; ++t) sum += static_cast<double>(__uint_as_float(v[t] << 16));
+    return sum;
+}
+
+// The fp64 sum of one dimension's 16 keys in token order, bit-exact (the
+// integer form where it applies, fp64 adds otherwise).
+__device__ __forceinline__ double page_dim_sum(const uint32_t (&v)[kPageSize])
+{
+    long long acc;
+    int emin;
+    if (page_dim_sum_fixed(v, acc, emin)) return ldexp(static_cast<double>(acc), emin - 134);
+    return page_dim_sum_f64(v);
+}
+
+// acc * 2^e2 (|acc| < 2^62, finite and within the bf16 range once rounded)
+// rounded to the nearest bf16, ties to even, by integer arithmetic.  The
+// result's last place is 2^(e_lead - 7) for a leading bit of weight
+// 2^e_lead >= 2^-126, else the subnormal step 2^-133; q, the rounded
+// significand on that place, then gives the encoding as
+// ((place + 133) << 7) + q for both kinds, a carry to q = 256 included.
+__device__ __forceinline__ uint32_t fixed_to_bf16_rne(long long acc, int e2)
+{
+    if (acc == 0) return 0u;                            // an exact sum of 0 is +0
+    const uint32_t sign = acc < 0 ? 0x8000u : 0u;
+    const unsigned long long m =
+        acc < 0 ? 0ull - static_cast<unsigned long long>(acc) : static_cast<unsigned long long>(acc);
+    const int e_lead = 63 - __clzll(static_cast<long long>(m)) + e2;
+    const int place = max(e_lead - 7, -133);
+    const int sh = place - e2;                          // bits of m below the result's last place
+    unsigned long long q;
+    if (sh <= 0) {
+        q = m << (-sh);
+    } else {
+        q = m >> sh;
+        const unsigned long long rem = m & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
+        q += (rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull;
+    }
+    return sign | (static_cast<uint32_t>(place + 133) << 7) + static_cast<uint32_t>(q);
 }
 
 // The low-bit record of KV head j from the warp's 128 fp64 means (lane l holds
@@ -184,7 +231,7 @@ __device__ void store_lowbit_warp(const double (&mean)[4], uint8_t *rec, int j, 
 constexpr int kSumWarps = 8;
 
 template <int kFmt>
-__global__ void __launch_bounds__(kSumWarps * 32) k_summarize(const uint2 *__restrict__ k_pool,
+__global__ void __launch_bounds__(kSumWarps * 32, 3) k_summarize(const uint2 *__restrict__ k_pool,
                                                                uint8_t *__restrict__ summ,
                                                                const int32_t *__restrict__ phys_pages, int items,
                                                                int hkv, long long num_pages, uint32_t *status)
@@ -203,20 +250,56 @@ __global__ void __launch_bounds__(kSumWarps * 32) k_summarize(const uint2 *__res
     uint2 row[kPageSize];
 #pragma unroll
     for (int t = 0; t < kPageSize; ++t) row[t] = __ldg(src + t * (kHeadDim / 4));
-    double mean[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t v[kPageSize];
-#pragma unroll
-        for (int t = 0; t < kPageSize; ++t) v[t] = ((i < 2 ? row[t].x : row[t].y) >> (16 * (i & 1))) & 0xFFFFu;
-        mean[i] = page_dim_sum(v) * (1.0 / kPageSize);
-    }
     if constexpr (kFmt == kSummBf16) {
-        uint2 out;
-        out.x = f64_to_bf16_rne(mean[0]) | (f64_to_bf16_rne(mean[1]) << 16);
-        out.y = f64_to_bf16_rne(mean[2]) | (f64_to_bf16_rne(mean[3]) << 16);
-        reinterpret_cast<uint2 *>(summ)[blk * (kHeadDim / 4) + lane] = out;
+        // exponent fields of the lane's 4 dimensions (16-bit halves of the two
+        // words), smallest and largest over the 16 tokens
+        uint32_t mn[2] = {0xFFFFFFFFu, 0xFFFFFFFFu}, mx[2] = {0u, 0u};
+#pragma unroll
+        for (int t = 0; t < kPageSize; ++t) {
+            const uint32_t ex = row[t].x & 0x7F807F80u, ey = row[t].y & 0x7F807F80u;
+            mn[0] = __vminu2(mn[0], ex);
+            mx[0] = __vmaxu2(mx[0], ex);
+            mn[1] = __vminu2(mn[1], ey);
+            mx[1] = __vmaxu2(mx[1], ey);
+        }
+        uint32_t out[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int sh = 16 * (i & 1);
+            const uint32_t lo = (mn[i >> 1] >> sh) & 0xFFFFu, hi = (mx[i >> 1] >> sh) & 0xFFFFu;
+            // every key normal (exponent field >= 1, so no zeros either), the
+            // largest below 2^124 (16 of them stay below the fp32 limit) and a
+            // span of at most 12: every fp32 partial sum is exact
+            if (lo >= (1u << 7) && hi <= (250u << 7) && hi - lo <= (12u << 7)) {
+                float sum = 0.f;
+#pragma unroll
+                for (int t = 0; t < kPageSize; ++t) {
+                    const uint32_t w = i < 2 ? row[t].x : row[t].y;
+                    sum += __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+                }
+                out[i] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(sum * (1.f / kPageSize))));
+            } else {
+                uint32_t v[kPageSize];
+#pragma unroll
+                for (int t = 0; t < kPageSize; ++t) v[t] = ((i < 2 ? row[t].x : row[t].y) >> sh) & 0xFFFFu;
+                long long acc;
+                int emin;
+                out[i] = page_dim_sum_fixed(v, acc, emin)
+                             ? fixed_to_bf16_rne(acc, emin - 134 - 4)
+                             : f64_to_bf16_rne(page_dim_sum_f64(v) * (1.0 / kPageSize));
+            }
+        }
+        reinterpret_cast<uint2 *>(summ)[blk * (kHeadDim / 4) + lane] =
+            make_uint2(out[0] | (out[1] << 16), out[2] | (out[3] << 16));
     } else {
+        double mean[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t v[kPageSize];
+#pragma unroll
+            for (int t = 0; t < kPageSize; ++t) v[t] = ((i < 2 ? row[t].x : row[t].y) >> (16 * (i & 1))) & 0xFFFFu;
+            mean[i] = page_dim_sum(v) * (1.0 / kPageSize);
+        }
         store_lowbit_warp<summ_bits(kFmt)>(mean, summ + static_cast<size_t>(p) * summ_page_bytes(kFmt, hkv), j,
                                            hkv);
     }

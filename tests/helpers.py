@@ -12,7 +12,9 @@ once):
     excuses and bound them, TIE_ONLY_MAX per test);
   * the CUDA set must still cover gamma under the oracle's masses (to 1e-4);
   * lengths must match exactly unless the oracle's running sum crosses gamma
-    within 1e-4 of it, where one page more or less is allowed;
+    within 1e-4 of it; then they may differ by at most the number of pages
+    whose cumulative-mass interval meets the band (one, unless the masses at
+    the cut are below 1e-4, as in the flat tail of gamma near 1);
   * structure: ascending logical order, the partial tail page last;
   * attention output (fp32) within max-abs 1e-2 and relative L2 1e-3 per
     (request, query head) row (bf16 inputs, fp32 accumulation).
@@ -140,7 +142,9 @@ def check_list(ud: UnitData, gpu_phys: np.ndarray, gamma: float, stats: dict | N
     if len(full_g) != k:
         c_km1 = cum[k - 2] if k >= 2 else 0.0
         near = abs(cum[k - 1] - gamma) <= BAND or abs(c_km1 - gamma) <= BAND
-        if not near or abs(len(full_g) - k) > 1:
+        before = np.concatenate([[0.0], cum[:-1]])
+        in_band = int(np.count_nonzero((before <= gamma + BAND) & (cum >= gamma - BAND)))
+        if not near or abs(len(full_g) - k) > max(1, in_band):
             return f"length {len(full_g)} vs oracle {k} (C_k-1={c_km1:.7f}, C_k={cum[k-1]:.7f})"
     return None
 

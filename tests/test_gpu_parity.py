@@ -98,12 +98,14 @@ def test_config_select_and_attend(name, over, gamma):
 
 def test_select_edge_lengths():
     """Empty, sub-page, exact-page and tail-only contexts in one ragged batch,
-    with max_pages larger than any request needs."""
-    sp = W.spec("llama8b_128k", batch=8, layers=1, context=(0, 1, 15, 16, 17, 16 * 33, 16 * 257 + 3, 5000))
+    with max_pages larger than any request needs; gamma from one page (1e-6)
+    to just below 1 (0.99999: the cut falls in the flat tail of masses far
+    below the comparison band) and dense."""
+    sp = W.spec("llama8b_128k", batch=8, layers=1, context=(0, 1, 15, 16, 17, 16 * 33, 16 * 257 + 3, 16 * 5000))
     w = W.make_workload(sp, seed=5, device="cuda")
     st = DecodeState(w, max_pages=w.max_pages + 37)
     st.summarize()
-    for gamma in (1e-6, 0.5, 0.99, 1.0):
+    for gamma in (1e-6, 0.5, 0.99, 0.99999, 1.0):
         _check_layer(w, st, 0, float(np.float32(gamma)))
 
 

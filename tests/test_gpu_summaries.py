@@ -1,13 +1,16 @@
 """The page-summary kernel's exact sums, through the C ABI, against the oracle.
 
-The kernel forms each dimension's sum of a page's 16 bf16 keys with 64-bit
-integer adds of the keys' significands when their exponents span at most 40
-(every partial sum then fits 53 bits, so the oracle's fp64 sum in token
-order is exact and equal), and with fp64 adds in token order otherwise.
-This pool is built so that both paths, and their edge, are taken: spreads of
-0 to 120 bits across dimensions, zeros of both signs, subnormals, exact
-cancellation, infinities, NaN and the largest finite keys.  Every summary in
-every format must match the oracle's bit for bit.
+The kernel forms each dimension's sum of a page's 16 bf16 keys in fp32 when
+the keys are normal, below 2^124 and their exponents span at most 12 (every
+partial sum then fits 24 bits), with 64-bit integer adds of the keys'
+significands when the exponents span at most 40 (every partial sum fits 53
+bits), and with fp64 adds in token order otherwise; in each case the
+oracle's fp64 sum in token order is exact and equal.  This pool is built so
+that every path, and each edge between them, is taken: spreads of 0 to 120
+bits across dimensions, zeros of both signs, subnormals, means that round to
+subnormals from normal keys, exact cancellation, infinities, NaN, keys just
+below and at the fp32 limit of 16 summed keys, and the largest finite keys.
+Every summary in every format must match the oracle's bit for bit.
 """
 import numpy as np
 import pytest
@@ -68,6 +71,16 @@ def _pool():
     ext[:, 1, :] = 0x0001                                                # 2^-133
     ext[:, 2:, :] = _bits(rng.standard_normal((HKV, S - 2, D)).astype(np.float32))
     pages.append(ext)
+    # 16 keys of one sign at exponent field 250 (the fp32 sum stays finite) and
+    # 251 (it would not), per head and dimension a random significand
+    for e in (250, 251):
+        lim = np.uint16(e << 7) | rng.integers(0, 128, (HKV, S, D)).astype(np.uint16)
+        lim[:, :, D // 2:] |= np.uint16(0x8000)
+        pages.append(lim)
+    # the smallest normal exponents: means below 2^-126 round to bf16 subnormals
+    tiny = (rng.integers(1, 8, (HKV, S, D)) << 7 | rng.integers(0, 128, (HKV, S, D))).astype(np.uint16)
+    tiny[:, 1::2, :] ^= np.uint16(0x8000)
+    pages.append(tiny)
     return np.stack(pages)                                               # [P][Hkv][S][d]
 
 
