@@ -47,9 +47,9 @@ FALLBACK_HBM_GBS = 6800.0
 # (below 64 lists and from 64 lists on).  The digest names the kernel sources
 # the captures were taken on; once they change the figure is withheld
 # (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "",
+ATTEND_TRAFFIC = {"sources_sha256": "d83c55d101d12d6142ee72baaf0dfc62cf7bda5f85b1a180a9700ab4880e5b34",
                   "many_lists_from": 64,
-                  "dram_bytes_per_entry": {"fused": None, "few_lists": None, "many_lists": None}}
+                  "dram_bytes_per_entry": {"fused": None, "few_lists": 8244.8, "many_lists": 8217.0}}
 ATTEND_SOURCES = ("attend_core.cuh", "attend.cu", "fused.cu", "select_core.cuh", "moira_device.cuh")
 
 # The other configurations reported next to the headline (γ = 0.99 each).
