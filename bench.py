@@ -50,7 +50,7 @@ FALLBACK_HBM_GBS = 6800.0
 ATTEND_TRAFFIC = {"sources_sha256": "d83c55d101d12d6142ee72baaf0dfc62cf7bda5f85b1a180a9700ab4880e5b34",
                   "many_lists_from": 64,
                   "dram_bytes_per_entry": {"fused": None, "few_lists": 8244.8, "many_lists": 8217.0}}
-ATTEND_SOURCES = ("attend_core.cuh", "attend.cu", "fused.cu", "select_core.cuh", "moira_device.cuh")
+ATTEND_SOURCES = ("attend_core.cuh", "attend.cu", "moira_device.cuh", "moira_launch.h")   # k_attend's own
 
 # The other configurations reported next to the headline (γ = 0.99 each).
 OTHER_WORKLOADS = ("llama8b_32k", "serving_ragged", "stress_regimes")

@@ -207,8 +207,6 @@ moira_status select_attend_impl(const moira_shape *shape, int32_t fmt, const voi
     f.weights = scores;
     f.chunks = chunks;
     f.page_table = page_table;
-    f.k_pool = static_cast<const uint8_t *>(k_pool);
-    f.v_pool = static_cast<const uint8_t *>(v_pool);
     f.lists = lists;
     f.lengths = lengths;
     f.bars = reinterpret_cast<uint32_t *>(w + L.fbars);

@@ -116,16 +116,6 @@ __device__ __forceinline__ void request_pages(int L, int mp, int &F, int &tail)
     tail = L % kPageSize;
 }
 
-// L2 prefetch of the K and V blocks (4 KB each) of physical page `pid`, KV
-// head j; ids outside the pool are skipped (the attention flags them).
-__device__ __forceinline__ void prefetch_page(const FusedArgs &f, int pid, int j)
-{
-    if (pid < 0 || pid >= f.at.num_pages) return;
-    const size_t off = (static_cast<size_t>(pid) * f.at.hkv + j) * kSlotBytes / 2;
-    prefetch_l2(f.k_pool + off, kSlotBytes / 2);
-    prefetch_l2(f.v_pool + off, kSlotBytes / 2);
-}
-
 template <int kSlots, int kConsumerWarps>
 __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, kBlocksPerSm)
     k_select_attend(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -202,7 +192,6 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, kBlocksPerSm)
     }
     const unsigned long long target = f.target;
     const int p4 = P0 + 4 * tid;                   // this thread's 4 pages of the run
-    const uint32_t likely = __float_as_uint(F > 0 ? 1.f / static_cast<float>(F) : 1.f);
 
     if (selb) {
         // ---- 1. normalisers, own masses, level-1 histogram ------------------
@@ -282,12 +271,6 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, kBlocksPerSm)
             xs[3] = page_mass_bits(w[0].w, w[1].w, w[2].w, w[3].w, fc);
             *reinterpret_cast<uint4 *>(f.mass + static_cast<size_t>(u) * f.ld + p4) =
                 make_uint4(xs[0], xs[1], xs[2], xs[3]);
-            // HBM is otherwise idle until the attention starts: bring the K and V
-            // of the pages that will very likely be kept (mass at least the
-            // average 1/F) into L2 now
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (p4 + i < P1 && xs[i] >= likely) prefetch_page(f, pref[i], j);
         }
         // masses below 2^-32 are 0 in fixed point and add nothing
 #pragma unroll
@@ -475,7 +458,6 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, kBlocksPerSm)
             if (g || (e && eb < need)) {
                 badp |= pref[i] < 0 || pref[i] >= a.num_pages;
                 out[gb + min(eb, need)] = pref[i];
-                if (s_mass[p4 + i] < likely) prefetch_page(f, pref[i], j);    // not brought in yet
             }
             gb += g;
             eb += e;

@@ -327,16 +327,6 @@ __device__ __forceinline__ bool group_barrier(uint32_t *bar, uint32_t n_blocks, 
     return !guard_failed(g);
 }
 
-// ---- L2 prefetch -----------------------------------------------------------------------
-// Bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2
-// without waiting for them.
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
-                 "r"(bytes)
-                 : "memory");
-}
-
 // ---- shared-memory histograms ------------------------------------------------------
 // hist[bin] += v for the active lanes.  When all active lanes of the warp hit
 // the same bin (a flat mass distribution sends whole warps to one bin) their

@@ -76,8 +76,6 @@ struct FusedArgs {
     const float *weights;          // k_score's chunk-relative weights
     const float *chunks;           // k_score's per-chunk (max, sum)
     const int32_t *page_table;
-    const uint8_t *k_pool;         // this layer's pools (raw), for L2 prefetches
-    const uint8_t *v_pool;
     int32_t *lists;                // out
     int32_t *lengths;              // out
     uint32_t *bars;                // [kFusedMaxUnits + 1][kBarWords]
