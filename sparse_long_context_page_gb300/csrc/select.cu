@@ -247,12 +247,13 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
         mbar_fence_init();
         guard_init(wg);
     }
-    // q, the summaries and the score buffers follow earlier kernels, so they
-    // are touched only after the wait.  With `early`, the launch follows a
-    // kernel of this library in the same step (which never writes the page
-    // table or the lengths), and the plan and the first page ids are read
-    // before it.  Every thread triggers its dependents after its own wait:
-    // k_select relies on that.
+    // q and the score buffers follow earlier kernels, so they are touched only
+    // after the wait.  With `early`, the launch follows this library's
+    // attention kernel in the same step (which writes neither the page table,
+    // the lengths nor the summaries, all of which the step's first scoring
+    // launch has waited for), so the plan, the page ids and the first items'
+    // summary copies go out before it.  Every thread triggers its dependents
+    // after its own wait: k_select relies on that.
     if (!early) {
         pdl_wait();
         pdl_trigger();
@@ -305,10 +306,12 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
         int phys = c.chunk * kScoreChunk + lane < max_pages
                        ? __ldg(page_table + static_cast<size_t>(c.r) * max_pages + c.chunk * kScoreChunk + lane)
                        : -1;
-        if (early) {
-            pdl_wait();
-            pdl_trigger();
-        }
+        // With `early`, the summaries are read before the wait too: the kernel
+        // before this one is the previous layer's attention, which writes no
+        // summaries, so the copies of the first ring's worth of items land
+        // while it finishes.  The producer waits (and only then triggers the
+        // dependents) once the ring is full or its items are issued.
+        bool waited = !early;
         for (int g = g0; g < g1; ++g) {
             // next item's page ids and length, requested before this item's copies
             ScoreCursor n = c;
@@ -343,6 +346,15 @@ __global__ void __launch_bounds__(kScoreThreads, kPersistent ? 3 : 4) k_score(
             c = n;
             L = L_n;
             phys = phys_n;
+            if (!waited && (g - g0 + 1 == stages || g + 1 == g1)) {
+                pdl_wait();
+                pdl_trigger();
+                waited = true;
+            }
+        }
+        if (!waited) {                        // the items ran out early (single wave)
+            pdl_wait();
+            pdl_trigger();
         }
         return;
     }
