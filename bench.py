@@ -47,9 +47,9 @@ FALLBACK_HBM_GBS = 6800.0
 # (below 64 lists and from 64 lists on).  The digest names the kernel sources
 # the captures were taken on; once they change the figure is withheld
 # (traffic = null).
-ATTEND_TRAFFIC = {"sources_sha256": "d83c55d101d12d6142ee72baaf0dfc62cf7bda5f85b1a180a9700ab4880e5b34",
+ATTEND_TRAFFIC = {"sources_sha256": "cf6c687decfdee847080b0cef60c1f1b6096cbfc9be413b50610ebb1895d5c1c",
                   "many_lists_from": 64,
-                  "dram_bytes_per_entry": {"fused": None, "few_lists": 8244.8, "many_lists": 8217.0}}
+                  "dram_bytes_per_entry": {"fused": None, "few_lists": 8240.6, "many_lists": 8217.2}}
 ATTEND_SOURCES = ("attend_core.cuh", "attend.cu", "moira_device.cuh", "moira_launch.h")   # k_attend's own
 
 # The other configurations reported next to the headline (γ = 0.99 each).
