@@ -39,17 +39,16 @@ sys.path.insert(0, ROOT)
 METRIC = "µs/decode-attn step & achieved HBM GB/s at 128k ctx, γ=0.99 vs γ=1 dense"
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) that the attention kernels move per list entry,
+# DRAM bytes (read + write) that the attention kernel moves per list entry,
 # i.e. per kept (page, KV head) with its 4 KB of K and 4 KB of V, from
 # one-pass ncu captures of dense launches (dram__bytes_read.sum +
-# dram__bytes_write.sum divided by the entries): the single-launch selection +
-# attention of small batches (k_select_attend) and k_attend's two block shapes
-# (below 64 lists and from 64 lists on).  The digest names the kernel sources
-# the captures were taken on; once they change the figure is withheld
+# dram__bytes_write.sum divided by the entries), for k_attend's two block
+# shapes (below 64 lists and from 64 lists on).  The digest names the kernel
+# sources the captures were taken on; once they change the figure is withheld
 # (traffic = null).
 ATTEND_TRAFFIC = {"sources_sha256": "cf6c687decfdee847080b0cef60c1f1b6096cbfc9be413b50610ebb1895d5c1c",
                   "many_lists_from": 64,
-                  "dram_bytes_per_entry": {"fused": None, "few_lists": 8240.6, "many_lists": 8217.2}}
+                  "dram_bytes_per_entry": {"few_lists": 8240.6, "many_lists": 8217.2}}
 ATTEND_SOURCES = ("attend_core.cuh", "attend.cu", "moira_device.cuh", "moira_launch.h")   # k_attend's own
 
 # The other configurations reported next to the headline (γ = 0.99 each).
@@ -320,35 +319,27 @@ def time_score(st, steps, warmup):
     return ms / st.layers
 
 
-def kernel_roofline(st, w, head, lengths, spb, step_ms, peak, steps, warmup, two_launch=None):
-    """The step's dominant kernel, its algorithmic bytes per launch (K and V
-    of the kept tokens, q, out) and its average in-graph launch duration.
-    Small batches run k_score then k_select_attend per layer: the latter's
-    duration is the step's per-layer time less the scoring kernel's (both
-    CUDA-event timed graphs).  Larger batches run k_score, k_select and
-    k_attend: k_attend's duration is timed in a graph of attention launches
-    alone (two_launch = time_parts' result)."""
-    import sparse_long_context_page_gb300 as moira
+def kernel_roofline(st, w, head, lengths, spb, peak, steps, warmup, two_launch=None):
+    """The step's dominant kernel (k_attend: the decode step runs k_score,
+    k_select and k_attend per layer), its algorithmic bytes per launch (K and
+    V of the kept tokens, q, out) and its average in-graph launch duration,
+    timed in a graph of attention launches alone (two_launch = time_parts'
+    result)."""
     sp = w.spec
     per_layer, _, _, parts = step_bytes(w, lengths, head, spb)
     att_bytes = per_layer - parts["summaries"] / sp.layers      # K/V of kept tokens + q + out
     entries = float(lengths.reshape(sp.layers, -1).sum(axis=1).mean())     # list entries per launch
-    fused = False          # the decode step runs k_score, k_select, k_attend per layer
     score_ms = time_score(st, steps, warmup)
-    if fused:
-        kernel, dur_ms, shape = "k_select_attend", step_ms / sp.layers - score_ms, "fused"
-    else:
-        if two_launch is None:
-            two_launch = time_parts(st, head, steps, warmup)
-        kernel, dur_ms = "k_attend", two_launch[1]
-        shape = "many_lists" if sp.batch * sp.kv_heads >= ATTEND_TRAFFIC["many_lists_from"] else "few_lists"
+    if two_launch is None:
+        two_launch = time_parts(st, head, steps, warmup)
+    kernel, dur_ms = "k_attend", two_launch[1]
+    shape = "many_lists" if sp.batch * sp.kv_heads >= ATTEND_TRAFFIC["many_lists_from"] else "few_lists"
     gbs = float(att_bytes.mean() / (dur_ms * 1e6))
     per_entry = ATTEND_TRAFFIC["dram_bytes_per_entry"].get(shape)
     traffic = None
     if per_entry and ATTEND_TRAFFIC["sources_sha256"] == attend_sources_digest():
         traffic = int(round(per_entry * entries))
-    how = ("step per layer less the scoring kernel per layer (two CUDA-event timed graphs)" if fused
-           else "graph of the layers' attention launches alone, CUDA events")
+    how = "graph of the layers' attention launches alone, CUDA events"
     return {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1), "peak": peak[0], "unit": "GB/s",
             "frac": round(gbs / peak[0], 4), "peak_source": peak[1], "traffic": traffic,
             "traffic_how": (f"ncu DRAM bytes per list entry of a dense launch of the same kernel "
@@ -356,7 +347,24 @@ def kernel_roofline(st, w, head, lengths, spb, step_ms, peak, steps, warmup, two
                             "null: no ncu capture of the current attention sources"),
             "entries_per_launch": round(entries, 1), "bytes_per_launch": int(att_bytes.mean()),
             "duration_us": round(dur_ms * 1e3, 2), "duration_how": how,
-            "score_us_per_layer": round(score_ms * 1e3, 2)}, fused
+            "score_us_per_layer": round(score_ms * 1e3, 2)}
+
+
+def time_single_launch(st, gamma, steps, warmup):
+    """Per-layer duration of moira_select_attend when it takes its one-launch
+    form for this batch (k_score, then k_select_attend), else None: the
+    layers' calls captured in one CUDA graph, CUDA events.  A comparison
+    only: the decode step runs three launches per layer."""
+    import sparse_long_context_page_gb300 as moira
+    if not moira.select_attend_is_fused(st.shape, st.batch, st.max_pages):
+        return None
+    lists = torch.zeros_like(st.lists)
+    out = torch.zeros_like(st.out)
+    g = capture_fn(lambda: [st.select_attend_layer(l, gamma, lists, st.lengths[l], out[l])
+                            for l in range(st.layers)])
+    ms, _ = time_graph(g, steps, warmup, 1)
+    del g
+    return ms / st.layers
 
 
 def load_balance(st, w, gamma):
@@ -420,14 +428,14 @@ def other_workload(name, args, peak, local):
     assert moira.read_device_status(st.ws) == 0, f"device status word set during {name}"
     lengths = st.lengths.cpu().numpy()          # the gamma = 0.99 step ran last
     _, total, frac, _ = step_bytes(w, lengths, head, spb)
-    roof, fused = kernel_roofline(st, w, head, lengths, spb, out[head], peak, steps, args.warmup)
+    roof = kernel_roofline(st, w, head, lengths, spb, peak, steps, args.warmup)
     res = {"workload": f"{name}: {w.spec.batch} request(s), {int(w.seq_lens.min())}..{int(w.seq_lens.max())} "
                        f"tokens, {w.spec.layers} layer(s), 32 q / 8 kv heads",
            "us_per_step": round(out[head] * 1e3, 2), "dense_us_per_step": round(out[1.0] * 1e3, 2),
            "speedup_vs_dense": round(out[1.0] / out[head], 3), "pages_read_fraction": round(frac, 4),
            "step_hbm_gbs": round(total / out[head] / 1e6, 1),
            "step_hbm_frac_of_measured": round(total / out[head] / 1e6 / peak[0], 4),
-           "single_launch_select_attend": bool(fused), "roofline": roof,
+           "roofline": roof,
            "load_balance": load_balance(st, w, head)}
     log(f"[bench] {name}: generated in {gen_s:.1f}s; {out[head] * 1e3:.1f} us/step "
         f"({res['step_hbm_frac_of_measured']:.3f} of peak), dense {out[1.0] * 1e3:.1f}, "
@@ -591,9 +599,10 @@ def run_ours(args):
 
     # dominant kernel and the layer's split (in-graph, CUDA events)
     two = time_parts(st, head, max(3, args.steps // 2), args.warmup)
-    roof, fused = kernel_roofline(st, w, head, results[head]["lengths"], spb, results[head]["ms"],
-                                  (peak, peak_src), max(3, args.steps // 2), args.warmup, two_launch=two)
+    roof = kernel_roofline(st, w, head, results[head]["lengths"], spb, (peak, peak_src),
+                           max(3, args.steps // 2), args.warmup, two_launch=two)
     sel_ms, att_ms = two
+    single_ms = time_single_launch(st, head, max(3, args.steps // 2), args.warmup)
     balance = load_balance(st, w, head)
 
     # the same step under the fixed-budget and relative-threshold rules, tuned
@@ -652,7 +661,7 @@ def run_ours(args):
 
     hd = results[head]
     dense = results[1.0]
-    launches_per_step = sp.layers * (2 if fused else 3)
+    launches_per_step = sp.layers * 3          # k_score, k_select, k_attend per layer
 
     line = {
         "metric": METRIC,
@@ -683,12 +692,12 @@ def run_ours(args):
                        "speedup_vs_dense": round(dense["ms"] / results[gammas[1]]["ms"], 3)},
         "per_layer_us": {"step": round(hd["ms"] * 1e3 / sp.layers, 2),
                          "score": roof["score_us_per_layer"],
-                         "select_attend": roof["duration_us"] if fused else None,
-                         "two_launch_select": round(sel_ms * 1e3, 2), "two_launch_attend": round(att_ms * 1e3, 2),
+                         "select": round(sel_ms * 1e3, 2), "attend": round(att_ms * 1e3, 2),
+                         "single_launch_layer": round(single_ms * 1e3, 2) if single_ms is not None else None,
                          "how": "in-graph, CUDA events: the step graph; graphs of the layers' scoring "
-                                "launches alone; and, for comparison, the two-launch form (score + "
-                                "k_select, then k_attend) timed half by half"},
-        "single_launch_select_attend": bool(fused),
+                                "launches alone; of their selections (k_score + k_select) and of their "
+                                "attentions (k_attend) alone; and, for comparison, moira_select_attend's "
+                                "one-launch form per layer where the batch takes it (not used by the step)"},
         "roofline": roof,
         "load_balance": balance,
         "summaries_kernel": summ_kernel,

@@ -57,4 +57,4 @@ def test_traffic_shape_threshold_matches_the_kernel():
     m = re.search(r"constexpr int kManyUnits = (\d+);", src)
     assert m, "kManyUnits not found in attend_core.cuh"
     assert int(m.group(1)) == bench.ATTEND_TRAFFIC["many_lists_from"]
-    assert set(bench.ATTEND_TRAFFIC["dram_bytes_per_entry"]) == {"fused", "few_lists", "many_lists"}
+    assert set(bench.ATTEND_TRAFFIC["dram_bytes_per_entry"]) == {"few_lists", "many_lists"}
