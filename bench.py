@@ -350,6 +350,23 @@ def kernel_roofline(st, w, head, lengths, spb, peak, steps, warmup, two_launch=N
             "score_us_per_layer": round(score_ms * 1e3, 2)}
 
 
+def time_clustered_select(st, gamma, steps, warmup):
+    """Per-layer duration of moira_select_clustered (the score and the cut in
+    one launch, a thread-block cluster per list) where the batch fits the
+    device's clusters, else None: the layers' calls captured in one CUDA
+    graph, CUDA events.  A comparison only: the step selects with k_score +
+    k_select."""
+    import sparse_long_context_page_gb300 as moira
+    if st.fmt != moira.SUMM_BF16 or not moira.select_cluster_size(st.shape, st.batch, st.max_pages):
+        return None
+    lists = torch.zeros_like(st.lists)
+    lengths = torch.zeros_like(st.lengths)
+    g = capture_fn(lambda: [st.select_layer_clustered(l, gamma, lists, lengths[l]) for l in range(st.layers)])
+    ms, _ = time_graph(g, steps, warmup, 1)
+    del g
+    return ms / st.layers
+
+
 def time_single_launch(st, gamma, steps, warmup):
     """Per-layer duration of moira_select_attend when it takes its one-launch
     form for this batch (k_score, then k_select_attend), else None: the
@@ -603,6 +620,7 @@ def run_ours(args):
                            max(3, args.steps // 2), args.warmup, two_launch=two)
     sel_ms, att_ms = two
     single_ms = time_single_launch(st, head, max(3, args.steps // 2), args.warmup)
+    clustered_ms = time_clustered_select(st, head, max(3, args.steps // 2), args.warmup)
     balance = load_balance(st, w, head)
 
     # the same step under the fixed-budget and relative-threshold rules, tuned
@@ -694,10 +712,12 @@ def run_ours(args):
                          "score": roof["score_us_per_layer"],
                          "select": round(sel_ms * 1e3, 2), "attend": round(att_ms * 1e3, 2),
                          "single_launch_layer": round(single_ms * 1e3, 2) if single_ms is not None else None,
+                         "clustered_select": round(clustered_ms * 1e3, 2) if clustered_ms is not None else None,
                          "how": "in-graph, CUDA events: the step graph; graphs of the layers' scoring "
                                 "launches alone; of their selections (k_score + k_select) and of their "
-                                "attentions (k_attend) alone; and, for comparison, moira_select_attend's "
-                                "one-launch form per layer where the batch takes it (not used by the step)"},
+                                "attentions (k_attend) alone; and, for comparison (neither is used by the "
+                                "step), moira_select_attend's one-launch layer and moira_select_clustered's "
+                                "one-launch selection where the batch takes them"},
         "roofline": roof,
         "load_balance": balance,
         "summaries_kernel": summ_kernel,

@@ -323,9 +323,31 @@ MOIRA_API moira_status moira_score_ex(const moira_shape *shape, int32_t format, 
                             int32_t max_pages, float sm_scale, void *workspace, size_t ws_bytes,
                             moira_stream_t stream);
 
-/* 1 if moira_select_attend (and the coverage-rule decode step) takes the
- * single-launch form for these sizes on the current device, 0 if it runs
- * moira_select then moira_attend (or the arguments are invalid). */
+/* The coverage selection of moira_select in one launch, one thread-block
+ * cluster of 16 or 8 blocks per list, the blocks exchanging the chunk
+ * statistics, histogram slices, candidates and kept counts through
+ * distributed shared memory (NEXT-1's score + select fusion).  Same
+ * arguments, results and errors as moira_select, whose lists and lengths it
+ * gives bit for bit; it is slower on GB300 at batch 1 (21 against 15 us per
+ * 128k layer), so neither moira_select nor the decode step uses it.  Returns
+ * MOIRA_EUNSUPPORTED, launching nothing, when the device cannot hold every
+ * list's cluster at once or max_pages needs more than two rounds of chunks
+ * per block (moira_select_cluster_size).  gamma >= 1 runs moira_select's
+ * dense path. */
+MOIRA_API moira_status moira_select_clustered(const moira_shape *shape, const void *q, const void *summ,
+                                    const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                                    int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
+                                    int32_t *lengths, void *workspace, size_t ws_bytes, moira_stream_t stream);
+
+/* The cluster size (16 or 8) moira_select_clustered takes for these sizes on
+ * the current device, or 0 when it returns MOIRA_EUNSUPPORTED (or the
+ * arguments are invalid). */
+MOIRA_API int32_t moira_select_cluster_size(const moira_shape *shape, int32_t batch, int32_t max_pages);
+
+/* 1 if moira_select_attend takes the single-launch form for these sizes on
+ * the current device, 0 if it runs moira_select then moira_attend (or the
+ * arguments are invalid).  The decode step always runs moira_select then
+ * moira_attend per layer. */
 MOIRA_API int32_t moira_select_attend_is_fused(const moira_shape *shape, int32_t batch, int32_t max_pages);
 
 /* One whole decode-attention step: for layer l = 0 .. num_layers-1,

@@ -13,13 +13,14 @@ from ._binding import (DEV_BADLEN, DEV_BADPAGE, DEV_TIMEOUT, EXPORTS, GROUP, HEA
                        RULE_TOPK, SUMM_BF16, SUMM_Q2, SUMM_Q8, MoiraError, Shape, append_kv, attend,
                        attend_grid_blocks, decode_step, decode_step_ex, decode_step_host,
                        library_path, load_library, make_summaries, make_workspace,
-                       read_device_status, select, select_attend, select_attend_is_fused, select_ex, select_rule, shape_of,
-                       summary_page_bytes, update_summaries, workspace_bytes, workspace_init)
+                       read_device_status, select, select_attend, select_attend_is_fused, select_cluster_size,
+                       select_clustered, select_ex, select_rule, shape_of, summary_page_bytes, update_summaries, workspace_bytes, workspace_init)
 
 __all__ = ["DEV_BADLEN", "DEV_BADPAGE", "DEV_TIMEOUT", "EXPORTS", "GROUP", "HEAD_DIM",
            "MAX_PAGES_PER_SEQ", "MAX_UNITS", "PAGE_SIZE", "RULE_COVERAGE", "RULE_TOPDELTA",
            "RULE_TOPK", "SUMM_BF16", "SUMM_Q2", "SUMM_Q8", "MoiraError", "Shape", "append_kv",
            "attend", "attend_grid_blocks", "decode_step", "decode_step_ex", "decode_step_host",
            "library_path", "load_library", "make_summaries", "make_workspace",
-           "read_device_status", "select", "select_attend", "select_attend_is_fused", "select_ex", "select_rule", "shape_of",
+           "read_device_status", "select", "select_attend", "select_attend_is_fused", "select_cluster_size",
+           "select_clustered", "select_ex", "select_rule", "shape_of",
            "summary_page_bytes", "update_summaries", "workspace_bytes", "workspace_init"]

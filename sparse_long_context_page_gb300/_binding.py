@@ -35,7 +35,8 @@ EXPORTS = ("moira_workspace_bytes", "moira_workspace_init", "moira_update_summar
            "moira_select_noalloc", "moira_select_rule", "moira_append_kv",
            "moira_diag_wait_timeout", "moira_summary_page_bytes", "moira_update_summaries_ex",
            "moira_append_kv_ex", "moira_select_ex", "moira_decode_step_ex", "moira_select_attend",
-           "moira_select_attend_ex", "moira_select_attend_is_fused", "moira_score_ex", "moira_diag_wait_chain", "moira_diag_barrier_timeout")
+           "moira_select_attend_ex", "moira_select_attend_is_fused", "moira_score_ex", "moira_diag_wait_chain",
+           "moira_diag_barrier_timeout", "moira_select_clustered", "moira_select_cluster_size")
 
 # page rules of moira_select_rule (moira_rule in include/moira.h)
 RULE_COVERAGE, RULE_TOPK, RULE_TOPDELTA = 0, 1, 2
@@ -153,6 +154,10 @@ def _declare(lib):
     lib.moira_score_ex.restype = ctypes.c_int
     lib.moira_select_attend_is_fused.argtypes = [sp, _i32, _i32]
     lib.moira_select_attend_is_fused.restype = _i32
+    lib.moira_select_clustered.argtypes = lib.moira_select.argtypes
+    lib.moira_select_clustered.restype = ctypes.c_int
+    lib.moira_select_cluster_size.argtypes = [sp, _i32, _i32]
+    lib.moira_select_cluster_size.restype = _i32
     lib.moira_diag_wait_chain.argtypes = [_vp, ctypes.c_size_t, ctypes.c_uint64, _i32, _vp]
     lib.moira_diag_wait_chain.restype = ctypes.c_int
     lib.moira_diag_barrier_timeout.argtypes = [_vp, ctypes.c_size_t, ctypes.c_uint64, _i32, _vp]
@@ -282,6 +287,27 @@ def select(shape: Shape, q, summ, page_table, seq_lens, gamma: float, sm_scale: 
                             float(gamma), float(sm_scale), _dev(lists, "lists", torch.int32),
                             _dev(lengths, "lengths", torch.int32), _dev(ws, "workspace", torch.uint8),
                             ws.numel(), _stream(stream)), "moira_select")
+
+
+def select_clustered(shape: Shape, q, summ, page_table, seq_lens, gamma: float, sm_scale: float, lists,
+                     lengths, ws, stream=None):
+    """moira_select in its one-launch cluster form (moira_select_clustered):
+    the same lists and lengths; raises MoiraError(MOIRA_EUNSUPPORTED) when the
+    batch does not fit the device's clusters."""
+    lib = load_library()
+    batch, max_pages = page_table.shape
+    _check(lib.moira_select_clustered(ctypes.byref(shape), _dev(q, "q", torch.bfloat16),
+                                      _dev(summ, "summ", torch.bfloat16),
+                                      _dev(page_table, "page_table", torch.int32, 2),
+                                      _dev(seq_lens, "seq_lens", torch.int32, 1), batch, max_pages,
+                                      float(gamma), float(sm_scale), _dev(lists, "lists", torch.int32),
+                                      _dev(lengths, "lengths", torch.int32), _dev(ws, "workspace", torch.uint8),
+                                      ws.numel(), _stream(stream)), "moira_select_clustered")
+
+
+def select_cluster_size(shape: Shape, batch: int, max_pages: int) -> int:
+    """Cluster size (16 or 8) of moira_select_clustered for these sizes, 0 if unsupported."""
+    return int(load_library().moira_select_cluster_size(ctypes.byref(shape), int(batch), int(max_pages)))
 
 
 def select_rule(shape: Shape, q, summ, page_table, seq_lens, rule: int, param: float,

@@ -414,6 +414,36 @@ moira_status moira_select_rule(const moira_shape *shape, const void *q, const vo
                            rule, param, sm_scale, lists, lengths, workspace, ws_bytes, stream);
 }
 
+moira_status moira_select_clustered(const moira_shape *shape, const void *q, const void *summ,
+                                    const int32_t *page_table, const int32_t *seq_lens, int32_t batch,
+                                    int32_t max_pages, float gamma, float sm_scale, int32_t *lists,
+                                    int32_t *lengths, void *workspace, size_t ws_bytes, moira_stream_t stream)
+{
+    moira_status st = check_select_args(shape, MOIRA_SUMM_BF16, q, summ, page_table, seq_lens, batch, max_pages,
+                                        MOIRA_RULE_COVERAGE, gamma, sm_scale, lists, lengths);
+    if (st != MOIRA_OK) return st;
+    if ((st = check_ws(shape, batch, max_pages, workspace, ws_bytes)) != MOIRA_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (gamma >= 1.0f)                                   // dense: no estimate, as moira_select
+        return select_impl(shape, MOIRA_SUMM_BF16, q, summ, page_table, seq_lens, batch, max_pages,
+                           MOIRA_RULE_COVERAGE, gamma, sm_scale, lists, lengths, workspace, ws_bytes, false, s);
+    const int C = cover_cluster_size(batch * shape->num_kv_heads, max_pages);
+    if (C == 0) return MOIRA_EUNSUPPORTED;
+    const WsLayout L = layout_for(shape, batch, max_pages);
+    uint32_t *status = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(workspace) + L.status);
+    const float scale_log2 = static_cast<float>(static_cast<double>(sm_scale) * 1.4426950408889634);
+    const unsigned long long gfx = static_cast<unsigned long long>(std::ceil(static_cast<double>(gamma) * 0x1p31));
+    return cuda_status(launch_cover(q, summ, page_table, seq_lens, batch, shape->num_q_heads, shape->num_kv_heads,
+                                    max_pages, shape->num_phys_pages, scale_log2, gfx, false, lists, lengths,
+                                    status, C, s));
+}
+
+int32_t moira_select_cluster_size(const moira_shape *shape, int32_t batch, int32_t max_pages)
+{
+    if (check_shape(shape) != MOIRA_OK || check_batch(shape, batch, max_pages) != MOIRA_OK) return 0;
+    return cover_cluster_size(batch * shape->num_kv_heads, max_pages);
+}
+
 moira_status moira_attend(const moira_shape *shape, const void *q, const void *k_pool,
                           const void *v_pool, const int32_t *lists, const int32_t *lengths,
                           const int32_t *seq_lens, int32_t batch, int32_t max_pages,

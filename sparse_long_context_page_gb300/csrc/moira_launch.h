@@ -89,6 +89,17 @@ struct FusedArgs {
 // Whether k_select_attend takes `units` lists of at most `max_pages` pages on
 // a grid of `blocks` (and fits 2 blocks per SM on the current device).
 bool select_attend_fits(int units, int max_pages, int blocks);
+
+// The coverage selection in one launch, one thread-block cluster per list
+// (k_cover, cover.cu): the cluster size a launch of `units` lists takes (16
+// or 8), or 0 when the device cannot hold every list's cluster at once or
+// max_pages needs more than two rounds of chunks per block; then the launch
+// itself (bf16 summaries; target = gamma on the 2^-31 grid, rounded up).
+int cover_cluster_size(int units, int max_pages);
+cudaError_t launch_cover(const void *q, const void *summ, const int32_t *page_table, const int32_t *seq_lens,
+                         int batch, int hq, int hkv, int max_pages, long long num_pages, float scale_log2,
+                         unsigned long long target, bool early, int32_t *lists, int32_t *lengths,
+                         uint32_t *status, int C, cudaStream_t stream);
 cudaError_t launch_select_attend(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
                                  const FusedArgs &args, int blocks, cudaStream_t stream);
 

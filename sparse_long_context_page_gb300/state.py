@@ -71,6 +71,14 @@ class DecodeState:
                          self.seq_lens, mb.RULE_COVERAGE, gamma, self.sm_scale, lists, lengths, self.ws)
         return lists, lengths
 
+    def select_layer_clustered(self, l: int, gamma: float, lists=None, lengths=None):
+        """moira_select_clustered on layer l (bf16 summaries only)."""
+        lists = self.lists if lists is None else lists
+        lengths = self.lengths[l] if lengths is None else lengths
+        mb.select_clustered(self.shape, self.w.q[l], self.summ[l], self.page_table, self.seq_lens, gamma,
+                            self.sm_scale, lists, lengths, self.ws)
+        return lists, lengths
+
     def select_layer_rule(self, l: int, rule: int, param: float, lists=None, lengths=None):
         lists = self.lists if lists is None else lists
         lengths = self.lengths[l] if lengths is None else lengths
