@@ -441,11 +441,12 @@ __device__ __forceinline__ void attend_consume(AttendSmem<kSlots, kConsumerWarps
     }
     load_q(u);
 
-    // The first segment's list may continue in earlier blocks and, when more
-    // segments follow, its arrival is taken at once but resolved after the
-    // block's last segment, so the ring keeps streaming meanwhile.
+    // The first segment's list may continue in earlier blocks.  When more
+    // segments follow, its partial is written at once but its arrival (an
+    // acq_rel atomic, whose release half waits for the partial to reach L2)
+    // and its merges wait for the block's last segment, so the consumer warps
+    // go straight on to the next list.
     int pend_u = -1;
-    uint32_t pend_prev = 0u;
 
     while (true) {
         const long long seg_lo = max(g0, static_cast<long long>(s_off[u]));
@@ -455,6 +456,15 @@ __device__ __forceinline__ void attend_consume(AttendSmem<kSlots, kConsumerWarps
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) D[mt][0] = D[mt][1] = D[mt][2] = D[mt][3] = 0.f;
 
+        // the next list's q rows (4 heads x 256 B) towards L2 while this segment streams
+        if (seg_hi < g1 && warp == 0 && lane < 8) {
+            int un = u + 1;
+            while (s_off[un + 1] == s_off[un]) ++un;
+            const int r = un / a.hkv, j = un % a.hkv;
+            const char *qn = reinterpret_cast<const char *>(static_cast<const uint16_t *>(a.q) +
+                                                          (static_cast<size_t>(r) * a.hq + j * kGroup) * kHeadDim);
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + lane * 128));
+        }
         const long long first = seg_lo + ((warp - (seg_lo - g0) % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
         for (long long g = first; g < seg_hi; g += kConsumerWarps) {
             const long long idx = g - g0;
@@ -609,15 +619,14 @@ __device__ __forceinline__ void attend_consume(AttendSmem<kSlots, kConsumerWarps
                 part[h] = M;
                 part[kGroup + h] = Lsum;
             }
-            // the CTA barrier makes every thread's partial visible to thread 0,
-            // whose acq_rel atomic publishes it and acquires the others
-            consumer_bar<kConsumerWarps>();
-            uint32_t prev = 0u;
-            if (ls.gn > 1 && tid == 0) prev = atomic_add_acq_rel_gpu(&a.gcounters[ls.gfirst + u], 1u);
-            if (more) {                    // first segment: resolved after the last one
+            if (more) {                    // first segment: arrival and merges after the last one
                 pend_u = u;
-                pend_prev = prev;
             } else {
+                // the CTA barrier makes every thread's partial visible to thread 0,
+                // whose acq_rel atomic publishes it and acquires the others
+                consumer_bar<kConsumerWarps>();
+                uint32_t prev = 0u;
+                if (ls.gn > 1 && tid == 0) prev = atomic_add_acq_rel_gpu(&a.gcounters[ls.gfirst + u], 1u);
                 resolve_list<kConsumerWarps>(a, sm.flag, u, ls, prev, h, d0, mring, wg);
             }
         }
@@ -625,10 +634,13 @@ __device__ __forceinline__ void attend_consume(AttendSmem<kSlots, kConsumerWarps
         if (!more) break;
         u = un;
     }
-    if (pend_u >= 0)
-        resolve_list<kConsumerWarps>(a, sm.flag, pend_u,
-                                     list_split(s_off, pend_u, b, W, n, flat_merge_max<kSlots>()),
-                                     pend_prev, h, d0, mring, wg);
+    if (pend_u >= 0) {
+        // its partial was written before the segment's closing barrier
+        const ListSplit ls = list_split(s_off, pend_u, b, W, n, flat_merge_max<kSlots>());
+        uint32_t prev = 0u;
+        if (ls.gn > 1 && tid == 0) prev = atomic_add_acq_rel_gpu(&a.gcounters[ls.gfirst + pend_u], 1u);
+        resolve_list<kConsumerWarps>(a, sm.flag, pend_u, ls, prev, h, d0, mring, wg);
+    }
 
     // after a give-up, let the copies still in flight land before the block
     // exits (their landing is what the skipped waits were for)
