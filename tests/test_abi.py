@@ -212,3 +212,23 @@ def test_select_noalloc_rejects_what_select_rejects_on_host():
         assert got in (1, 4), (kw, got)
         if not ({"lists", "summ"} & kw.keys()):
             assert got == sel, (kw, got, sel)
+
+
+def test_select_clustered_rejects_what_select_rejects_on_host():
+    """moira_select_clustered shares moira_select's argument checks, and
+    moira_select_cluster_size answers 0 for invalid arguments."""
+    lib = moira.load_library()
+    ok = moira.Shape.of(32, 8, 1024)
+
+    def clustered(shape=ok, q=FAKE, gamma=0.9, sm=0.088, batch=1, max_pages=64):
+        return lib.moira_select_clustered(ctypes.byref(shape), q, FAKE, FAKE, FAKE, batch, max_pages, gamma, sm,
+                                          FAKE, FAKE, FAKE, 1 << 30, None)
+
+    for kw in [dict(gamma=0.0), dict(gamma=1.5), dict(gamma=float("nan")), dict(sm=-1.0), dict(q=0),
+               dict(q=FAKE + 2), dict(batch=0), dict(max_pages=mb.MAX_PAGES_PER_SEQ + 1),
+               dict(shape=moira.Shape.of(32, 8, 1024, head_dim=64)), dict(shape=moira.Shape.of(30, 8, 1024))]:
+        sel = _select(lib, kw.get("shape", ok), gamma=kw.get("gamma", 0.9), sm=kw.get("sm", 0.088),
+                      q=kw.get("q", FAKE), batch=kw.get("batch", 1), max_pages=kw.get("max_pages", 64))
+        assert clustered(**kw) == sel, kw
+    assert lib.moira_select_cluster_size(ctypes.byref(moira.Shape.of(30, 8, 1024)), 1, 64) == 0
+    assert lib.moira_select_cluster_size(ctypes.byref(ok), 0, 64) == 0
